@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the ForwardPass hot path on one GB300 (or N independent
+replicas, one per GPU, under torchrun).
+
+Workload (the decode batch): 64 lanes x 1 row, 32 q / 8 kv heads, head_dim
+128, bf16, 16-slot pages randomly permuted in a 65,536-page pool, cached
+length C ~ U[512, 4096] per lane.  One step is one full pass of the hot path
+for the next token of every lane: plan (host metadata -> device work lists),
+RoPE + slot scatter, split-KV attention + combine + readout, fold (all).
+Step t puts each lane's row at position/slot C+t and reads C+t+1 slots.
+
+Reported (one JSON line on rank 0):
+  value        attended tokens/s (sum over rows of visible slots), inputs
+               resident in HBM, CUDA events around exactly K steps;
+  e2e          the same metric with q/k/v copied from pinned host memory and
+               the readout copied back to the host inside every step;
+  roofline     achieved HBM GB/s of the attention call (algorithmic bytes /
+               measured duration) against the measured copy bandwidth;
+  cpu_baseline the CPU oracle on a bounded sample of the same workload.
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "attended tokens/s; decode HBM GB/s and prefill TFLOP/s as % of GB300 roofline"
+UNIT = "attended tokens/s"
+WORKLOAD = "decode_batch"
+PROFILE = os.path.join(ROOT, "profiles", "attend_decode_batch.md")
+KERNEL_SRC = os.path.join(ROOT, "programmable_paged_kv_gb300", "csrc", "attend_decode.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return ws, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ accounting
+def attended_tokens(p) -> int:
+    """Sum over rows of |visible slots| for a default-visibility pass."""
+    lane = np.repeat(np.arange(p.num_lanes), np.diff(p.row_indptr))
+    kv = p.kv_len[lane].astype(np.int64)
+    return int(np.minimum(kv, p.slots.astype(np.int64) + 1).sum())
+
+
+def attend_alg_bytes(p, desc) -> int:
+    """Algorithmic bytes of one attention call: each distinct visible KV slot
+    read once per kv head (K and V), q_rot read, readout rows written (+lse),
+    page-table entries of the touched pages."""
+    b = W.ELEM_BYTES[desc.dtype]
+    d, hq, hkv = desc.head_dim, desc.num_q_heads, desc.num_kv_heads
+    kv_slots = int(p.kv_len.astype(np.int64).sum())
+    pages = int(sum((int(k) + desc.page_size - 1) // desc.page_size for k in p.kv_len))
+    R = p.num_lanes
+    return (kv_slots * hkv * 2 * d * b + p.num_rows * hq * d * b + R * hq * (d * b + 4)
+            + pages * 4)
+
+
+def step_alg_bytes(p, desc) -> int:
+    b = W.ELEM_BYTES[desc.dtype]
+    d, hq, hkv = desc.head_dim, desc.num_q_heads, desc.num_kv_heads
+    n = p.num_rows
+    append = n * (hq + 2 * hkv) * d * b + n * hq * d * b + n * 2 * hkv * d * b
+    return append + attend_alg_bytes(p, desc)
+
+
+# ------------------------------------------------------------------ peaks / clocks / traffic
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(path))
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pie_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profiled_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    t = re.search(r"dram_bytes_per_attend_call:\s*([0-9]+)", txt)
+    if not m or not t or m.group(1) != src_hash:
+        return None
+    return int(t.group(1))
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_rate(seed: int, seconds: float):
+    import oracle as O
+    sc = W.decode_batch(seed, lanes=64)
+    p = sc.passes[0]
+    cores = os.cpu_count() or 1
+    cp = sc.compact_page_ids(p.page_ids)
+    tok = attended_tokens(p)
+    total, passes = 0.0, 0
+    while total < seconds or passes == 0:
+        k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
+        ts = time.perf_counter()
+        r = O.run_pass(sc.desc, p, k, v, fr, page_ids=cp, num_threads=cores)
+        total += time.perf_counter() - ts
+        assert r["err"] == O.OK
+        passes += 1
+    return tok * passes / total, cores, passes, total
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle as O
+    O.build()
+    sc = W.decode_batch(args.seed, lanes=64)
+    p = sc.passes[0]
+    cp = sc.compact_page_ids(p.page_ids)
+    cores = os.cpu_count() or 1
+    tok = attended_tokens(p)
+    for _ in range(args.warmup):
+        k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
+        O.run_pass(sc.desc, p, k, v, fr, page_ids=cp, num_threads=cores)
+    times = []
+    for _ in range(args.steps):
+        k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
+        ts = time.perf_counter()
+        r = O.run_pass(sc.desc, p, k, v, fr, page_ids=cp, num_threads=cores)
+        times.append(time.perf_counter() - ts)
+        assert r["err"] == O.OK
+    el = sum(times)
+    val = tok * args.steps / el
+    sample = "one full decode-batch pass (64 lanes x 1 row) per step, all host cores"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1,
+                                        "q_heads": 32, "kv_heads": 8, "head_dim": 128,
+                                        "page_size": 16, "kv_len": "C+1, C~U[512,4096]"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, ws, rank, local, pg):
+    import torch
+    from programmable_paged_kv_gb300 import ForwardPlan, build, make_desc, make_meta, runner
+    from programmable_paged_kv_gb300.abi import load
+    torch.cuda.set_device(local)
+    build()
+    load()
+    K, Wm = args.steps, args.warmup
+    total_steps = 2 * (K + Wm) + 2
+    desc, C, lane_pages, pass_meta = W.decode_loop_meta(seed=args.seed + rank, steps=total_steps)
+    cdesc = make_desc(desc)
+    dev = torch.device("cuda", local)
+    torch.manual_seed(1000 + args.seed + rank)
+    shape = (65536, desc.num_kv_heads, desc.page_size, desc.head_dim)
+    k_pool = torch.randn(shape, dtype=torch.bfloat16, device=dev)
+    v_pool = torch.randn(shape, dtype=torch.bfloat16, device=dev)
+    frozen = torch.from_numpy(C.copy()).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    L, Hq, Hkv, D = 64, desc.num_q_heads, desc.num_kv_heads, desc.head_dim
+    NB = 4  # distinct q/k/v batches cycled through the steps
+    q_d = [torch.randn((L, Hq, D), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+    k_d = [torch.randn((L, Hkv, D), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+    v_d = [torch.randn((L, Hkv, D), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+    q_rot = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((L, Hq), dtype=torch.float32, device=dev)
+    metas = [make_meta(pass_meta(t), 65536) for t in range(total_steps)]
+    from programmable_paged_kv_gb300 import workspace_bytes
+    ws_bytes = max(workspace_bytes(cdesc, metas[t]) for t in (0, total_steps - 1))
+    workspace = torch.empty(ws_bytes + 4096, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    live = []
+
+    def step(t, q, k, v, timed_ev=None):
+        plan = ForwardPlan(cdesc, metas[t], workspace=workspace)
+        plan.append_kv(q, k, v, q_rot, k_pool, v_pool, frozen, status)
+        if timed_ev is not None:
+            timed_ev[0].record(stream)
+        plan.attend(q_rot, k_pool, v_pool, None, out, lse, None, None, status)
+        if timed_ev is not None:
+            timed_ev[1].record(stream)
+        plan.fold(frozen, None, status)
+        live.append(plan)
+        if len(live) > 4:
+            live.pop(0).close()
+
+    t = 0
+    for _ in range(Wm):
+        step(t, q_d[t % NB], k_d[t % NB], v_d[t % NB])
+        t += 1
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    tokens = 0
+    bytes_step = 0
+    bytes_attend = 0
+    t_start.record(stream)
+    for i in range(K):
+        p = pass_meta(t)
+        tokens += attended_tokens(p)
+        bytes_step += step_alg_bytes(p, desc)
+        bytes_attend += attend_alg_bytes(p, desc)
+        step(t, q_d[t % NB], k_d[t % NB], v_d[t % NB], ev[i])
+        t += 1
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(pg)
+    el_ms = t_start.elapsed_time(t_end)
+    attend_ms = [a.elapsed_time(b) for a, b in ev]
+    el_max = max_over_ranks(pg, el_ms)
+    tokens_all = sum_over_ranks(pg, tokens)
+    value = tokens_all / (el_max / 1e3)
+    st = int(status.item())
+
+    # ---- end to end: host q/k/v in, readout back to host, every step
+    q_h = [x.cpu().pin_memory() for x in q_d]
+    k_h = [x.cpu().pin_memory() for x in k_d]
+    v_h = [x.cpu().pin_memory() for x in v_d]
+    q_in = torch.empty_like(q_d[0])
+    k_in = torch.empty_like(k_d[0])
+    v_in = torch.empty_like(v_d[0])
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step(t):
+        j = t % NB
+        q_in.copy_(q_h[j], non_blocking=True)
+        k_in.copy_(k_h[j], non_blocking=True)
+        v_in.copy_(v_h[j], non_blocking=True)
+        step(t, q_in, k_in, v_in)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(Wm):
+        e2e_step(t)
+        t += 1
+    torch.cuda.synchronize()
+    barrier(pg)
+    e_tok = 0
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e_tok += attended_tokens(pass_meta(t))
+        e2e_step(t)
+        t += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e_ms = max_over_ranks(pg, e0.elapsed_time(e1))
+    e_val = sum_over_ranks(pg, e_tok) / (e_ms / 1e3)
+    h2d = (q_in.numel() + k_in.numel() + v_in.numel()) * 2
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    for pl in live:
+        pl.close()
+
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    att_s = sum(attend_ms) / len(attend_ms) / 1e3
+    achieved = (bytes_attend / K) / att_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": Wm,
+        "ms_per_step": el_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1, "q_heads": Hq,
+                   "kv_heads": Hkv, "head_dim": D, "page_size": desc.page_size,
+                   "pool_pages": 65536, "kv_len": "C+t+1, C~U[512,4096]",
+                   "l2": "inputs larger than L2 (~600 MB of KV read per step)",
+                   "step": "plan+append_kv+attend+fold"},
+        "gpu_launches": 4 * K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": profiled_traffic(),
+                     "kernel": "pie_fwd_attend (split-KV attention + combine)",
+                     "peak_kind": peak_kind, "alg_bytes_per_launch": bytes_attend / K,
+                     "launch_ms": att_s * 1e3,
+                     "step_alg_gbs": (bytes_step / K) / (el_max / K / 1e3) / 1e9},
+        "e2e": {"value": e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "status": st,
+    }
+    if clk:
+        line["clocks"] = clk
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle as O
+        O.build()
+        rate, cores, passes, secs = oracle_rate(args.seed, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{passes} full decode-batch passes (64 lanes x 1 row, "
+                                          f"seed {args.seed}) in {secs:.1f} s on {cores} threads"}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    ws, rank, local, pg = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * pie_fwd.h -- C ABI of the GB300 (sm_103a) ForwardPass hot path.
+ *
+ * One Pie ForwardPass carries many lanes in one launch ("The forward pass",
+ * section Lanes): every lane has its own rows, concatenated and delimited by
+ * a row offset array, and its own working set of KV pages.  For one
+ * attention layer the pass
+ *   1. rotates each row's q and k at the row's explicit position ID and
+ *      writes the row's K/V into its slot of the lane's working set
+ *      (section State geometry: positions, slots);
+ *   2. runs grouped-query attention of every row over the lane's first
+ *      kv_len slots, restricted by the row's slot mask when one is given
+ *      (sections State geometry: kv_len; Attention masks);
+ *   3. returns outputs for the readout rows, by default the last row of each
+ *      lane (section Readouts);
+ *   4. freezes each lane's `fold` newly written slots: none, all, a count,
+ *      or a count that device code wrote into a channel (section State
+ *      geometry, speculative decoding paragraph).
+ * The four steps are the four calls pie_fwd_plan, pie_fwd_append_kv,
+ * pie_fwd_attend and pie_fwd_fold, issued in that order on one stream
+ * (section Pipelines and frames: passes on one pipeline run in submission
+ * order).
+ *
+ * Conventions
+ *   - Every device pointer is owned by the caller and must stay valid until
+ *     the work queued on `stream` that uses it has finished.  `stream` is a
+ *     cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Element types: PIE_F32 (float) or PIE_BF16 (bfloat16 stored as 16-bit
+ *     words).  Arithmetic is fp32 on the GPU in both cases.
+ *   - K/V pools are laid out [num_pool_pages][num_kv_heads][page_size]
+ *     [head_dim], elements of the pass dtype.  Slot s of lane l lives in
+ *     page page_ids[page_indptr[l] + s / page_size] at offset s % page_size.
+ *   - Per-row tensors: q, q_rot [num_rows][num_q_heads][head_dim];
+ *     k, v [num_rows][num_kv_heads][head_dim]; contiguous.
+ *   - Mask words: slot s is visible to row r iff bit (s & 31) of
+ *     mask_words[mask_word_indptr[r] + (s >> 5)] is set (LSB first).  A row
+ *     needs at least ceil(kv_len / 32) words; bits at or past kv_len are
+ *     ignored.  Without a mask a row sees slots s <= its own slot and
+ *     s < kv_len (causal in slot space, which is the folding() geometry).
+ *   - Every call returns PIE_OK (0) or a negative error code and queues no
+ *     work on error.  pie_fwd_last_error() gives a message for the calling
+ *     thread's last error.  No call synchronizes the host with the device.
+ *   - Device-side findings are ORed into a caller-owned uint32 status word
+ *     (PIE_STATUS_*); the caller reads it whenever convenient.
+ */
+#ifndef PIE_FWD_H_
+#define PIE_FWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes -------------------------------------------------------- */
+#define PIE_OK 0
+#define PIE_EINVAL (-1)       /* malformed argument or metadata              */
+#define PIE_ERANGE (-2)       /* a value outside its allowed range           */
+#define PIE_ENOSPACE (-3)     /* workspace smaller than required             */
+#define PIE_ECUDA (-4)        /* a CUDA runtime call failed                  */
+#define PIE_EUNSUPPORTED (-5) /* dtype / head_dim / page_size not built      */
+
+/* ---- element types ------------------------------------------------------ */
+#define PIE_F32 0
+#define PIE_BF16 1
+
+/* ---- fold modes (StateGeometry.fold per lane) ---------------------------- */
+#define PIE_FOLD_NONE 0    /* freeze nothing                                   */
+#define PIE_FOLD_ALL 1     /* freeze every row written by this pass            */
+#define PIE_FOLD_COUNT 2   /* freeze fold_count[l] rows (host literal)         */
+#define PIE_FOLD_CHANNEL 3 /* freeze channel[l] rows, read on the device       */
+
+/* ---- device status bits ---------------------------------------------------- */
+#define PIE_STATUS_FROZEN_WRITE 1u /* a row's slot was frozen; its K/V write was skipped */
+#define PIE_STATUS_FOLD_CLAMP 2u   /* a channel count outside [0, n] was clamped          */
+#define PIE_STATUS_FOLD_GAP 8u     /* a folding lane's first slot != its frozen length    */
+#define PIE_STATUS_TIMEOUT 16u     /* a kernel's bounded wait expired; outputs invalid    */
+
+/* Static description of the attention layer. */
+typedef struct pie_fwd_desc {
+  int32_t num_q_heads;  /* Hq; a multiple of num_kv_heads                     */
+  int32_t num_kv_heads; /* Hkv; q head h reads kv head h / (Hq / Hkv)          */
+  int32_t head_dim;     /* d: 64 or 128                                        */
+  int32_t page_size;    /* P: 8, 16 or 32 slots per KV page                     */
+  int32_t dtype;        /* PIE_F32 or PIE_BF16                                  */
+  float rope_base;      /* RoPE base (e.g. 10000); rotate-half pairing i, i+d/2 */
+  float sm_scale;       /* softmax scale; 0 means 1 / sqrt(head_dim)            */
+} pie_fwd_desc;
+
+/* Per-pass metadata.  All arrays are HOST memory, read only during
+ * pie_fwd_workspace_bytes / pie_fwd_plan and not retained. */
+typedef struct pie_fwd_meta {
+  int32_t num_lanes; /* L >= 0                                                 */
+  int32_t num_rows;  /* N >= 0                                                 */
+  const int32_t* row_indptr;  /* [L+1]: rows of lane l are [row_indptr[l], row_indptr[l+1]) */
+  const int32_t* positions;   /* [N]: RoPE position ID of each row (>= 0)            */
+  const int32_t* slots;       /* [N]: working-set slot each row writes               */
+  const int32_t* kv_len;      /* [L]: slots the lane reads, <= its page capacity     */
+  const int32_t* page_indptr; /* [L+1]: the lane's pages are page_ids[page_indptr[l]..] */
+  const int32_t* page_ids;    /* physical page ids in [0, num_pool_pages)            */
+  int32_t num_pool_pages;
+  const int32_t* fold_mode;   /* [L]: PIE_FOLD_*                                     */
+  const int32_t* fold_count;  /* [L]: used by PIE_FOLD_COUNT; may be NULL otherwise  */
+  const int64_t* mask_word_indptr; /* [N+1] or NULL (default causal visibility)    */
+  const int32_t* readout;     /* [R] row indices, or NULL: last row of every lane
+                                 that has rows                                      */
+  int32_t num_readout;        /* R when readout != NULL                              */
+} pie_fwd_meta;
+
+typedef struct pie_fwd_plan pie_fwd_plan_t;
+
+/* Device workspace the plan needs for this pass (metadata, work lists and
+ * split-softmax partials).  Host only; no CUDA call.
+ * Errors: PIE_EINVAL / PIE_ERANGE / PIE_EUNSUPPORTED as pie_fwd_plan. */
+int pie_fwd_workspace_bytes(const pie_fwd_desc* desc, const pie_fwd_meta* meta,
+                            size_t* bytes);
+
+/* Plan one pass (the "state" and "mask"/"readout" set-up of a ForwardPass).
+ * Validates the metadata:
+ *   PIE_EINVAL  - non-monotone or inconsistent indptr arrays, unknown fold
+ *                 mode, two rows writing the same physical slot (the
+ *                 hazard-freedom condition of the Pie review, Eq. (4)), or a
+ *                 folding lane whose slots are not consecutive;
+ *   PIE_ERANGE  - negative position, slot outside the lane's pages, kv_len
+ *                 above the lane's capacity, page id outside the pool,
+ *                 readout row out of range, fold_count outside [0, n], or a
+ *                 row with fewer than ceil(kv_len/32) mask words;
+ *   PIE_EUNSUPPORTED - head_dim / page_size / dtype not built;
+ *   PIE_ENOSPACE - ws_bytes < pie_fwd_workspace_bytes().
+ * Builds the work lists on the host and queues one host-to-device copy into
+ * `dev_workspace` (256-byte aligned, caller-owned, must outlive the plan's
+ * use) on `stream`.  The returned plan is immutable, owned by the library,
+ * usable for any number of append/attend/fold calls on streams ordered after
+ * `stream`, and released with pie_fwd_plan_destroy. */
+int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_workspace,
+                 size_t ws_bytes, void* stream, pie_fwd_plan_t** out);
+
+/* Number of readout rows R of a plan (the first dimension of out_readout). */
+int32_t pie_fwd_plan_num_readout(const pie_fwd_plan_t* plan);
+
+/* Step 1 (State geometry: positions, slots).  For every row r of lane l:
+ *   q_rot[r,h]  = RoPE(q[r,h], positions[r])                 for all q heads
+ *   K_pool[slot] = RoPE(k[r,g], positions[r]), V_pool[slot] = v[r,g]
+ * RoPE pairs element i with i + d/2 at angle positions[r] * base^(-2i/d)
+ * (fp32 angle).  A row whose slot is below frozen_len[l] is not written and
+ * sets PIE_STATUS_FROZEN_WRITE; a lane with fold != NONE whose first slot is
+ * not frozen_len[l] sets PIE_STATUS_FOLD_GAP.
+ * q, k, v: device, read; q_rot: device [N,Hq,d], written; k_pool, v_pool:
+ * device pools, written at the rows' slots only; frozen_len: device int32 [L];
+ * status: device uint32 (may be NULL).  Errors: PIE_EINVAL on a NULL
+ * required pointer, PIE_ECUDA on a failed launch. */
+int pie_fwd_append_kv(const pie_fwd_plan_t* plan, const void* q, const void* k, const void* v,
+                      void* q_rot, void* k_pool, void* v_pool, const int32_t* frozen_len,
+                      uint32_t* status, void* stream);
+
+/* Step 2-3 (State geometry: kv_len; Attention masks; Readouts).  For every
+ * row r of lane l and q head h (kv head g = h / (Hq/Hkv)), over the visible
+ * slots V(r) of [0, kv_len[l]):
+ *   z_s = sm_scale * <q_rot[r,h], K[s,g]>,  o = sum_s softmax(z)_s V[s,g],
+ *   lse = log(sum_s exp(z_s)).
+ * An empty V(r) gives o = 0 and lse = -inf.
+ * mask_words: device uint32 words (required iff the plan has a mask).
+ * out_readout: device [R,Hq,d] in the dtype (may be NULL if R == 0);
+ * lse_readout: device float [R,Hq] or NULL; out_all: device [N,Hq,d] or
+ * NULL (every row's output); lse_all: device float [N,Hq] or NULL.
+ * The pools are only read.  Precondition: every slot below kv_len holds
+ * finite K and V (masked-out slots included); slots at or past kv_len may
+ * hold anything.  status: device uint32 or NULL (PIE_STATUS_TIMEOUT). */
+int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_pool,
+                   const void* v_pool, const uint32_t* mask_words, void* out_readout,
+                   float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
+                   void* stream);
+
+/* Step 4 (State geometry: fold).  frozen_len[l] += k_l with k_l = 0 (NONE),
+ * n_l (ALL), fold_count[l] (COUNT) or clamp(channel[l], 0, n_l) (CHANNEL;
+ * PIE_STATUS_FOLD_CLAMP when clamped).  channel: device int32 [L], written
+ * earlier on `stream` (required iff a lane uses PIE_FOLD_CHANNEL). */
+int pie_fwd_fold(const pie_fwd_plan_t* plan, int32_t* frozen_len, const int32_t* channel,
+                 uint32_t* status, void* stream);
+
+/* Releases a plan.  Waits for the plan's own host-to-device copy if it is
+ * still in flight; never waits for kernels. */
+void pie_fwd_plan_destroy(pie_fwd_plan_t* plan);
+
+/* Message for the calling thread's most recent error ("" if none). */
+const char* pie_fwd_last_error(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int pie_fwd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIE_FWD_H_ */

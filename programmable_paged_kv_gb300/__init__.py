@@ -1,0 +1,153 @@
+"""GB300 (sm_103a) ForwardPass hot path: RoPE + slot scatter, paged GQA
+attention under per-row slot masks, readout and fold, behind a C ABI
+(include/pie_fwd.h).
+
+This package is a thin binding: it marshals host metadata (numpy arrays)
+and torch device tensors into the C entry points of libpie_fwd.so.  PyTorch
+only provides device memory and the current stream.  There is no fallback:
+if the library is missing every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import numpy as np
+
+from . import abi
+from .abi import (PIE_BF16, PIE_F32, PIE_FOLD_ALL, PIE_FOLD_CHANNEL, PIE_FOLD_COUNT,
+                  PIE_FOLD_NONE, PIE_STATUS_FOLD_CLAMP, PIE_STATUS_FOLD_GAP,
+                  PIE_STATUS_FROZEN_WRITE, PIE_STATUS_TIMEOUT, PieError)
+
+__all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes", "build",
+           "PIE_F32", "PIE_BF16", "PIE_FOLD_NONE", "PIE_FOLD_ALL", "PIE_FOLD_COUNT",
+           "PIE_FOLD_CHANNEL", "PIE_STATUS_FROZEN_WRITE", "PIE_STATUS_FOLD_CLAMP",
+           "PIE_STATUS_FOLD_GAP", "PIE_STATUS_TIMEOUT"]
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _b
+    return _b(force=force)
+
+
+def make_desc(d) -> abi.pie_fwd_desc:
+    """From any object with num_q_heads, num_kv_heads, head_dim, page_size,
+    dtype (PIE_F32 / PIE_BF16), rope_base and sm_scale attributes."""
+    return abi.pie_fwd_desc(int(d.num_q_heads), int(d.num_kv_heads), int(d.head_dim),
+                            int(d.page_size), int(d.dtype), float(d.rope_base),
+                            float(getattr(d, "sm_scale", 0.0)))
+
+
+class _HostMeta:
+    """pie_fwd_meta over numpy arrays that stay alive with this object."""
+
+    def __init__(self, row_indptr, positions, slots, kv_len, page_indptr, page_ids,
+                 num_pool_pages, fold_mode, fold_count=None, mask_word_indptr=None,
+                 readout=None):
+        i32 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+        self.keep = dict(row_indptr=i32(row_indptr), positions=i32(positions), slots=i32(slots),
+                         kv_len=i32(kv_len), page_indptr=i32(page_indptr),
+                         page_ids=i32(page_ids), fold_mode=i32(fold_mode),
+                         fold_count=i32(fold_count), readout=i32(readout),
+                         mask_word_indptr=None if mask_word_indptr is None else
+                         np.ascontiguousarray(mask_word_indptr, dtype=np.int64))
+        k = self.keep
+        ptr = lambda a: None if a is None else a.ctypes.data
+        self.c = abi.pie_fwd_meta(
+            int(k["kv_len"].shape[0]), int(k["positions"].shape[0]), ptr(k["row_indptr"]),
+            ptr(k["positions"]), ptr(k["slots"]), ptr(k["kv_len"]), ptr(k["page_indptr"]),
+            ptr(k["page_ids"]), int(num_pool_pages), ptr(k["fold_mode"]), ptr(k["fold_count"]),
+            ptr(k["mask_word_indptr"]), ptr(k["readout"]),
+            0 if k["readout"] is None else int(k["readout"].shape[0]))
+
+
+def make_meta(p, num_pool_pages: int, page_ids=None) -> _HostMeta:
+    """From any object with the pass fields (row_indptr, positions, slots,
+    kv_len, page_indptr, page_ids, fold_mode, fold_count, mask_word_indptr,
+    readout)."""
+    return _HostMeta(p.row_indptr, p.positions, p.slots, p.kv_len, p.page_indptr,
+                     p.page_ids if page_ids is None else page_ids, num_pool_pages, p.fold_mode,
+                     p.fold_count, p.mask_word_indptr, p.readout)
+
+
+def workspace_bytes(desc: abi.pie_fwd_desc, meta: _HostMeta) -> int:
+    n = C.c_size_t(0)
+    abi.check(abi.load().pie_fwd_workspace_bytes(C.byref(desc), C.byref(meta.c), C.byref(n)),
+              "pie_fwd_workspace_bytes")
+    return int(n.value)
+
+
+def _ptr(t, what: str, required: bool = True):
+    """Device address of a tensor; None becomes NULL (the C side decides
+    whether the argument may be NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class ForwardPlan:
+    """One planned ForwardPass (pie_fwd_plan) and its three device steps.
+
+    desc: pie_fwd_desc (see make_desc); meta: _HostMeta (see make_meta).
+    workspace: optional uint8 CUDA tensor of at least workspace_bytes();
+    allocated here when omitted.
+    """
+
+    def __init__(self, desc: abi.pie_fwd_desc, meta: _HostMeta, workspace=None, stream=None):
+        import torch
+        self.lib = abi.load()
+        self.desc = desc
+        self.meta = meta
+        if workspace is None:
+            need = workspace_bytes(desc, meta)
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        # a caller-supplied workspace that is too small is refused by the
+        # planner itself (PIE_ENOSPACE)
+        self.workspace = workspace
+        h = C.c_void_p()
+        abi.check(self.lib.pie_fwd_plan(C.byref(desc), C.byref(meta.c), _ptr(workspace, "workspace"),
+                                        workspace.numel(), _stream(stream), C.byref(h)),
+                  "pie_fwd_plan")
+        self.handle = h
+        self.num_readout = int(self.lib.pie_fwd_plan_num_readout(h))
+
+    def append_kv(self, q, k, v, q_rot, k_pool, v_pool, frozen_len, status=None, stream=None):
+        abi.check(self.lib.pie_fwd_append_kv(
+            self.handle, _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(q_rot, "q_rot"),
+            _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"), _ptr(frozen_len, "frozen_len"),
+            _ptr(status, "status", False), _stream(stream)), "pie_fwd_append_kv")
+
+    def attend(self, q_rot, k_pool, v_pool, mask_words=None, out_readout=None, lse_readout=None,
+               out_all=None, lse_all=None, status=None, stream=None):
+        abi.check(self.lib.pie_fwd_attend(
+            self.handle, _ptr(q_rot, "q_rot"), _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
+            _ptr(mask_words, "mask_words", False), _ptr(out_readout, "out_readout", False),
+            _ptr(lse_readout, "lse_readout", False), _ptr(out_all, "out_all", False),
+            _ptr(lse_all, "lse_all", False), _ptr(status, "status", False), _stream(stream)),
+            "pie_fwd_attend")
+
+    def fold(self, frozen_len, channel=None, status=None, stream=None):
+        abi.check(self.lib.pie_fwd_fold(
+            self.handle, _ptr(frozen_len, "frozen_len"), _ptr(channel, "channel", False),
+            _ptr(status, "status", False), _stream(stream)), "pie_fwd_fold")
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.pie_fwd_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,108 @@
+"""ctypes declarations of the C ABI in include/pie_fwd.h.
+
+Argument marshalling only: every step of the ForwardPass hot path runs in
+libpie_fwd.so.  Loading fails loudly when the library has not been built;
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpie_fwd.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pie_fwd.h")
+
+PIE_OK = 0
+PIE_EINVAL = -1
+PIE_ERANGE = -2
+PIE_ENOSPACE = -3
+PIE_ECUDA = -4
+PIE_EUNSUPPORTED = -5
+
+PIE_F32 = 0
+PIE_BF16 = 1
+
+PIE_FOLD_NONE = 0
+PIE_FOLD_ALL = 1
+PIE_FOLD_COUNT = 2
+PIE_FOLD_CHANNEL = 3
+
+PIE_STATUS_FROZEN_WRITE = 1
+PIE_STATUS_FOLD_CLAMP = 2
+PIE_STATUS_FOLD_GAP = 8
+PIE_STATUS_TIMEOUT = 16
+
+
+class pie_fwd_desc(C.Structure):
+    _fields_ = [("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("page_size", C.c_int32), ("dtype", C.c_int32),
+                ("rope_base", C.c_float), ("sm_scale", C.c_float)]
+
+
+class pie_fwd_meta(C.Structure):
+    _fields_ = [("num_lanes", C.c_int32), ("num_rows", C.c_int32),
+                ("row_indptr", C.c_void_p), ("positions", C.c_void_p),
+                ("slots", C.c_void_p), ("kv_len", C.c_void_p),
+                ("page_indptr", C.c_void_p), ("page_ids", C.c_void_p),
+                ("num_pool_pages", C.c_int32), ("fold_mode", C.c_void_p),
+                ("fold_count", C.c_void_p), ("mask_word_indptr", C.c_void_p),
+                ("readout", C.c_void_p), ("num_readout", C.c_int32)]
+
+
+_P = C.c_void_p
+# name -> (restype, argtypes), in header order
+SIGNATURES = {
+    "pie_fwd_workspace_bytes": (C.c_int, [C.POINTER(pie_fwd_desc), C.POINTER(pie_fwd_meta),
+                                          C.POINTER(C.c_size_t)]),
+    "pie_fwd_plan": (C.c_int, [C.POINTER(pie_fwd_desc), C.POINTER(pie_fwd_meta), _P, C.c_size_t,
+                               _P, C.POINTER(_P)]),
+    "pie_fwd_plan_num_readout": (C.c_int32, [_P]),
+    "pie_fwd_append_kv": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pie_fwd_attend": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pie_fwd_fold": (C.c_int, [_P, _P, _P, _P, _P]),
+    "pie_fwd_plan_destroy": (None, [_P]),
+    "pie_fwd_last_error": (C.c_char_p, []),
+    "pie_fwd_abi_version": (C.c_int, []),
+}
+
+
+def header_functions() -> list:
+    """Names of the functions include/pie_fwd.h declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pie_fwd_[a-z0-9_]+)\s*\(", src)))
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libpie_fwd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing: run "
+                           "programmable_paged_kv_gb300.build.build() first")
+    lib = C.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+class PieError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where} failed with {code}: {msg}")
+        self.code = code
+
+
+def check(code: int, where: str):
+    if code != PIE_OK:
+        raise PieError(code, where, load().pie_fwd_last_error().decode())
+    return code

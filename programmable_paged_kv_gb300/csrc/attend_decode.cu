@@ -1,0 +1,446 @@
+// Step 2-3 of a ForwardPass for lanes with few query vectors per kv head
+// (decode rows, short drafts): split-KV grouped-query attention over paged
+// K/V (Pie "The forward pass": State geometry kv_len; Attention masks), and
+// the combine step that merges the split partial softmax states and gathers
+// the readout rows (section Readouts).
+//
+// Decode attention is bound by HBM: every visible slot's K and V head rows
+// are read once and used by the NQ query vectors of the GQA group.  The
+// kernel therefore
+//   * streams pages through a ring of shared-memory stages with 1-D TMA bulk
+//     copies (one copy per (page, kv head) block, contiguous in the
+//     [page][kv head][slot][d] pools), completed on mbarriers, issued by a
+//     dedicated producer warp with an evict-first L2 hint;
+//   * lets each of 4 compute warps own 16 slots of every 64-slot stage, with
+//     its own online-softmax state, so the main loop needs no CTA barrier;
+//   * keeps the NQ query vectors in registers split along d (16 bytes per
+//     lane) and reduces the NQ x 16 partial dot products of a warp with a
+//     transposed butterfly (each round halves the values a lane holds), so
+//     that scoring a slot costs about two shuffles instead of log2(lanes)
+//     per query;
+//   * accumulates P.V with lanes split along d and probabilities broadcast
+//     from a per-warp shared buffer.
+// Scores are kept in the log2 domain (q pre-scaled by sm_scale * log2 e).
+// Each work item writes one partial (max, sum, unnormalised output) per
+// query vector; the combine kernel merges an item's chunks.
+
+#include "common.cuh"
+
+namespace pie {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T, int D, int NQ>
+struct DecCfg {
+  static constexpr int EPL = 16 / sizeof(T);      // q/K elements per lane (one 16-byte vector)
+  static constexpr int LPR = D / EPL;             // lanes covering one K row
+  static constexpr int RPS = 32 / LPR;            // K rows per warp step
+  static constexpr int STEPS = kWarpSlots / RPS;  // steps per 16-slot unit
+  static constexpr int NV = STEPS * NQ;           // partial dot products per lane
+  static constexpr int E = NV / LPR;              // scores per lane after the reduction
+  static constexpr int DPL = D / 32;              // output elements per lane in P.V
+  static constexpr int WARPS = 4;                 // compute warps (+1 producer warp)
+  static constexpr int THREADS = (WARPS + 1) * 32;
+  static constexpr int ROW_BYTES = D * sizeof(T);
+  static constexpr int STAGE_BYTES = 2 * kStageSlots * ROW_BYTES;  // K + V
+  static constexpr int STAGES = (98304 / STAGE_BYTES) < 2 ? 2
+                                : (98304 / STAGE_BYTES) > 4 ? 4 : (98304 / STAGE_BYTES);
+  static constexpr int PBUF_FLOATS = WARPS * kWarpSlots * NQ;
+  static constexpr int ABUF_FLOATS = WARPS * NQ;
+  static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES +
+                                 sizeof(float) * (PBUF_FLOATS + ABUF_FLOATS) +
+                                 sizeof(uint64_t) * 2 * STAGES;
+  static_assert(E == NQ / 2, "reduction layout assumes E = NQ / 2");
+  static_assert(kWarpSlots % RPS == 0, "unit must hold whole steps");
+  static_assert(size_t(WARPS) * NQ * (D + 2) * 4 <= size_t(STAGES) * STAGE_BYTES,
+                "merge buffers must fit in the stage ring");
+};
+
+// Transposed butterfly: v[0..N) partial sums per lane; after log2(LPR)
+// rounds lane j of its row group holds the complete sums of entries
+// [j * N/LPR, (j+1) * N/LPR) in v[0 .. N/LPR).
+template <int N, int OFF>
+struct TReduce {
+  static __device__ __forceinline__ void run(float* v, int j) {
+    const bool upper = (j & OFF) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = upper ? v[i] : v[i + N / 2];
+      const float keep = upper ? v[i + N / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+    }
+    TReduce<N / 2, OFF / 2>::run(v, j);
+  }
+};
+template <int N>
+struct TReduce<N, 0> {
+  static __device__ __forceinline__ void run(float*, int) {}
+};
+
+__device__ __forceinline__ float warp_max_pairs(float x) {
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+__device__ __forceinline__ float warp_sum_pairs(float x) {
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Load DPL consecutive elements (4, 8 or 16 bytes) as floats.
+template <typename T, int DPL>
+__device__ __forceinline__ void load_dpl(const T* p, float* f) {
+  if constexpr (sizeof(T) * DPL == 16) {
+    unpack16<T>(*reinterpret_cast<const uint4*>(p), f);
+  } else if constexpr (sizeof(T) * DPL == 8) {
+    unpack8<T>(*reinterpret_cast<const uint2*>(p), f);
+  } else {
+    static_assert(sizeof(T) * DPL == 4, "unsupported lane width");
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    if constexpr (sizeof(T) == 2) {
+      f[0] = __uint_as_float(u << 16);
+      f[1] = __uint_as_float(u & 0xFFFF0000u);
+    } else {
+      f[0] = __uint_as_float(u);
+    }
+  }
+}
+
+template <typename T, int D, int NQ>
+__global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kernel(
+    DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const T* __restrict__ q_rot,
+    const T* __restrict__ k_pool, const T* __restrict__ v_pool,
+    const uint32_t* __restrict__ mask_words, uint32_t* status) {
+  using C = DecCfg<T, D, NQ>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  T* ring = reinterpret_cast<T*>(smem);
+  float* pbuf = reinterpret_cast<float*>(smem + size_t(C::STAGES) * C::STAGE_BYTES);
+  float* abuf = pbuf + C::PBUF_FLOATS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(abuf + C::ABUF_FLOATS);
+  uint64_t* empty = full + C::STAGES;
+
+  const DecItem it = m.dec_items[blockIdx.x];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = it.kv_begin, ke = it.kv_end;
+  const int nstages = ke > kb ? (ke - kb + kStageSlots - 1) / kStageSlots : 0;
+  const int nqv = it.nrows * G;  // valid query vectors
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::WARPS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == C::WARPS) {
+    // ---------------- producer warp: TMA bulk copies of K/V pages ----------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
+      const int64_t head_stride = int64_t(P) * D;  // elements per (page, kv head) block
+      for (int s = 0; s < nstages; ++s) {
+        const int st = s % C::STAGES, use = s / C::STAGES;
+        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1)) {
+          set_status(status, PIE_STATUS_TIMEOUT);
+          break;
+        }
+        const int sb = kb + s * kStageSlots;
+        const int se = min(sb + kStageSlots, ke);
+        const int p0 = sb / P, p1 = (se - 1) / P;
+        const uint32_t blk = uint32_t(P) * C::ROW_BYTES;
+        mbar_arrive_expect_tx(&full[st], 2u * blk * uint32_t(p1 - p0 + 1));
+        T* kdst = ring + size_t(st) * 2 * kStageSlots * D;
+        T* vdst = kdst + kStageSlots * D;
+        for (int pg = p0; pg <= p1; ++pg) {
+          const int64_t src = (int64_t(pages[pg]) * Hkv + it.kv_head) * head_stride;
+          const int off = (pg * P - sb) * D;
+          bulk_g2s_hint(kdst + off, k_pool + src, blk, &full[st], pol);
+          bulk_g2s_hint(vdst + off, v_pool + src, blk, &full[st], pol);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps ---------------------------------------------
+  const int j = lane % C::LPR;   // lane within its K row group
+  const int rg = lane / C::LPR;  // row group (slot within a step)
+
+  float qr[NQ][C::EPL];
+#pragma unroll
+  for (int qq = 0; qq < NQ; ++qq) {
+    const int qv = min(qq, nqv - 1);
+    const int row = it.row0 + qv / G, head = it.kv_head * G + qv % G;
+    const uint4 u =
+        *reinterpret_cast<const uint4*>(q_rot + (int64_t(row) * Hq + head) * D + j * C::EPL);
+    unpack16<T>(u, qr[qq]);
+#pragma unroll
+    for (int e = 0; e < C::EPL; ++e) qr[qq][e] *= scale_log2;
+  }
+  // the E query vectors whose scores this lane holds after the reduction
+  bool qvalid[C::E];
+  int slot_lim[C::E];
+  int64_t mbase[C::E];
+#pragma unroll
+  for (int e = 0; e < C::E; ++e) {
+    const int qq = (j & 1) * C::E + e;
+    qvalid[e] = qq < nqv;
+    const int row = it.row0 + min(qq, nqv - 1) / G;
+    slot_lim[e] = m.slots[row];
+    mbase[e] = mask_words ? m.mask_word_indptr[row] : 0;
+  }
+
+  float m_run[C::E], l_run[C::E];
+#pragma unroll
+  for (int e = 0; e < C::E; ++e) {
+    m_run[e] = -INFINITY;
+    l_run[e] = 0.f;
+  }
+  float acc[NQ][C::DPL];
+#pragma unroll
+  for (int qq = 0; qq < NQ; ++qq)
+#pragma unroll
+    for (int c = 0; c < C::DPL; ++c) acc[qq][c] = 0.f;
+
+  float* my_p = pbuf + warp * kWarpSlots * NQ;
+  float* my_a = abuf + warp * NQ;
+  const int s_in_unit = (j >> 1) * C::RPS + rg;
+  bool timed_out = false;
+
+  for (int s = 0; s < nstages; ++s) {
+    const int st = s % C::STAGES;
+    if (!mbar_wait(&full[st], (s / C::STAGES) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const int unit_base = kb + s * kStageSlots + warp * kWarpSlots;
+    const int nvalid = min(kWarpSlots, ke - unit_base);
+    if (nvalid > 0) {
+      const T* Ks = ring + size_t(st) * 2 * kStageSlots * D + warp * kWarpSlots * D;
+      const T* Vs = Ks + kStageSlots * D;
+      // ---- scores: NQ x 16 dot products, reduced across the row group
+      float part[C::NV];
+#pragma unroll
+      for (int t = 0; t < C::STEPS; ++t) {
+        float kf[C::EPL];
+        unpack16<T>(*reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rg) * D + j * C::EPL), kf);
+#pragma unroll
+        for (int qq = 0; qq < NQ; ++qq) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < C::EPL; ++e) a = fmaf(qr[qq][e], kf[e], a);
+          part[t * NQ + qq] = a;
+        }
+      }
+      TReduce<C::NV, C::LPR / 2>::run(part, j);
+      // ---- online softmax for this warp's 16 slots
+      const int s_abs = unit_base + s_in_unit;
+      uint32_t word[C::E];
+#pragma unroll
+      for (int e = 0; e < C::E; ++e)
+        word[e] = (mask_words && s_in_unit < nvalid) ? mask_words[mbase[e] + (s_abs >> 5)] : 0u;
+#pragma unroll
+      for (int e = 0; e < C::E; ++e) {
+        const bool in = qvalid[e] && s_in_unit < nvalid;
+        const bool vis = in && (mask_words ? ((word[e] >> (s_abs & 31)) & 1u) != 0
+                                           : s_abs <= slot_lim[e]);
+        const float sc = vis ? part[e] : -INFINITY;
+        const float m_new = fmaxf(m_run[e], warp_max_pairs(sc));
+        const bool none = m_new == -INFINITY;
+        const float alpha = none ? 1.f : exp2f(m_run[e] - m_new);
+        const float p = vis ? exp2f(sc - m_new) : 0.f;
+        l_run[e] = l_run[e] * alpha + warp_sum_pairs(p);
+        m_run[e] = m_new;
+        const int qq = (j & 1) * C::E + e;
+        my_p[s_in_unit * NQ + qq] = p;
+        if (lane < 2) my_a[qq] = alpha;
+      }
+      __syncwarp();
+      // ---- P.V with lanes split along d
+#pragma unroll
+      for (int qq = 0; qq < NQ; ++qq) {
+        const float a = my_a[qq];
+#pragma unroll
+        for (int c = 0; c < C::DPL; ++c) acc[qq][c] *= a;
+      }
+      for (int sl = 0; sl < nvalid; ++sl) {
+        float vf[C::DPL];
+        load_dpl<T, C::DPL>(Vs + sl * D + lane * C::DPL, vf);
+        float pq[NQ];
+#pragma unroll
+        for (int qq = 0; qq < NQ; ++qq) pq[qq] = my_p[sl * NQ + qq];
+#pragma unroll
+        for (int qq = 0; qq < NQ; ++qq)
+#pragma unroll
+          for (int c = 0; c < C::DPL; ++c) acc[qq][c] = fmaf(pq[qq], vf[c], acc[qq][c]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+  if (timed_out && lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
+
+  // ---- merge the 4 warps' states (ring memory is free: every stage was
+  // consumed, so no copy is in flight) and write the item's partials
+  asm volatile("bar.sync 1, %0;" ::"n"(C::WARPS * 32) : "memory");
+  float* mw = reinterpret_cast<float*>(smem);   // [WARPS][NQ]
+  float* lw = mw + C::WARPS * NQ;               // [WARPS][NQ]
+  float* ow = lw + C::WARPS * NQ;               // [WARPS][NQ][D]
+  if (rg == 0 && j < 2) {
+#pragma unroll
+    for (int e = 0; e < C::E; ++e) {
+      mw[warp * NQ + j * C::E + e] = m_run[e];
+      lw[warp * NQ + j * C::E + e] = l_run[e];
+    }
+  }
+#pragma unroll
+  for (int qq = 0; qq < NQ; ++qq)
+#pragma unroll
+    for (int c = 0; c < C::DPL; ++c) ow[(warp * NQ + qq) * D + lane * C::DPL + c] = acc[qq][c];
+  asm volatile("bar.sync 1, %0;" ::"n"(C::WARPS * 32) : "memory");
+  for (int idx = threadIdx.x; idx < NQ * D; idx += C::WARPS * 32) {
+    const int qq = idx / D, c = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, mw[w * NQ + qq]);
+    float O = 0.f, Ls = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::WARPS; ++w) {
+        const float f = exp2f(mw[w * NQ + qq] - M);
+        O = fmaf(f, ow[(w * NQ + qq) * D + c], O);
+        Ls = fmaf(f, lw[w * NQ + qq], Ls);
+      }
+    }
+    m.part_o[int64_t(it.part_base + qq) * D + c] = O;
+    if (c == 0) m.part_ml[it.part_base + qq] = make_float2(M, Ls);
+  }
+}
+
+template <typename T, int D, int NQ>
+static cudaError_t launch_dec(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
+                              const void* v_pool, const uint32_t* mask_words, uint32_t* status,
+                              cudaStream_t s) {
+  using C = DecCfg<T, D, NQ>;
+  static bool configured = false;  // per instantiation; attribute is per device function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attend_decode_kernel<T, D, NQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  attend_decode_kernel<T, D, NQ><<<p.num_dec_items, C::THREADS, C::SMEM, s>>>(
+      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.desc.page_size,
+      p.desc.sm_scale * kLog2e, static_cast<const T*>(q_rot), static_cast<const T*>(k_pool),
+      static_cast<const T*>(v_pool), mask_words, status);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_dec_nq(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
+                                 const void* v_pool, const uint32_t* mask_words, uint32_t* status,
+                                 cudaStream_t s) {
+  switch (p.nq) {
+    case 2: return launch_dec<T, D, 2>(p, q_rot, k_pool, v_pool, mask_words, status, s);
+    case 4: return launch_dec<T, D, 4>(p, q_rot, k_pool, v_pool, mask_words, status, s);
+    default: return launch_dec<T, D, 8>(p, q_rot, k_pool, v_pool, mask_words, status, s);
+  }
+}
+
+cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
+                                 const void* v_pool, const uint32_t* mask_words,
+                                 uint32_t* status, cudaStream_t s) {
+  const bool bf = p.desc.dtype == PIE_BF16;
+  if (p.desc.head_dim == 128)
+    return bf ? launch_dec_nq<__nv_bfloat16, 128>(p, q_rot, k_pool, v_pool, mask_words, status, s)
+              : launch_dec_nq<float, 128>(p, q_rot, k_pool, v_pool, mask_words, status, s);
+  return bf ? launch_dec_nq<__nv_bfloat16, 64>(p, q_rot, k_pool, v_pool, mask_words, status, s)
+            : launch_dec_nq<float, 64>(p, q_rot, k_pool, v_pool, mask_words, status, s);
+}
+
+// ---------------------------------------------------------------------------
+// Combine: one warp per (target row, q head).  Targets [0, R) are the readout
+// rows (written to out_readout / lse_readout); targets [R, R + N) are all rows
+// (out_all / lse_all) when requested.  Merges the chunks' (max, sum, output)
+// in the log2 domain; an empty visible set gives o = 0 and lse = -inf.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv, int G, int N,
+                                                      int R, int with_all, T* out_readout,
+                                                      float* lse_readout, T* out_all,
+                                                      float* lse_all) {
+  constexpr int DPL = D / 32;
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int targets = R + (with_all ? N : 0);
+  if (gw >= targets * Hq) return;
+  const int tgt = gw / Hq, h = gw % Hq;
+  const bool is_ro = tgt < R;
+  const int row = is_ro ? m.readout[tgt] : tgt - R;
+  const CombEntry ce = m.comb[int64_t(row) * Hkv + h / G];
+  const int qi = ce.q_off + h % G;
+  float M = -INFINITY;
+  for (int c = 0; c < ce.nchunks; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
+  float o[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+  float Ls = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < ce.nchunks; ++c) {
+      const int idx = ce.part_base + c * ce.stride + qi;
+      const float2 ml = m.part_ml[idx];
+      const float f = exp2f(ml.x - M);
+      Ls = fmaf(f, ml.y, Ls);
+      const float* po = m.part_o + int64_t(idx) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[e] = fmaf(f, po[e], o[e]);
+    }
+  }
+  const bool empty = !(Ls > 0.f);
+  const float inv = empty ? 0.f : 1.f / Ls;
+  const float lse = empty ? -INFINITY : (M + log2f(Ls)) * kLn2;
+  T* dst = is_ro ? out_readout : out_all;
+  float* ldst = is_ro ? lse_readout : lse_all;
+  const int64_t orow = is_ro ? tgt : row;
+  if (dst) {
+    T* d = dst + (orow * Hq + h) * D + lane * DPL;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) d[e] = Elem<T>::from_f(o[e] * inv);
+  }
+  if (ldst && lane == 0) ldst[orow * Hq + h] = lse;
+}
+
+template <typename T, int D>
+static cudaError_t launch_comb(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
+                               void* out_all, float* lse_all, cudaStream_t s) {
+  const int with_all = (out_all || lse_all) ? 1 : 0;
+  const int64_t warps = int64_t(p.R + (with_all ? p.N : 0)) * p.desc.num_q_heads;
+  if (warps == 0) return cudaSuccess;
+  combine_kernel<T, D><<<int((warps + 3) / 4), 128, 0, s>>>(
+      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
+      static_cast<T*>(out_readout), lse_readout, static_cast<T*>(out_all), lse_all);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
+                           void* out_all, float* lse_all, cudaStream_t s) {
+  const bool bf = p.desc.dtype == PIE_BF16;
+  if (p.desc.head_dim == 128)
+    return bf ? launch_comb<__nv_bfloat16, 128>(p, out_readout, lse_readout, out_all, lse_all, s)
+              : launch_comb<float, 128>(p, out_readout, lse_readout, out_all, lse_all, s);
+  return bf ? launch_comb<__nv_bfloat16, 64>(p, out_readout, lse_readout, out_all, lse_all, s)
+            : launch_comb<float, 64>(p, out_readout, lse_readout, out_all, lse_all, s);
+}
+
+// The tensor-core kernel is not built in this configuration: the planner
+// never emits tensor-core items, so this launcher is unreachable.
+cudaError_t launch_attend_tc(const pie_fwd_plan_t&, const void*, const void*, const void*,
+                             const uint32_t*, uint32_t*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pie

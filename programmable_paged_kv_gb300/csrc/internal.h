@@ -1,0 +1,101 @@
+// Internal structures shared by the host planner and the CUDA kernels of the
+// ForwardPass hot path.  Not part of the public ABI (include/pie_fwd.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pie_fwd.h"
+
+namespace pie {
+
+// Work item of the split-KV attention kernel: the queries of rows
+// [row0, row0 + nrows) of `lane` that read kv head `kv_head` (nrows * G query
+// vectors, padded to the kernel's NQ), over the slot chunk [kv_begin, kv_end).
+// kv_begin is a multiple of kStageSlots.  Partial softmax state goes to
+// partial slots part_base .. part_base + NQ - 1.
+struct alignas(16) DecItem {
+  int32_t lane, kv_head, row0, nrows;
+  int32_t kv_begin, kv_end, part_base, pad;
+};
+
+// How the combine step finds the partials of (row, kv head): chunk c of query
+// q lives at part_base + c * stride + q_off + (h % G).
+struct alignas(16) CombEntry {
+  int32_t part_base, nchunks, stride, q_off;
+};
+
+// Work item of the tensor-core attention kernel: a tile of up to 128 query
+// vectors (rows [row0, row0 + nrows) of `lane`, G heads each, head-major
+// within a row) over kv head `kv_head`, reading slots [kv_begin, kv_end) in
+// 128-slot tiles; partial softmax state for the tile's queries goes to
+// partial slots part_base .. part_base + 127.
+struct alignas(16) TcItem {
+  int32_t lane, kv_head, row0, nrows;
+  int32_t kv_begin, kv_end, part_base, pad;
+};
+
+constexpr int kStageSlots = 64;   // slots per pipeline stage of the decode kernel
+constexpr int kWarpSlots = 16;    // slots per compute warp per stage
+constexpr int kTcTileSlots = 128; // slots per KV tile of the tensor-core kernel
+constexpr int kTcTileQueries = 128;
+
+// Device pointers into the caller's workspace, filled by the planner.
+struct DevMeta {
+  const int32_t* row_indptr;
+  const int32_t* positions;
+  const int32_t* slots;
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_ids;
+  const int32_t* fold_mode;
+  const int32_t* fold_count;
+  const int32_t* row_lane;
+  const int64_t* mask_word_indptr;  // NULL when the pass has no mask
+  const int32_t* readout;
+  const float* rope_freq;           // [d/2]
+  const DecItem* dec_items;
+  const TcItem* tc_items;
+  const CombEntry* comb;            // [N * Hkv]
+  float* part_o;                    // [num_part_slots][d] unnormalised
+  float2* part_ml;                  // [num_part_slots] (max, sum), log2 domain
+};
+
+struct PinnedBlock;
+
+}  // namespace pie
+
+struct pie_fwd_plan {
+  pie_fwd_desc desc;
+  int32_t L, N, R;
+  int32_t G;                 // q heads per kv head
+  int32_t num_pool_pages;
+  bool has_mask;
+  bool any_channel;
+  int32_t nq;                // query vectors per decode item (2, 4 or 8)
+  int32_t num_dec_items;
+  int32_t num_tc_items;
+  int64_t num_part_slots;
+  pie::DevMeta dev;
+  pie::PinnedBlock* staging;
+};
+
+namespace pie {
+
+// Kernel launchers (defined next to their kernels).  Each returns the launch
+// status; none synchronizes.
+cudaError_t launch_rope_scatter(const pie_fwd_plan_t& p, const void* q, const void* k,
+                                const void* v, void* q_rot, void* k_pool, void* v_pool,
+                                const int32_t* frozen_len, uint32_t* status, cudaStream_t s);
+cudaError_t launch_fold(const pie_fwd_plan_t& p, int32_t* frozen_len, const int32_t* channel,
+                        uint32_t* status, cudaStream_t s);
+cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
+                                 const void* v_pool, const uint32_t* mask_words,
+                                 uint32_t* status, cudaStream_t s);
+cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
+                             const void* v_pool, const uint32_t* mask_words, uint32_t* status,
+                             cudaStream_t s);
+cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
+                           void* out_all, float* lse_all, cudaStream_t s);
+
+}  // namespace pie

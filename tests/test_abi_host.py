@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/pie_fwd.h declares, and its planner's
+metadata validation agrees with the oracle's on valid and invalid passes."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from programmable_paged_kv_gb300 import abi, build, make_desc, make_meta
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return abi.load()
+
+
+def test_library_exports_every_header_function(lib):
+    names = abi.header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in abi.SIGNATURES, n
+
+
+def test_abi_version(lib):
+    assert lib.pie_fwd_abi_version() == 100
+
+
+def _ws(desc, p, num_pool_pages):
+    n = C.c_size_t(0)
+    m = make_meta(p, num_pool_pages)
+    rc = abi.load().pie_fwd_workspace_bytes(C.byref(make_desc(desc)), C.byref(m.c), C.byref(n))
+    return rc, int(n.value)
+
+
+@pytest.mark.parametrize("name", W.SMALL_NAMES)
+def test_valid_scenarios_plan_on_host(lib, name):
+    sc = W.small(name, 0)
+    for p in sc.passes:
+        rc, n = _ws(sc.desc, p, sc.num_pool_pages)
+        assert rc == abi.PIE_OK, lib.pie_fwd_last_error()
+        assert n > 0 and n % 256 == 0
+
+
+def _base():
+    desc = W.Desc(4, 2, 64, 16, W.BF16)
+    z = np.zeros((2, 4, 64), np.uint16)
+    zk = np.zeros((2, 2, 64), np.uint16)
+    p = W.Pass(row_indptr=np.array([0, 2], np.int32), positions=np.array([20, 21], np.int32),
+               slots=np.array([20, 21], np.int32), kv_len=np.array([22], np.int32),
+               page_indptr=np.array([0, 2], np.int32), page_ids=np.array([3, 1], np.int32),
+               fold_mode=np.array([W.FOLD_ALL], np.int32), fold_count=np.zeros(1, np.int32),
+               q=z, k=zk, v=zk)
+    return desc, p
+
+
+def _set(**kw):
+    def f(p):
+        for k, v in kw.items():
+            setattr(p, k, v)
+    return f
+
+
+CASES = [
+    ("ok", lambda p: None),
+    ("indptr_end", _set(row_indptr=np.array([0, 3], np.int32))),
+    ("indptr_start", _set(row_indptr=np.array([1, 2], np.int32))),
+    ("slot_past_pages", _set(slots=np.array([20, 32], np.int32))),
+    ("negative_slot", _set(slots=np.array([-1, 21], np.int32), fold_mode=np.array([0], np.int32))),
+    ("negative_position", _set(positions=np.array([-5, 21], np.int32))),
+    ("kv_len_past_pages", _set(kv_len=np.array([33], np.int32))),
+    ("negative_kv_len", _set(kv_len=np.array([-1], np.int32))),
+    ("page_outside_pool", _set(page_ids=np.array([3, 4], np.int32))),
+    ("fold_non_consecutive", _set(slots=np.array([21, 20], np.int32))),
+    ("duplicate_target", _set(slots=np.array([21, 21], np.int32), fold_mode=np.array([0], np.int32))),
+    ("unknown_fold", _set(fold_mode=np.array([9], np.int32))),
+    ("fold_count_range", _set(fold_mode=np.array([2], np.int32), fold_count=np.array([3], np.int32))),
+    ("fold_count_ok", _set(fold_mode=np.array([2], np.int32), fold_count=np.array([2], np.int32))),
+    ("readout_range", _set(readout=np.array([0, 2], np.int32))),
+    ("readout_ok", _set(readout=np.array([1, 0, 1], np.int32))),
+    ("mask_too_short", _set(mask_word_indptr=np.array([0, 1, 1], np.int64))),
+    ("mask_ok", _set(mask_word_indptr=np.array([0, 1, 2], np.int64))),
+    ("mask_decreasing", _set(mask_word_indptr=np.array([0, 2, 1], np.int64))),
+]
+
+
+@pytest.mark.parametrize("name,mutate", CASES, ids=[c[0] for c in CASES])
+def test_validation_agrees_with_oracle(lib, name, mutate):
+    desc, p = _base()
+    mutate(p)
+    rc_lib, _ = _ws(desc, p, 4)
+    rc_orc = O.validate(desc, p, num_pool_pages=4)
+    assert rc_lib == rc_orc, (name, rc_lib, rc_orc, lib.pie_fwd_last_error())
+
+
+def test_unsupported_shapes_are_refused(lib):
+    _, p = _base()
+    for desc in (W.Desc(4, 2, 96, 16, W.BF16), W.Desc(4, 2, 64, 12, W.BF16),
+                 W.Desc(32, 2, 64, 16, W.BF16)):
+        rc, _ = _ws(desc, p, 4)
+        assert rc == abi.PIE_EUNSUPPORTED
+    rc, _ = _ws(W.Desc(4, 3, 64, 16, W.BF16), p, 4)
+    assert rc == abi.PIE_EINVAL
+
+
+def test_empty_pass_plans(lib):
+    desc = W.Desc(4, 2, 64, 16, W.BF16)
+    e = np.zeros(0, np.int32)
+    z = np.zeros((0, 4, 64), np.uint16)
+    p = W.Pass(row_indptr=np.zeros(1, np.int32), positions=e, slots=e, kv_len=e,
+               page_indptr=np.zeros(1, np.int32), page_ids=e, fold_mode=e, fold_count=e,
+               q=z, k=z, v=z)
+    rc, n = _ws(desc, p, 0)
+    assert rc == abi.PIE_OK and n >= 0

@@ -303,6 +303,33 @@ def decode_batch(seed: int = 0, lanes: int = 64, c_lo: int = 512, c_hi: int = 40
                            "q/k/v ~ N(0,1) bf16, pages permuted")
 
 
+def decode_loop_meta(seed: int = 0, lanes: int = 64, steps: int = 64, c_lo: int = 512,
+                     c_hi: int = 4096, num_pool_pages: int = 65536,
+                     desc: Optional[Desc] = None):
+    """The decode batch continued for `steps` single-row passes: pass t puts
+    each lane's row at position/slot C+t, reads C+t+1 slots and folds it.
+    Returns (desc, C, lane_pages, pass_meta(t) -> Pass without q/k/v)."""
+    desc = desc or Desc(32, 8, 128, 16, BF16)
+    r_meta = _rngs(seed, 2)[0]
+    C = r_meta.integers(c_lo, c_hi + 1, size=lanes).astype(np.int32)
+    counts = [_pages_for(int(c) + steps, desc.page_size) for c in C]
+    lane_pages = _permuted_pool(r_meta, num_pool_pages, counts)
+    page_indptr = np.zeros(lanes + 1, np.int32)
+    page_indptr[1:] = np.cumsum(counts)
+    page_ids = np.concatenate(lane_pages).astype(np.int32)
+    e = np.zeros((0,), np.uint16)
+
+    def pass_meta(t: int) -> Pass:
+        pos = (C + t).astype(np.int32)
+        return Pass(row_indptr=np.arange(lanes + 1, dtype=np.int32), positions=pos,
+                    slots=pos.copy(), kv_len=(pos + 1).astype(np.int32),
+                    page_indptr=page_indptr, page_ids=page_ids,
+                    fold_mode=np.full(lanes, FOLD_ALL, np.int32),
+                    fold_count=np.zeros(lanes, np.int32), q=e, k=e, v=e)
+
+    return desc, C, lane_pages, pass_meta
+
+
 # ---- configuration 3: guidance lane pairs ---------------------------------------
 def guidance_pairs(seed: int = 0, pairs: int = 32, prefix: int = 1024, prefill: int = 64,
                    decodes: int = 16, num_pool_pages: int = 4096,
