@@ -170,7 +170,9 @@ def test_frozen_write_fold_gap_and_channel_clamp_status():
     p = _mk_pass(desc, lanes, rng, fold=W.FOLD_CHANNEL, channel=[1, 9, -3])
     p.slots = np.array([5, 6, 10, 11, 12, 13], np.int32)
     p.positions = p.slots.copy()
-    sc = _one_pass_scenario(desc, p, [10, 10, 11], 3, [10, 10, 11])
+    # lane 2 holds finite K/V in slot 11 (read by its rows) although only
+    # slots below 11 are frozen
+    sc = _one_pass_scenario(desc, p, [10, 10, 11], 3, [10, 10, 12])
     gpu, orc = _run_both(sc)
     compare_scenario(sc, gpu, orc)
     st = gpu[3][0]["status"]
