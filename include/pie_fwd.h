@@ -76,6 +76,8 @@ extern "C" {
 #define PIE_STATUS_FOLD_CLAMP 2u   /* a channel count outside [0, n] was clamped          */
 #define PIE_STATUS_FOLD_GAP 8u     /* a folding lane's first slot != its frozen length    */
 #define PIE_STATUS_TIMEOUT 16u     /* a kernel's bounded wait expired; outputs invalid    */
+#define PIE_STATUS_NOALLOC_TRUNC 32u /* no-allocation decode: a kv_len above max_kv_len was
+                                        cut to max_kv_len                                   */
 
 /* Static description of the attention layer. */
 typedef struct pie_fwd_desc {
@@ -188,6 +190,42 @@ const char* pie_fwd_last_error(void);
 
 /* ABI version of this header (major * 100 + minor). */
 int pie_fwd_abi_version(void);
+
+/* Decode attention that allocates nothing.  The Pie pages have no
+ * counterpart for this call: it is a deployment variant of the split-KV
+ * attention and combine steps of pie_fwd_attend for callers that cannot
+ * allocate device memory when they launch attention (for example code
+ * running under a foreign memory manager with a fixed device budget, or a
+ * host path that must not take the allocator's locks), and so cannot provide
+ * the plan workspace.
+ *
+ * One query row per lane: row l attends, with default visibility, over slots
+ * [0, min(kv_len[l], slots[l] + 1)) of lane l's working set, exactly as
+ * pie_fwd_attend does for a plan whose lanes have one row each.
+ *   slots, kv_len: device int32 [num_lanes]; page_indptr: device int32
+ *   [num_lanes + 1]; page_ids: device int32 (pool layout as above);
+ *   q_rot: device [num_lanes][Hq][d] (e.g. from pie_fwd_append_kv);
+ *   k_pool, v_pool: device pools, read only;
+ *   out: device [num_lanes][Hq][d] in the dtype; lse: device float
+ *   [num_lanes][Hq] or NULL; status: device uint32 or NULL.
+ *   max_kv_len: host upper bound of kv_len (sizes the launch); larger device
+ *   values are cut to it and set PIE_STATUS_NOALLOC_TRUNC.
+ * Scratch lives in one static __device__ array of 16 MiB that every GPU
+ * loading the library holds until exit; a call needing more
+ * (num_lanes * num_kv_heads * ceil(max_kv_len / 512) * partial states)
+ * returns PIE_ERANGE.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, so make
+ * it before any stream capture.  Every call reuses the same array: calls
+ * whose executions overlap on the GPU race; issue them on one stream.
+ * Calls no allocator (no cudaMalloc, cudaFree or allocating library).
+ * Errors: PIE_EINVAL (NULL pointer, bad head counts, negative size),
+ * PIE_EUNSUPPORTED (shape), PIE_ERANGE (scratch), PIE_ECUDA (launch). */
+int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t num_lanes,
+                                  int32_t max_kv_len, const int32_t* slots,
+                                  const int32_t* kv_len, const int32_t* page_indptr,
+                                  const int32_t* page_ids, const void* q_rot,
+                                  const void* k_pool, const void* v_pool, void* out,
+                                  float* lse, uint32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,7 @@ PIE_STATUS_FROZEN_WRITE = 1
 PIE_STATUS_FOLD_CLAMP = 2
 PIE_STATUS_FOLD_GAP = 8
 PIE_STATUS_TIMEOUT = 16
+PIE_STATUS_NOALLOC_TRUNC = 32
 
 
 class pie_fwd_desc(C.Structure):
@@ -65,6 +66,8 @@ SIGNATURES = {
     "pie_fwd_plan_destroy": (None, [_P]),
     "pie_fwd_last_error": (C.c_char_p, []),
     "pie_fwd_abi_version": (C.c_int, []),
+    "pie_fwd_decode_attend_noalloc": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32, C.c_int32,
+                                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 

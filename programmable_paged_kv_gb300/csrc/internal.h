@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "../../include/pie_fwd.h"
 
 namespace pie {
@@ -97,5 +99,9 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
                              cudaStream_t s);
 cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
                            void* out_all, float* lse_all, cudaStream_t s);
+
+// Records `msg` as the calling thread's last error (pie_fwd_last_error) and
+// returns `code`.
+int set_last_error(int code, const std::string& msg);
 
 }  // namespace pie

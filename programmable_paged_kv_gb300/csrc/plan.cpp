@@ -36,6 +36,8 @@ static int fail(int code, const std::string& msg) {
   return code;
 }
 
+int set_last_error(int code, const std::string& msg) { return fail(code, msg); }
+
 // ---------------------------------------------------------------------------
 // pinned staging pool: plans copy their metadata from pinned host memory so
 // that the copy is truly asynchronous; a block returns to the pool when its
