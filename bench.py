@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--pool-pages", type=int, default=65536,
+                    help="pages per K/V pool (smaller pools serve profiler captures)")
     return ap.parse_args()
 
 
@@ -271,11 +273,13 @@ def run_ours(args, ws, rank, local, pg):
     load()
     K, Wm = args.steps, args.warmup
     total_steps = 2 * (K + Wm) + 2
-    desc, C, lane_pages, pass_meta = W.decode_loop_meta(seed=args.seed + rank, steps=total_steps)
+    NP = args.pool_pages
+    desc, C, lane_pages, pass_meta = W.decode_loop_meta(seed=args.seed + rank, steps=total_steps,
+                                                        num_pool_pages=NP)
     cdesc = make_desc(desc)
     dev = torch.device("cuda", local)
     torch.manual_seed(1000 + args.seed + rank)
-    shape = (65536, desc.num_kv_heads, desc.page_size, desc.head_dim)
+    shape = (NP, desc.num_kv_heads, desc.page_size, desc.head_dim)
     k_pool = torch.randn(shape, dtype=torch.bfloat16, device=dev)
     v_pool = torch.randn(shape, dtype=torch.bfloat16, device=dev)
     frozen = torch.from_numpy(C.copy()).to(dev)
@@ -288,7 +292,7 @@ def run_ours(args, ws, rank, local, pg):
     q_rot = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
     out = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((L, Hq), dtype=torch.float32, device=dev)
-    metas = [make_meta(pass_meta(t), 65536) for t in range(total_steps)]
+    metas = [make_meta(pass_meta(t), NP) for t in range(total_steps)]
     from programmable_paged_kv_gb300 import workspace_bytes
     ws_bytes = max(workspace_bytes(cdesc, metas[t]) for t in (0, total_steps - 1))
     workspace = torch.empty(ws_bytes + 4096, dtype=torch.uint8, device=dev)
@@ -397,7 +401,7 @@ def run_ours(args, ws, rank, local, pg):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1, "q_heads": Hq,
                    "kv_heads": Hkv, "head_dim": D, "page_size": desc.page_size,
-                   "pool_pages": 65536, "kv_len": "C+t+1, C~U[512,4096]",
+                   "pool_pages": NP, "kv_len": "C+t+1, C~U[512,4096]",
                    "l2": "inputs larger than L2 (~600 MB of KV read per step)",
                    "step": "plan+append_kv+attend+fold"},
         "gpu_launches": 4 * K,

@@ -436,11 +436,4 @@ cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* ls
             : launch_comb<float, 64>(p, out_readout, lse_readout, out_all, lse_all, s);
 }
 
-// The tensor-core kernel is not built in this configuration: the planner
-// never emits tensor-core items, so this launcher is unreachable.
-cudaError_t launch_attend_tc(const pie_fwd_plan_t&, const void*, const void*, const void*,
-                             const uint32_t*, uint32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
 }  // namespace pie

@@ -125,13 +125,13 @@ static int choose_chunk(int64_t total_slots_x_heads) {
   int64_t ch = (total_slots_x_heads + kTargetItems - 1) / kTargetItems;
   ch = std::max<int64_t>(ch, 256);
   ch = std::min<int64_t>(ch, 4096);
-  ch = (ch + kStageSlots - 1) / kStageSlots * kStageSlots;
+  ch = (ch + kTcTileSlots - 1) / kTcTileSlots * kTcTileSlots;  // whole tiles of both kernels
   return static_cast<int>(ch);
 }
 
 // Lanes with at least this many query vectors per kv head use the
 // tensor-core kernel (bf16 only).
-static bool g_tc_enabled = false;
+static bool g_tc_enabled = true;
 constexpr int kTcMinQueries = 16;
 
 static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, HostPlan& H) {
@@ -254,7 +254,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
     for (int r = r0; r < r1; ++r) mx = std::max(mx, M.slots[r]);
     return std::min(kv, mx + 1);
   };
-  const bool tc_ok = g_tc_enabled && D.dtype == PIE_BF16;
+  const bool tc_ok = g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128;
   int64_t work = 0;
   for (int l = 0; l < L; ++l) work += static_cast<int64_t>(M.kv_len[l]) * Hkv;
   const int CH = choose_chunk(work);
