@@ -54,6 +54,11 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="decode_batch",
+                    choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
+                             "masked_tova", "decode_pass"],
+                    help="decode_batch (default) is the benchmark line; the others time one "
+                         "pass of another configuration")
     ap.add_argument("--pool-pages", type=int, default=65536,
                     help="pages per K/V pool (smaller pools serve profiler captures)")
     return ap.parse_args()
@@ -427,11 +432,155 @@ def run_ours(args, ws, rank, local, pg):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------------ other workloads
+def pass_accounting(p, desc):
+    """(attended tokens, attention algorithmic bytes, attention FLOPs) of a
+    pass with default or mask visibility.  Bytes count each distinct visible
+    physical KV slot once per kv head (shared prefix pages once), q_rot read,
+    readout rows written, mask words and page-table entries read."""
+    b = W.ELEM_BYTES[desc.dtype]
+    d, hq, hkv, P = desc.head_dim, desc.num_q_heads, desc.num_kv_heads, desc.page_size
+    vis_count = 0
+    phys = []
+    mask_bytes = 0
+    for l in range(p.num_lanes):
+        r0, r1 = int(p.row_indptr[l]), int(p.row_indptr[l + 1])
+        kv = int(p.kv_len[l])
+        if r1 == r0 or kv == 0:
+            continue
+        if p.mask_word_indptr is None:
+            ext = np.minimum(kv, p.slots[r0:r1].astype(np.int64) + 1)
+            vis_count += int(ext.sum())
+            lane_vis = np.arange(int(ext.max()))
+        else:
+            nw = (kv + 31) // 32
+            union = np.zeros(nw, np.uint32)
+            for r in range(r0, r1):
+                w = p.mask_words[p.mask_word_indptr[r]:p.mask_word_indptr[r] + nw].copy()
+                if kv % 32:
+                    w[-1] &= np.uint32((1 << (kv % 32)) - 1)
+                vis_count += int(np.unpackbits(w.view(np.uint8)).sum())
+                union |= w
+            mask_bytes += (r1 - r0) * nw * 4
+            bits = np.unpackbits(union.view(np.uint8), bitorder="little")[:kv]
+            lane_vis = np.nonzero(bits)[0]
+        pages = p.page_ids[p.page_indptr[l]:p.page_indptr[l + 1]].astype(np.int64)
+        phys.append(pages[lane_vis // P] * P + lane_vis % P)
+    distinct = int(np.unique(np.concatenate(phys)).size) if phys else 0
+    R = p.readout.size if p.readout is not None else int((np.diff(p.row_indptr) > 0).sum())
+    npages = int(sum((int(k) + P - 1) // P for k in p.kv_len))
+    byts = (distinct * hkv * 2 * d * b + p.num_rows * hq * d * b + R * hq * (d * b + 4)
+            + mask_bytes + npages * 4)
+    flops = 4 * d * hq * vis_count
+    return vis_count, byts, flops
+
+
+WORKLOADS = {
+    "guidance_prefill": lambda s: W.guidance_pairs(s, decodes=0),
+    "spec_verify": lambda s: W.spec_verify(s),
+    "masked_window": lambda s: W.masked_long(s, "window"),
+    "masked_tova": lambda s: W.masked_long(s, "tova"),
+    "decode_pass": lambda s: W.decode_batch(s),
+}
+
+
+def run_workload(args, local):
+    """Time one pass of another configuration (first pass of its scenario);
+    frozen lengths are restored before every step so each step is identical."""
+    import torch
+    from programmable_paged_kv_gb300 import ForwardPlan, build, make_desc, make_meta, runner
+    torch.cuda.set_device(local)
+    build()
+    sc = WORKLOADS[args.workload](args.seed)
+    d = sc.desc
+    p = sc.passes[0]
+    desc = make_desc(d)
+    pools = runner.DevicePools(sc)
+    frozen0 = torch.from_numpy(sc.frozen_len0.astype(np.int32)).cuda()
+    frozen = frozen0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tdt = torch.bfloat16 if d.dtype == W.BF16 else torch.float32
+    N, Hq, D = p.num_rows, d.num_q_heads, d.head_dim
+    q = runner.to_device(p.q, d.dtype)
+    k = runner.to_device(p.k, d.dtype)
+    v = runner.to_device(p.v, d.dtype)
+    q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+    meta = make_meta(p, sc.num_pool_pages)
+    from programmable_paged_kv_gb300 import workspace_bytes
+    ws = torch.empty(workspace_bytes(desc, meta) + 4096, dtype=torch.uint8, device="cuda")
+    plan0 = ForwardPlan(desc, meta, workspace=ws)
+    R = plan0.num_readout
+    plan0.close()
+    out = torch.empty((R, Hq, D), dtype=tdt, device="cuda")
+    lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+    mw = None if p.mask_words is None else torch.from_numpy(p.mask_words.view(np.int32)).cuda()
+    chan = None if p.channel is None else torch.from_numpy(p.channel.astype(np.int32)).cuda()
+    stream = torch.cuda.current_stream()
+    live = []
+    K, Wm = args.steps, args.warmup
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+
+    def step(e=None):
+        frozen.copy_(frozen0, non_blocking=True)
+        plan = ForwardPlan(desc, meta, workspace=ws)
+        plan.append_kv(q, k, v, q_rot, pools.k, pools.v, frozen, status)
+        if e is not None:
+            e[0].record(stream)
+        plan.attend(q_rot, pools.k, pools.v, mw, out, lse, None, None, status)
+        if e is not None:
+            e[1].record(stream)
+        plan.fold(frozen, chan, status)
+        live.append(plan)
+        if len(live) > 4:
+            live.pop(0).close()
+
+    for _ in range(Wm):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    el = t0.elapsed_time(t1) / 1e3
+    att = sorted(a.elapsed_time(b) for a, b in ev)
+    att_med = att[len(att) // 2] / 1e3
+    tok, byts, flops = pass_accounting(p, d)
+    hbm, kind = peaks()
+    try:
+        tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        tf = 1900.0
+    t_roof = max(byts / (hbm * 1e9), flops / (tf * 1e12))
+    line = {"workload": args.workload, "metric": METRIC, "unit": UNIT,
+            "value": tok * K / el, "ms_per_step": 1e3 * el / K, "steps": K, "warmup": Wm,
+            "attend_ms_median": att_med * 1e3, "attended_tokens_per_step": tok,
+            "attend_alg_bytes": byts, "attend_alg_flops": flops,
+            "attend_hbm_gbs": byts / att_med / 1e9, "attend_hbm_frac": byts / att_med / 1e9 / hbm,
+            "attend_tflops": flops / att_med / 1e12, "attend_tensor_frac": flops / att_med / 1e12 / tf,
+            "attend_roofline_frac": t_roof / att_med, "status": int(status.item()),
+            "peaks": {"hbm_gbs": hbm, "bf16_tflops": tf, "kind": kind}}
+    if clk:
+        line["clocks"] = clk
+    for pl in live:
+        pl.close()
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     ws, rank, local, pg = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.workload != "decode_batch":
+        run_workload(args, local)
     else:
         run_ours(args, ws, rank, local, pg)
     if pg is not None:
