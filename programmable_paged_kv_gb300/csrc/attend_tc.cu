@@ -1,28 +1,39 @@
 // Step 2-3 of a ForwardPass for lanes with many query vectors per kv head
 // (prefill rows, speculative-verify drafts, masked prefill): grouped-query
 // attention over paged K/V on the 5th-generation tensor cores (Pie "The
-// forward pass": State geometry kv_len; Attention masks).
+// forward pass": State geometry kv_len; Attention masks; Readouts).
 //
-// One CTA handles a work item: up to 128 query vectors (the G heads of a kv
-// group for up to 128/G consecutive rows of one lane, head-minor) against
-// one chunk of the lane's slots, in 128-slot KV tiles.
-//   warp 0  TMA producer: the query tile once (4-D tensor map over q_rot
-//           [N][Hkv][G][d]), then per KV tile the K and V blocks of every
-//           page in the tile (2-D tensor maps over the pools, one 64-column
-//           box per half of d), 128-byte swizzled, double-buffered;
-//   warp 1  allocates 512 TMEM columns and issues, from one thread,
-//           S = Q K^T (M=128, N=128, K=16 per instruction, operands in shared
-//           memory, fp32 accumulator in TMEM; two S buffers so the next
-//           tile's scores overlap this tile's softmax) and O += P V (P from
-//           shared memory, V used MN-major straight from its tile);
-//           tcgen05.commit arrives on mbarriers;
-//   warps 2-5  softmax: each thread owns one query row (its TMEM lane),
-//           reads 128 scores with one tcgen05.ld, applies the row's
-//           visibility (slot-causal or its mask words), keeps the online
-//           max/sum in the log2 domain, rescales O in TMEM when the max
-//           grows, and writes P (bf16, swizzled) for the P.V product.
-// At the end each thread writes its row's partial state (max, sum and the
-// unnormalised output) for the combine step.  Every wait is bounded.
+// One CTA handles a work item: NT (1 or 2) tiles of 128 query vectors (the G
+// heads of a kv group for 128/G consecutive rows of one lane per tile,
+// head-minor) against one chunk of the lane's slots, in 128-slot KV tiles.
+// With NT = 2 both query tiles share every K/V tile, so the KV chunk is read
+// once for 256 query vectors.
+//   warp 0   TMA producer: the query tiles once (4-D tensor map over q_rot
+//            viewed as [N][Hkv][G][d]), then per KV tile the K and V blocks
+//            of every page in the tile (2-D tensor maps over the pools, one
+//            64-column box per half of d, 128-byte swizzle) into an NS-deep
+//            ring of stages;
+//   warp 1   allocates TMEM and, from one thread, issues for every KV tile
+//            S_t = Q_t K^T (M=128, N=128, operands in shared memory) for each
+//            query tile, then O_t += P_t V with P_t read from TMEM (it
+//            overwrites the first half of S_t's columns as packed bf16) and V
+//            used MN-major straight from its tile; tcgen05.commit arrives on
+//            mbarriers.  tcgen05.mma issued by one thread execute in order,
+//            so S_t of the next tile never overwrites P_t before P_t V reads
+//            it;
+//   warps 2+ one 4-warp softmax group per query tile: each thread owns one
+//            query row (its TMEM lane), loads its 128 scores with one
+//            tcgen05.ld, applies the row's visibility (slot-causal or its
+//            mask words; tiles visible in full skip the per-column test),
+//            keeps the online max/sum in the log2 domain (the max used for
+//            the exponent only moves when the tile max exceeds it by more
+//            than 2^8, so O is rarely rescaled), rescales O in TMEM when it
+//            does move, and stores P as bf16 pairs into TMEM.  Warps whose
+//            32 query rows are all padding skip the work.
+// At the end each thread writes its row's output: normalised to bf16 plus lse
+// when the item covers the row's whole visible range, else its partial state
+// (max, sum, unnormalised output) for the combine step.  Every wait is
+// bounded in time.
 
 #include <cuda.h>
 
@@ -35,25 +46,29 @@ namespace pie {
 
 namespace tc {
 
-constexpr int kThreads = 192;
-constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes: one half of d for a tile
-constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes: one half of d for one tile
 
+template <int NT, int NS>
 struct __align__(1024) Smem {
-  uint8_t q[2][kHalfBytes];        // [half of d][query][128 B]
-  uint8_t k[2][2][kHalfBytes];     // [stage][half of d][slot][128 B]
-  uint8_t v[2][2][kHalfBytes];     // [stage][half of d][slot][128 B]
-  uint8_t p[2][kHalfBytes];        // [half of slots][query][128 B]
+  uint8_t q[NT][2][kHalfBytes];   // [query tile][half of d][query][128 B]
+  uint8_t k[NS][2][kHalfBytes];   // [stage][half of d][slot][128 B]
+  uint8_t v[NS][2][kHalfBytes];   // [stage][half of d][slot][128 B]
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done;
+  uint64_t kv_full[NS], kv_empty[NS];
+  uint64_t s_full[NT], p_full[NT], o_done[NT];
   uint32_t tmem_base;
 };
 
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
-// address, leading and stride byte offsets in 16-byte units, descriptor
-// version 1, layout type 2 = 128-byte swizzle).
+template <int NT>
+struct Cfg {
+  static constexpr int NS = NT == 1 ? 3 : 2;            // KV stages that fit beside Q
+  static constexpr int kThreads = 64 + 128 * NT;
+  static constexpr uint32_t kTmemCols = NT == 1 ? 256 : 512;  // per tile: S/P [0,128), O [128,256)
+};
+
+// Shared-memory matrix descriptor, 128-byte swizzle (start address, leading
+// and stride byte offsets in 16-byte units, descriptor version 1, layout
+// type 2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t sdesc(const void* p, uint32_t lbo, uint32_t sbo) {
   const uint32_t a = smem_u32(p);
   uint64_t d = uint64_t((a >> 4) & 0x3FFFu);
@@ -78,12 +93,23 @@ __device__ __forceinline__ void fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                    uint32_t accumulate) {
+// D (TMEM) (+)= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                       uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM) * B (shared memory)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
       : "memory");
 }
 
@@ -108,6 +134,10 @@ __device__ __forceinline__ void tmem_st128(uint32_t taddr, const float* f) {
   asm volatile(PIE_TMEM_ST128_ASM ::"r"(taddr), PIE_TMEM_ST_INS : "memory");
 }
 
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t* r) {
+  asm volatile(PIE_TMEM_ST64_ASM ::"r"(taddr), PIE_TMEM_ST64_INS : "memory");
+}
+
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
                                        uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -126,38 +156,51 @@ __device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* map, int x,
       : "memory");
 }
 
+struct Out {
+  __nv_bfloat16* out_readout;
+  float* lse_readout;
+  __nv_bfloat16* out_all;
+  float* lse_all;
+};
+
 }  // namespace tc
 
-__global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(
-    DevMeta m, int G, int Hkv, int P, float scale_log2, const uint32_t* __restrict__ mask_words,
-    uint32_t* status, const __grid_constant__ CUtensorMap qmap,
-    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+template <int NT>
+__global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
+    DevMeta m, int G, int Hq, int Hkv, int P, float scale_log2,
+    const uint32_t* __restrict__ mask_words, tc::Out out, uint32_t* status,
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap vmap) {
   using namespace tc;
+  constexpr int NS = Cfg<NT>::NS;
+  constexpr int D = 128;
+  constexpr float kLn2 = 0.6931471805599453f;
+  using SM = Smem<NT, NS>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SM& S = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcItem it = m.tc_items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = it.kv_begin, ke = it.kv_end;
   const int T = ke > kb ? (ke - kb + kTcTileSlots - 1) / kTcTileSlots : 0;
-  const int nqv = it.nrows * G;
-  constexpr int D = 128;
+  const int nqv = it.nrows * G;  // valid query vectors of the item
 
   if (threadIdx.x == 0) {
     mbar_init(&S.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&S.kv_full[i], 1);
       mbar_init(&S.kv_empty[i], 1);
-      mbar_init(&S.s_full[i], 1);
-      mbar_init(&S.s_free[i], 4);
     }
-    mbar_init(&S.p_full, 4);
-    mbar_init(&S.o_done, 1);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(&S.s_full[t], 1);
+      mbar_init(&S.p_full[t], 4);
+      mbar_init(&S.o_done[t], 1);
+    }
     fence_barrier_init();
   }
   if (warp == 1 && T > 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&S.tmem_base)),
-                 "r"(kTmemCols)
+                 "r"(Cfg<NT>::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -167,27 +210,21 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(
   const uint32_t tmem = S.tmem_base;
   bool bad = false;
 
-  if (T == 0) {
-    // nothing visible in this chunk: empty partial states
-    if (threadIdx.x < nqv) {
-      float* po = m.part_o + int64_t(it.part_base + threadIdx.x) * D;
-      for (int c = 0; c < D; ++c) po[c] = 0.f;
-      m.part_ml[it.part_base + threadIdx.x] = make_float2(-INFINITY, 0.f);
-    }
-    return;
-  }
-
   if (warp == 0) {
     // ---------------- TMA producer ------------------------------------------
-    if (lane == 0) {
+    if (lane == 0 && T > 0) {
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(&S.q_full, 2 * kHalfBytes);
-      tma_4d(S.q[0], &qmap, 0, 0, it.kv_head, it.row0, &S.q_full);
-      tma_4d(S.q[1], &qmap, 64, 0, it.kv_head, it.row0, &S.q_full);
+      mbar_arrive_expect_tx(&S.q_full, NT * 2 * kHalfBytes);
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+          tma_4d(S.q[t][a], &qmap, 64 * a, 0, it.kv_head, it.row0 + t * (kTcTileQueries / G),
+                 &S.q_full);
       const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
-      for (int j = 0; j < T && !bad; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&S.kv_empty[st], ((j >> 1) - 1) & 1)) {
+      for (int j = 0; j < T; ++j) {
+        const int st = j % NS;
+        if (j >= NS && !mbar_wait(&S.kv_empty[st], ((j / NS) - 1) & 1)) {
           bad = true;
           break;
         }
@@ -197,166 +234,220 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(
         mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
         for (int pg = p0; pg <= p1; ++pg) {
           // first row of (page, kv head) in the [page * Hkv + head][slot] view
-          const int yy = (pages[pg] * Hkv + it.kv_head) * P;
+          const int y = (pages[pg] * Hkv + it.kv_head) * P;
           const int off = (pg * P - ts) * 128;
 #pragma unroll
           for (int a = 0; a < 2; ++a) {
-            tma_2d(S.k[st][a] + off, &kmap, 64 * a, yy, &S.kv_full[st], pol);
-            tma_2d(S.v[st][a] + off, &vmap, 64 * a, yy, &S.kv_full[st], pol);
+            tma_2d(S.k[st][a] + off, &kmap, 64 * a, y, &S.kv_full[st], pol);
+            tma_2d(S.v[st][a] + off, &vmap, 64 * a, y, &S.kv_full[st], pol);
           }
         }
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ---------------------------------------------
-    if (lane == 0) {
+    if (lane == 0 && T > 0) {
       constexpr uint32_t ID_S = idesc(128, 128, false);
       constexpr uint32_t ID_O = idesc(128, 128, true);
-      const uint32_t tO = tmem + 256;
-      auto pv = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(&S.p_full, i & 1)) return false;
-        fence_after();
-        const int valid = min(kTcTileSlots, ke - (kb + i * kTcTileSlots));
-        const int ksteps = (valid + 15) >> 4;
-        for (int k = 0; k < ksteps; ++k) {
-          const uint64_t a = sdesc(S.p[k >> 2] + (k & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc(S.v[st][0] + k * 2048, kHalfBytes, 1024);
-          mma(tO, a, b, ID_O, (i > 0 || k > 0) ? 1u : 0u);
-        }
-        commit(&S.o_done);
-        commit(&S.kv_empty[st]);
-        return true;
-      };
       if (!mbar_wait(&S.q_full, 0)) bad = true;
       for (int j = 0; j < T && !bad; ++j) {
-        const int st = j & 1, b = j & 1;
-        if (!mbar_wait(&S.kv_full[st], (j >> 1) & 1)) { bad = true; break; }
-        if (j >= 2 && !mbar_wait(&S.s_free[b], ((j >> 1) - 1) & 1)) { bad = true; break; }
+        const int st = j % NS;
+        if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) { bad = true; break; }
         fence_after();
-        const uint32_t tS = tmem + b * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(S.q[k >> 2] + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc(S.k[st][k >> 2] + (k & 3) * 32, 16, 1024);
-          mma(tS, a, bd, ID_S, k > 0 ? 1u : 0u);
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t a = sdesc(S.q[t][k >> 2] + (k & 3) * 32, 16, 1024);
+            const uint64_t b = sdesc(S.k[st][k >> 2] + (k & 3) * 32, 16, 1024);
+            mma_ss(tmem + 256 * t, a, b, ID_S, k > 0 ? 1u : 0u);
+          }
+          commit(&S.s_full[t]);
         }
-        commit(&S.s_full[b]);
-        if (j >= 1 && !pv(j - 1)) { bad = true; break; }
+        const int valid = min(kTcTileSlots, ke - (kb + j * kTcTileSlots));
+        const int ksteps = (valid + 15) >> 4;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (!mbar_wait(&S.p_full[t], j & 1)) { bad = true; break; }
+          fence_after();
+          for (int k = 0; k < ksteps; ++k) {
+            const uint64_t b = sdesc(S.v[st][0] + k * 2048, kHalfBytes, 1024);
+            mma_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * k, b, ID_O,
+                   (j > 0 || k > 0) ? 1u : 0u);
+          }
+          commit(&S.o_done[t]);
+        }
+        commit(&S.kv_empty[st]);
       }
-      if (!bad && !pv(T - 1)) bad = true;
     }
-  } else {
-    // ---------------- softmax warps (one query row per thread) --------------
-    const int quad = warp & 3;
-    const int qm = quad * 32 + lane;  // query index == TMEM lane
-    const bool valid_q = qm < nqv;
-    const int row = it.row0 + (valid_q ? qm : 0) / G;
-    const int row_slot = valid_q ? m.slots[row] : -1;
+  } else if (T > 0) {
+    // ---------------- softmax groups: thread = query row ---------------------
+    const int t = (warp - 2) >> 2;      // query tile of this group
+    const int quad = warp & 3;          // TMEM lane quadrant of this warp
+    const int qm = quad * 32 + lane;    // query row within the tile == TMEM lane
+    const int q = t * kTcTileQueries + qm;
+    const bool valid_q = q < nqv;
+    const bool warp_live = __any_sync(0xffffffffu, valid_q);
+    const int row = it.row0 + (valid_q ? q : 0) / G;
+    const int head = it.kv_head * G + (valid_q ? q : 0) % G;
+    const int row_slot = valid_q ? m.slots[row] : INT_MAX;
     const int64_t mbase = (mask_words && valid_q) ? m.mask_word_indptr[row] : 0;
-    const uint32_t tl = tmem + (uint32_t(quad * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
-    float s[128];
+    const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + 256 * t;
+    const uint32_t tS = lane_base, tO = lane_base + 128;
+    float m_used = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
       const int ts = kb + j * kTcTileSlots;
-      uint32_t words[4] = {0u, 0u, 0u, 0u};
+      uint32_t words[4] = {~0u, ~0u, ~0u, ~0u};
       if (mask_words && valid_q) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (ts + 32 * i < ke) words[i] = mask_words[mbase + (ts >> 5) + i];
+        for (int i = 0; i < 4; ++i) words[i] = ts + 32 * i < ke ? mask_words[mbase + (ts >> 5) + i] : 0u;
       }
-      if (!mbar_wait(&S.s_full[b], (j >> 1) & 1)) { bad = true; break; }
+      if (!mbar_wait(&S.s_full[t], j & 1)) { bad = true; break; }
       fence_after();
-      tmem_ld128(tl + b * 128, s);
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.s_free[b]);
-      float tmax = -INFINITY;
+      if (warp_live) {
+        float s[128];
+        tmem_ld128(tS, s);
+        // a tile every column of which every live row of the warp sees
+        const bool all_vis = (ts + kTcTileSlots <= ke) &&
+                             (mask_words ? ((words[0] & words[1] & words[2] & words[3]) == ~0u)
+                                         : (ts + kTcTileSlots - 1 <= row_slot));
+        float mx = -INFINITY;
+        if (__all_sync(0xffffffffu, all_vis || !valid_q)) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const int sa = ts + c;
-        const bool vis = valid_q && sa < ke &&
-                         (mask_words ? ((words[c >> 5] >> (c & 31)) & 1u) != 0 : sa <= row_slot);
-        s[c] = vis ? s[c] * scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[c]);
-      }
-      const float m_new = fmaxf(m_run, tmax);
-      const bool none = m_new == -INFINITY;
-      const float alpha = none ? 1.f : exp2f(m_run - m_new);
-      float rs = 0.f;
+          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        } else {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = none ? 0.f : exp2f(s[c] - m_new);
-        s[c] = p;
-        rs += p;
-      }
-      l_run = l_run * alpha + rs;
-      m_run = m_new;
-      // P.V of the previous tile must be done: it reads the P buffer and
-      // accumulates into O, both of which change below
-      if (j >= 1) {
-        if (!mbar_wait(&S.o_done, (j - 1) & 1)) { bad = true; break; }
-        fence_after();
-      }
-      // P row -> shared memory, bf16, 128-byte swizzle: [slot half][query][128 B]
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint8_t* rowp = S.p[h] + qm * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(s[h * 64 + ch * 8 + 2 * e],
-                                                      s[h * 64 + ch * 8 + 2 * e + 1]);
-            w[e] = *reinterpret_cast<uint32_t*>(&v2);
+          for (int c = 0; c < 128; ++c) {
+            const int sa = ts + c;
+            const bool vis = valid_q && sa < ke &&
+                             (mask_words ? ((words[c >> 5] >> (c & 31)) & 1u) != 0 : sa <= row_slot);
+            s[c] = vis ? s[c] : -INFINITY;
+            mx = fmaxf(mx, s[c]);
           }
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (qm & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        float o[128];
-        tmem_ld128(tl + 256, o);
+        const float m_tile = mx * scale_log2;  // scale > 0: max commutes with it
+        float m_new = m_used;
+        if (m_used == -INFINITY || m_tile > m_used + 8.f) m_new = fmaxf(m_used, m_tile);
+        const float alpha = (m_new == m_used) ? 1.f : exp2f(m_used - m_new);
+        const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+        float rs = 0.f;
+        uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) o[c] *= alpha;
-        tmem_st128(tl + 256, o);
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = exp2f(fmaf(s[2 * c], scale_log2, neg_m));
+          const float p1 = exp2f(fmaf(s[2 * c + 1], scale_log2, neg_m));
+          rs += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[c] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        l_run = l_run * alpha + rs;
+        m_used = m_new;
+        // P.V of the previous tile has completed (it precedes this tile's S
+        // in the in-order tensor pipe), so P may be replaced and O rescaled.
+        tmem_st64(tS, pk);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          float o[128];
+          tmem_ld128(tO, o);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) o[c] *= alpha;
+          tmem_st128(tO, o);
+        }
       }
       // last tile: zero the V rows between the last valid slot and the end of
       // its 16-slot MMA step (they hold whatever the page held past kv_len)
       const int valid = min(kTcTileSlots, ke - ts);
-      if (j == T - 1 && (valid & 15)) {
-        const int r0 = valid, r1 = (valid + 15) & ~15;
-        const int chunks = (r1 - r0) * 8 * 2;
-        for (int i = threadIdx.x - 64; i < chunks; i += 128) {
-          const int h = i / ((r1 - r0) * 8), rem = i % ((r1 - r0) * 8);
-          *reinterpret_cast<uint4*>(S.v[j & 1][h] + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+      if (t == 0 && j == T - 1 && (valid & 15)) {
+        const int r0 = valid, nr = ((valid + 15) & ~15) - valid;
+        for (int i = threadIdx.x - 64; i < nr * 16; i += 128) {
+          const int h = i / (nr * 8), rem = i % (nr * 8);
+          *reinterpret_cast<uint4*>(S.v[j % NS][h] + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full);
+      if (lane == 0) mbar_arrive(&S.p_full[t]);
     }
-    if (!bad && !mbar_wait(&S.o_done, (T - 1) & 1)) bad = true;
+    if (!bad && !mbar_wait(&S.o_done[t], (T - 1) & 1)) bad = true;
     fence_after();
-    float o[128];
-    tmem_ld128(tl + 256, o);
-    if (valid_q && !bad) {
-      float4* po = reinterpret_cast<float4*>(m.part_o + int64_t(it.part_base + qm) * D);
+    if (warp_live && !bad) {
+      float o[128];
+      tmem_ld128(tO, o);
+      if (valid_q) {
+        if (it.direct) {
+          const bool empty = !(l_run > 0.f);
+          const float inv = empty ? 0.f : 1.f / l_run;
+          const float lse = empty ? -INFINITY : (m_used + log2f(l_run)) * kLn2;
+          uint4 packed[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-      m.part_ml[it.part_base + qm] = make_float2(m_run, l_run);
+          for (int c = 0; c < 16; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            packed[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (out.out_all) {
+            uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) dst[c] = packed[c];
+          }
+          if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = lse;
+          for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
+            const int jj = m.ro_idx[r];
+            if (out.out_readout) {
+              uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) dst[c] = packed[c];
+            }
+            if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = lse;
+          }
+        } else {
+          float4* po = reinterpret_cast<float4*>(m.part_o + int64_t(it.part_base + q) * D);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+          m.part_ml[it.part_base + q] = make_float2(m_used, l_run);
+        }
+      }
+    }
+  }
+  if (T == 0 && threadIdx.x < NT * 128) {
+    // nothing visible in this chunk: an empty partial state (a direct item
+    // with no visible slot writes zeros and -inf)
+    const int q = threadIdx.x;
+    if (q < nqv) {
+      if (it.direct) {
+        const int row = it.row0 + q / G, head = it.kv_head * G + q % G;
+        if (out.out_all) {
+          uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
+          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = -INFINITY;
+        for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
+          const int jj = m.ro_idx[r];
+          if (out.out_readout) {
+            uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
+            for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = -INFINITY;
+        }
+      } else {
+        float* po = m.part_o + int64_t(it.part_base + q) * D;
+        for (int c = 0; c < D; ++c) po[c] = 0.f;
+        m.part_ml[it.part_base + q] = make_float2(-INFINITY, 0.f);
+      }
     }
   }
   if (bad) set_status(status, PIE_STATUS_TIMEOUT);
   fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && T > 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(Cfg<NT>::kTmemCols)
                  : "memory");
   }
 }
@@ -393,12 +484,31 @@ static bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int NT>
+static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words, tc::Out out,
+                             uint32_t* status, const CUtensorMap& qm, const CUtensorMap& km,
+                             const CUtensorMap& vm, cudaStream_t s) {
+  const size_t smem = sizeof(tc::Smem<NT, tc::Cfg<NT>::NS>) + 1024;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  attend_tc_kernel<NT><<<p.num_tc_items, tc::Cfg<NT>::kThreads, smem, s>>>(
+      p.dev, p.G, p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
+      p.desc.sm_scale * 1.4426950408889634f, mask_words, out, status, qm, km, vm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
-                             const void* v_pool, const uint32_t* mask_words, uint32_t* status,
+                             const void* v_pool, const uint32_t* mask_words, void* out_readout,
+                             float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
                              cudaStream_t s) {
   const int D = p.desc.head_dim, Hq = p.desc.num_q_heads, Hkv = p.desc.num_kv_heads;
   const int G = p.G, P = p.desc.page_size;
-  if (D != 128 || p.desc.dtype != PIE_BF16) return cudaErrorNotSupported;
+  if (D != 128 || p.desc.dtype != PIE_BF16 || kTcTileQueries % G != 0) return cudaErrorNotSupported;
   CUtensorMap qm, km, vm;
   {
     const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(G), cuuint64_t(Hkv), cuuint64_t(p.N)};
@@ -413,17 +523,10 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
     if (!make_map(&km, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
     if (!make_map(&vm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  const size_t smem = sizeof(tc::Smem) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  attend_tc_kernel<<<p.num_tc_items, tc::kThreads, smem, s>>>(
-      p.dev, G, Hkv, P, p.desc.sm_scale * 1.4426950408889634f, mask_words, status, qm, km, vm);
-  return cudaGetLastError();
+  tc::Out out{static_cast<__nv_bfloat16*>(out_readout), lse_readout,
+              static_cast<__nv_bfloat16*>(out_all), lse_all};
+  return p.tc_nt == 2 ? launch_nt<2>(p, mask_words, out, status, qm, km, vm, s)
+                      : launch_nt<1>(p, mask_words, out, status, qm, km, vm, s);
 }
 
 }  // namespace pie

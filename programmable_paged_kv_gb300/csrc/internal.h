@@ -22,19 +22,22 @@ struct alignas(16) DecItem {
 };
 
 // How the combine step finds the partials of (row, kv head): chunk c of query
-// q lives at part_base + c * stride + q_off + (h % G).
+// q lives at part_base + c * stride + q_off + (h % G).  nchunks < 0 marks rows
+// whose outputs the tensor-core kernel wrote directly (nothing to combine).
 struct alignas(16) CombEntry {
   int32_t part_base, nchunks, stride, q_off;
 };
 
-// Work item of the tensor-core attention kernel: a tile of up to 128 query
-// vectors (rows [row0, row0 + nrows) of `lane`, G heads each, head-major
-// within a row) over kv head `kv_head`, reading slots [kv_begin, kv_end) in
-// 128-slot tiles; partial softmax state for the tile's queries goes to
-// partial slots part_base .. part_base + 127.
+// Work item of the tensor-core attention kernel: up to NT tiles of 128 query
+// vectors (rows [row0, row0 + nrows) of `lane`, G heads each, head-minor
+// within a row; tile t holds rows row0 + t*128/G ...) over kv head
+// `kv_head`, reading slots [kv_begin, kv_end) in 128-slot KV tiles.  When
+// `direct` is set the item covers the rows' whole visible range and writes
+// final outputs; otherwise it writes partial softmax states for query q of
+// the item at part_base + q (128 per tile).
 struct alignas(16) TcItem {
   int32_t lane, kv_head, row0, nrows;
-  int32_t kv_begin, kv_end, part_base, pad;
+  int32_t kv_begin, kv_end, part_base, direct;
 };
 
 constexpr int kStageSlots = 64;   // slots per pipeline stage of the decode kernel
@@ -55,6 +58,8 @@ struct DevMeta {
   const int32_t* row_lane;
   const int64_t* mask_word_indptr;  // NULL when the pass has no mask
   const int32_t* readout;
+  const int32_t* ro_indptr;         // [N+1]: readout positions of row r are
+  const int32_t* ro_idx;            //   ro_idx[ro_indptr[r] .. ro_indptr[r+1])
   const float* rope_freq;           // [d/2]
   const DecItem* dec_items;
   const TcItem* tc_items;
@@ -77,6 +82,7 @@ struct pie_fwd_plan {
   int32_t nq;                // query vectors per decode item (2, 4 or 8)
   int32_t num_dec_items;
   int32_t num_tc_items;
+  int32_t tc_nt;             // query tiles per tensor-core item (1 or 2)
   int64_t num_part_slots;
   pie::DevMeta dev;
   pie::PinnedBlock* staging;
@@ -95,7 +101,8 @@ cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, con
                                  const void* v_pool, const uint32_t* mask_words,
                                  uint32_t* status, cudaStream_t s);
 cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
-                             const void* v_pool, const uint32_t* mask_words, uint32_t* status,
+                             const void* v_pool, const uint32_t* mask_words, void* out_readout,
+                             float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
                              cudaStream_t s);
 cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
                            void* out_all, float* lse_all, cudaStream_t s);

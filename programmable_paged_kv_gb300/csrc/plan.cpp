@@ -93,7 +93,8 @@ static void pinned_release(PinnedBlock* b) {
 // host plan: validated metadata + work lists, before layout
 // ---------------------------------------------------------------------------
 struct HostPlan {
-  int L = 0, N = 0, R = 0, G = 1, nq = 4;
+  int L = 0, N = 0, R = 0, G = 1, nq = 4, tc_nt = 1;
+  std::vector<int32_t> ro_indptr, ro_idx;
   bool has_mask = false, any_channel = false;
   std::vector<int32_t> row_lane, readout;
   std::vector<float> rope_freq;
@@ -133,6 +134,7 @@ static int choose_chunk(int64_t total_slots_x_heads) {
 // tensor-core kernel (bf16 only).
 static bool g_tc_enabled = true;
 constexpr int kTcMinQueries = 16;
+constexpr int kTcTargetSms = 152;  // SMs of the part the item counts are sized for
 
 static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, HostPlan& H) {
   if (!desc || !meta) return fail(PIE_EINVAL, "desc and meta are required");
@@ -254,10 +256,38 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
     for (int r = r0; r < r1; ++r) mx = std::max(mx, M.slots[r]);
     return std::min(kv, mx + 1);
   };
-  const bool tc_ok = g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128;
+  const bool tc_ok =
+      g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128 && kTcTileQueries % G == 0;
+  auto lane_tc = [&](int l) {
+    return tc_ok && (M.row_indptr[l + 1] - M.row_indptr[l]) * G >= kTcMinQueries;
+  };
+  // split-KV items: chunk length from the total work
   int64_t work = 0;
-  for (int l = 0; l < L; ++l) work += static_cast<int64_t>(M.kv_len[l]) * Hkv;
+  for (int l = 0; l < L; ++l)
+    if (!lane_tc(l)) work += static_cast<int64_t>(M.kv_len[l]) * Hkv;
   const int CH = choose_chunk(work);
+  // tensor-core items: two query tiles per item when some lane has more than
+  // 128 query vectors per kv head (they then share every K/V tile)
+  int max_tc_q = 0;
+  for (int l = 0; l < L; ++l)
+    if (lane_tc(l)) max_tc_q = std::max(max_tc_q, (M.row_indptr[l + 1] - M.row_indptr[l]) * G);
+  H.tc_nt = max_tc_q > kTcTileQueries ? 2 : 1;
+  const int tc_rows = std::max(1, H.tc_nt * kTcTileQueries / G);
+  // split a tensor-core unit's KV range only as far as needed to give about
+  // four waves of items; the nearest whole number of chunks, each a whole
+  // number of 128-slot tiles
+  int64_t tc_total = 0, tc_units = 0;
+  for (int l = 0; l < L; ++l) {
+    if (!lane_tc(l)) continue;
+    const int r0 = M.row_indptr[l], r1 = M.row_indptr[l + 1];
+    for (int b0 = r0; b0 < r1; b0 += tc_rows) {
+      tc_total += static_cast<int64_t>(extent(l, b0, std::min(r1, b0 + tc_rows))) * Hkv;
+      tc_units += Hkv;
+    }
+  }
+  const int64_t tc_target = 4 * kTcTargetSms;
+  const int64_t tc_ch = tc_units >= tc_target ? INT32_MAX
+                        : std::max<int64_t>(512, (tc_total + tc_target - 1) / tc_target);
   H.comb.assign(static_cast<size_t>(N) * Hkv, CombEntry{0, 0, 0, 0});
   H.dec.clear();
   H.tc.clear();
@@ -265,32 +295,52 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   for (int l = 0; l < L; ++l) {
     const int r0 = M.row_indptr[l], r1 = M.row_indptr[l + 1], n = r1 - r0;
     if (n == 0) continue;
-    const bool use_tc = tc_ok && n * G >= kTcMinQueries;
-    const int blk_rows = use_tc ? std::max(1, kTcTileQueries / G) : rows_per_item;
+    const bool use_tc = lane_tc(l);
+    const int blk_rows = use_tc ? tc_rows : rows_per_item;
     const int stride = use_tc ? kTcTileQueries : H.nq;
     for (int g = 0; g < Hkv; ++g) {
       for (int b0 = r0; b0 < r1; b0 += blk_rows) {
         const int b1 = std::min(r1, b0 + blk_rows);
         const int ext = extent(l, b0, b1);
-        const int nchunks = (ext + CH - 1) / CH;
+        int nchunks, chunk;
+        if (use_tc) {
+          nchunks = static_cast<int>(std::max<int64_t>(1, (ext + tc_ch / 2) / tc_ch));
+          chunk = ((ext + nchunks - 1) / nchunks + kTcTileSlots - 1) / kTcTileSlots * kTcTileSlots;
+          nchunks = std::max(1, (ext + chunk - 1) / std::max(1, chunk));
+        } else {
+          nchunks = (ext + CH - 1) / CH;
+          chunk = CH;
+        }
+        const bool direct = use_tc && nchunks == 1;
         for (int r = b0; r < b1; ++r) {
           CombEntry& e = H.comb[static_cast<size_t>(r) * Hkv + g];
           e.part_base = static_cast<int32_t>(part);
-          e.nchunks = nchunks;
-          e.stride = stride;
+          e.nchunks = direct ? -1 : nchunks;
+          e.stride = use_tc ? stride * H.tc_nt : stride;
           e.q_off = (r - b0) * G;
         }
         for (int c = 0; c < nchunks; ++c) {
-          const int kb = c * CH, ke = std::min(ext, kb + CH);
+          const int kb = c * chunk, ke = std::min(ext, kb + chunk);
           if (use_tc) {
-            H.tc.push_back(TcItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part), 0});
+            H.tc.push_back(TcItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part),
+                                  direct ? 1 : 0});
+            part += direct ? 0 : stride * H.tc_nt;
           } else {
             H.dec.push_back(DecItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part), 0});
+            part += stride;
           }
-          part += stride;
         }
       }
     }
+  }
+  // readout positions per row (a row may be read out several times)
+  H.ro_indptr.assign(N + 1, 0);
+  for (int j = 0; j < H.R; ++j) H.ro_indptr[H.readout[j] + 1]++;
+  for (int r = 0; r < N; ++r) H.ro_indptr[r + 1] += H.ro_indptr[r];
+  H.ro_idx.assign(H.R, 0);
+  {
+    std::vector<int32_t> fill(H.ro_indptr.begin(), H.ro_indptr.end() - 1);
+    for (int j = 0; j < H.R; ++j) H.ro_idx[fill[H.readout[j]]++] = j;
   }
   if (part > INT32_MAX) return fail(PIE_ERANGE, "pass too large: partial index overflow");
   H.num_part_slots = part;
@@ -303,7 +353,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t row_indptr, positions, slots, kv_len, page_indptr, page_ids, fold_mode, fold_count,
-      row_lane, mask_word_indptr, readout, rope_freq, dec, tc, comb;
+      row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb;
   size_t copy_bytes;  // everything above
   size_t part_o, part_ml;
   size_t total;
@@ -330,6 +380,8 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.row_lane = take(4 * H.N);
   Y.mask_word_indptr = take(H.has_mask ? 8 * (H.N + 1) : 0);
   Y.readout = take(4 * H.R);
+  Y.ro_indptr = take(4 * (H.N + 1));
+  Y.ro_idx = take(4 * H.R);
   Y.rope_freq = take(4 * (D.head_dim / 2));
   Y.dec = take(sizeof(DecItem) * H.dec.size());
   Y.tc = take(sizeof(TcItem) * H.tc.size());
@@ -393,6 +445,8 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   put(Y.row_lane, H.row_lane.data(), 4 * H.N);
   if (H.has_mask) put(Y.mask_word_indptr, M.mask_word_indptr, 8 * (H.N + 1));
   put(Y.readout, H.readout.data(), 4 * H.R);
+  put(Y.ro_indptr, H.ro_indptr.data(), 4 * (H.N + 1));
+  put(Y.ro_idx, H.ro_idx.data(), 4 * H.R);
   put(Y.rope_freq, H.rope_freq.data(), 4 * H.rope_freq.size());
   put(Y.dec, H.dec.data(), sizeof(DecItem) * H.dec.size());
   put(Y.tc, H.tc.data(), sizeof(TcItem) * H.tc.size());
@@ -423,6 +477,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->nq = H.nq;
   p->num_dec_items = static_cast<int32_t>(H.dec.size());
   p->num_tc_items = static_cast<int32_t>(H.tc.size());
+  p->tc_nt = H.tc_nt;
   p->num_part_slots = H.num_part_slots;
   char* w = static_cast<char*>(dev_workspace);
   DevMeta& dm = p->dev;
@@ -437,6 +492,8 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.row_lane = reinterpret_cast<const int32_t*>(w + Y.row_lane);
   dm.mask_word_indptr = H.has_mask ? reinterpret_cast<const int64_t*>(w + Y.mask_word_indptr) : nullptr;
   dm.readout = reinterpret_cast<const int32_t*>(w + Y.readout);
+  dm.ro_indptr = reinterpret_cast<const int32_t*>(w + Y.ro_indptr);
+  dm.ro_idx = reinterpret_cast<const int32_t*>(w + Y.ro_idx);
   dm.rope_freq = reinterpret_cast<const float*>(w + Y.rope_freq);
   dm.dec_items = reinterpret_cast<const DecItem*>(w + Y.dec);
   dm.tc_items = reinterpret_cast<const TcItem*>(w + Y.tc);
@@ -484,7 +541,8 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
   cudaError_t e = cudaSuccess;
   if (plan->num_dec_items > 0) e = launch_attend_decode(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
   if (e == cudaSuccess && plan->num_tc_items > 0)
-    e = launch_attend_tc(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
+    e = launch_attend_tc(*plan, q_rot, k_pool, v_pool, mask_words, out_readout, lse_readout,
+                         out_all, lse_all, status, s);
   if (e == cudaSuccess) e = launch_combine(*plan, out_readout, lse_readout, out_all, lse_all, s);
   if (e != cudaSuccess) return fail(PIE_ECUDA, std::string("attend launch: ") + cudaGetErrorString(e));
   return PIE_OK;
