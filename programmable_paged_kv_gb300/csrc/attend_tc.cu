@@ -156,6 +156,18 @@ __device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* map, int x,
       : "memory");
 }
 
+// Four 128-byte rows (one box of the map each, at rows y0..y3, column x) into
+// four consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int y0,
+                                            int y1, int y2, int y3, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 struct Out {
   __nv_bfloat16* out_readout;
   float* lse_readout;
@@ -170,7 +182,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     DevMeta m, int G, int Hq, int Hkv, int P, float scale_log2,
     const uint32_t* __restrict__ mask_words, tc::Out out, uint32_t* status,
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap) {
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kgmap,
+    const __grid_constant__ CUtensorMap vgmap) {
   using namespace tc;
   constexpr int NS = Cfg<NT>::NS;
   constexpr int D = 128;
@@ -180,7 +193,19 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   SM& S = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcItem it = m.tc_items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = it.kv_begin, ke = it.kv_end;
+  // gather mode (masked passes): positions [kb, ke) of the row block's
+  // compacted visible-slot list, this item's share of its 128-entry tiles;
+  // otherwise slots [kb, ke) of the lane
+  const bool gather = it.block >= 0;
+  int kb = it.kv_begin, ke = it.kv_end;
+  MaskBlock mb{0, 0, 0, 0, 0, 0, 0, 0};
+  if (gather) {
+    mb = m.mblocks[it.block];
+    const int U = m.list_len[it.block];
+    const int tiles = (U + kTcTileSlots - 1) / kTcTileSlots;
+    kb = (it.chunk * tiles / it.nchunks) * kTcTileSlots;
+    ke = min(U, ((it.chunk + 1) * tiles / it.nchunks) * kTcTileSlots);
+  }
   const int T = ke > kb ? (ke - kb + kTcTileSlots - 1) / kTcTileSlots : 0;
   const int nqv = it.nrows * G;  // valid query vectors of the item
 
@@ -212,16 +237,19 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
 
   if (warp == 0) {
     // ---------------- TMA producer ------------------------------------------
-    if (lane == 0 && T > 0) {
+    if (T > 0) {
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(&S.q_full, NT * 2 * kHalfBytes);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&S.q_full, NT * 2 * kHalfBytes);
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-          tma_4d(S.q[t][a], &qmap, 64 * a, 0, it.kv_head, it.row0 + t * (kTcTileQueries / G),
-                 &S.q_full);
+          for (int a = 0; a < 2; ++a)
+            tma_4d(S.q[t][a], &qmap, 64 * a, 0, it.kv_head, it.row0 + t * (kTcTileQueries / G),
+                   &S.q_full);
+      }
       const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
+      const int32_t* list = gather ? m.list + mb.list_off : nullptr;
       for (int j = 0; j < T; ++j) {
         const int st = j % NS;
         if (j >= NS && !mbar_wait(&S.kv_empty[st], ((j / NS) - 1) & 1)) {
@@ -230,16 +258,41 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         }
         const int ts = kb + j * kTcTileSlots;
         const int te = min(ts + kTcTileSlots, ke);
-        const int p0 = ts / P, p1 = (te - 1) / P;
-        mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
-        for (int pg = p0; pg <= p1; ++pg) {
-          // first row of (page, kv head) in the [page * Hkv + head][slot] view
-          const int y = (pages[pg] * Hkv + it.kv_head) * P;
-          const int off = (pg * P - ts) * 128;
+        if (gather) {
+          // slot-granular: 4 listed slots per lane, K and V rows of both halves
+          // of d; rows up to the next multiple of 16 repeat the last listed
+          // slot so that every row a P.V step reads holds finite data
+          const int rows = ((te - ts) + 15) & ~15;
+          if (lane == 0) mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(rows) * 128u * 4u);
+          __syncwarp();
+          if (4 * lane < rows) {
+            int y[4];
 #pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            tma_2d(S.k[st][a] + off, &kmap, 64 * a, y, &S.kv_full[st], pol);
-            tma_2d(S.v[st][a] + off, &vmap, 64 * a, y, &S.kv_full[st], pol);
+            for (int e = 0; e < 4; ++e) {
+              const int slot = list[min(ts + 4 * lane + e, te - 1)];
+              y[e] = (pages[slot / P] * Hkv + it.kv_head) * P + slot % P;
+            }
+            const int off = 4 * lane * 128;
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              tma_gather4(S.k[st][a] + off, &kgmap, 64 * a, y[0], y[1], y[2], y[3],
+                          &S.kv_full[st], pol);
+              tma_gather4(S.v[st][a] + off, &vgmap, 64 * a, y[0], y[1], y[2], y[3],
+                          &S.kv_full[st], pol);
+            }
+          }
+        } else if (lane == 0) {
+          const int p0 = ts / P, p1 = (te - 1) / P;
+          mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
+          for (int pg = p0; pg <= p1; ++pg) {
+            // first row of (page, kv head) in the [page * Hkv + head][slot] view
+            const int y = (pages[pg] * Hkv + it.kv_head) * P;
+            const int off = (pg * P - ts) * 128;
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              tma_2d(S.k[st][a] + off, &kmap, 64 * a, y, &S.kv_full[st], pol);
+              tma_2d(S.v[st][a] + off, &vmap, 64 * a, y, &S.kv_full[st], pol);
+            }
           }
         }
       }
@@ -291,16 +344,22 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     const int row = it.row0 + (valid_q ? q : 0) / G;
     const int head = it.kv_head * G + (valid_q ? q : 0) % G;
     const int row_slot = valid_q ? m.slots[row] : INT_MAX;
-    const int64_t mbase = (mask_words && valid_q) ? m.mask_word_indptr[row] : 0;
+    // the row's mask words: over the compacted list (gather mode) or over
+    // the lane's slots; nullptr without a mask
+    const bool masked = mask_words != nullptr;
+    const uint32_t* mrow = nullptr;
+    if (masked && valid_q)
+      mrow = gather ? m.cmask + mb.cmask_off + int64_t(row - mb.r0) * mb.nw
+                    : mask_words + m.mask_word_indptr[row];
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + 256 * t;
     const uint32_t tS = lane_base, tO = lane_base + 128;
     float m_used = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
       const int ts = kb + j * kTcTileSlots;
       uint32_t words[4] = {~0u, ~0u, ~0u, ~0u};
-      if (mask_words && valid_q) {
+      if (mrow) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) words[i] = ts + 32 * i < ke ? mask_words[mbase + (ts >> 5) + i] : 0u;
+        for (int i = 0; i < 4; ++i) words[i] = ts + 32 * i < ke ? mrow[(ts >> 5) + i] : 0u;
       }
       if (!mbar_wait(&S.s_full[t], j & 1)) { bad = true; break; }
       fence_after();
@@ -356,7 +415,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       // last tile: zero the V rows between the last valid slot and the end of
       // its 16-slot MMA step (they hold whatever the page held past kv_len)
       const int valid = min(kTcTileSlots, ke - ts);
-      if (t == 0 && j == T - 1 && (valid & 15)) {
+      if (!gather && t == 0 && j == T - 1 && (valid & 15)) {
         const int r0 = valid, nr = ((valid + 15) & ~15) - valid;
         for (int i = threadIdx.x - 64; i < nr * 16; i += 128) {
           const int h = i / (nr * 8), rem = i % (nr * 8);
@@ -487,7 +546,8 @@ static bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint6
 template <int NT>
 static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words, tc::Out out,
                              uint32_t* status, const CUtensorMap& qm, const CUtensorMap& km,
-                             const CUtensorMap& vm, cudaStream_t s) {
+                             const CUtensorMap& vm, const CUtensorMap& kgm,
+                             const CUtensorMap& vgm, cudaStream_t s) {
   const size_t smem = sizeof(tc::Smem<NT, tc::Cfg<NT>::NS>) + 1024;
   static bool configured = false;
   if (!configured) {
@@ -498,7 +558,7 @@ static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words
   }
   attend_tc_kernel<NT><<<p.num_tc_items, tc::Cfg<NT>::kThreads, smem, s>>>(
       p.dev, p.G, p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
-      p.desc.sm_scale * 1.4426950408889634f, mask_words, out, status, qm, km, vm);
+      p.desc.sm_scale * 1.4426950408889634f, mask_words, out, status, qm, km, vm, kgm, vgm);
   return cudaGetLastError();
 }
 
@@ -523,10 +583,19 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
     if (!make_map(&km, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
     if (!make_map(&vm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // one-row boxes for the slot-granular gathers of masked passes
+  CUtensorMap kgm = km, vgm = vm;
+  if (p.num_mblocks > 0) {
+    const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(p.num_pool_pages) * Hkv * P};
+    const cuuint64_t str[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t box[2] = {64, 1};
+    if (!make_map(&kgm, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&vgm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
   tc::Out out{static_cast<__nv_bfloat16*>(out_readout), lse_readout,
               static_cast<__nv_bfloat16*>(out_all), lse_all};
-  return p.tc_nt == 2 ? launch_nt<2>(p, mask_words, out, status, qm, km, vm, s)
-                      : launch_nt<1>(p, mask_words, out, status, qm, km, vm, s);
+  return p.tc_nt == 2 ? launch_nt<2>(p, mask_words, out, status, qm, km, vm, kgm, vgm, s)
+                      : launch_nt<1>(p, mask_words, out, status, qm, km, vm, kgm, vgm, s);
 }
 
 }  // namespace pie

@@ -38,6 +38,21 @@ struct alignas(16) CombEntry {
 struct alignas(16) TcItem {
   int32_t lane, kv_head, row0, nrows;
   int32_t kv_begin, kv_end, part_base, direct;
+  // masked passes: the row block whose compacted visible-slot list the item
+  // walks (else -1), and this item's share of it: chunk `chunk` of `nchunks`
+  // equal shares of the list's 128-entry tiles (kv_begin/kv_end unused)
+  int32_t block, chunk, nchunks, pad;
+};
+
+// A row block of a masked pass on the tensor-core path: rows [r0, r1) of
+// `lane`, whose masks cover nw = ceil(kv_len / 32) words each.  The mask
+// pre-pass writes, at these offsets of the scratch arrays, the block's
+// compacted list of slots visible to at least one of its rows (list_off, up to
+// kv_len entries), and each row's mask re-expressed over that list (cmask_off,
+// (r1 - r0) rows of nw words).
+struct alignas(16) MaskBlock {
+  int32_t lane, r0, r1, nw;
+  int32_t list_off, cmask_off, pad0, pad1;
 };
 
 constexpr int kStageSlots = 64;   // slots per pipeline stage of the decode kernel
@@ -66,6 +81,10 @@ struct DevMeta {
   const CombEntry* comb;            // [N * Hkv]
   float* part_o;                    // [num_part_slots][d] unnormalised
   float2* part_ml;                  // [num_part_slots] (max, sum), log2 domain
+  const MaskBlock* mblocks;         // [num_mblocks] (masked passes with tensor-core lanes)
+  int32_t* list;                    // compacted visible-slot lists (scratch)
+  uint32_t* cmask;                  // rows' masks over the lists (scratch)
+  int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
 };
 
 struct PinnedBlock;
@@ -83,6 +102,8 @@ struct pie_fwd_plan {
   int32_t num_dec_items;
   int32_t num_tc_items;
   int32_t tc_nt;             // query tiles per tensor-core item (1 or 2)
+  int32_t num_mblocks;       // masked row blocks (0 unless masked tensor-core lanes)
+  int32_t mblock_max_nw;     // largest nw over the masked row blocks
   int64_t num_part_slots;
   pie::DevMeta dev;
   pie::PinnedBlock* staging;
@@ -104,6 +125,8 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
                              const void* v_pool, const uint32_t* mask_words, void* out_readout,
                              float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
                              cudaStream_t s);
+cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_words,
+                                cudaStream_t s);
 cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
                            void* out_all, float* lse_all, cudaStream_t s);
 

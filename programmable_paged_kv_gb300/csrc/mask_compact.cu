@@ -1,0 +1,130 @@
+// Mask pre-pass for masked passes on the tensor-core path (Pie "The forward
+// pass", Attention masks: a row may skip slots it would read under a causal
+// mask -- sliding windows, attention sinks, TOVA-style eviction).
+//
+// Reading only the slots some row can see is what keeps a masked pass near
+// its algorithmic bytes: a window of 4,096 slots in a 32,768-slot working set
+// touches an eighth of the pages, and a TOVA mask that keeps a quarter of the
+// slots touches nearly every page but only a quarter of the slots.  For every
+// row block (the rows one tensor-core item serves) three small kernels build
+//   1. the union of the rows' mask words (bits at or past kv_len cleared);
+//   2. the compacted list of the slots set in the union, ascending, and its
+//      length;
+//   3. each row's mask re-expressed over that list (bit i of a row's word
+//      i/32 = the row sees list[i]).
+// The tensor-core kernel then walks 128-entry tiles of the list, gathering
+// the K/V rows of those slots, and tests visibility with the re-expressed
+// words exactly as it tests plain mask words.  The union words are kept in
+// the first row of the block's re-expressed mask area until step 3
+// overwrites it.
+
+#include "common.cuh"
+
+namespace pie {
+
+// 1. grid (ceil(max_nw / 32), num_blocks), 256 threads: each warp ORs every
+// 8th row of the block over 32 consecutive words.
+__global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
+                                                         const uint32_t* __restrict__ mask) {
+  __shared__ uint32_t part[8][32];
+  const MaskBlock B = m.mblocks[blockIdx.y];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * 32 + lane;
+  if (blockIdx.x * 32 >= B.nw) return;
+  uint32_t acc = 0;
+  if (w < B.nw)
+    for (int r = B.r0 + warp; r < B.r1; r += 8) acc |= mask[m.mask_word_indptr[r] + w];
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && w < B.nw) {
+    uint32_t u = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u |= part[i][lane];
+    const int kv = m.kv_len[B.lane];
+    if (w == B.nw - 1 && (kv & 31)) u &= (1u << (kv & 31)) - 1u;
+    m.cmask[B.cmask_off + w] = u;
+  }
+}
+
+// 2. one CTA of 1024 threads per block: prefix count of the union's set bits
+// and the slot list.
+__global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
+  __shared__ int warp_tot[32];
+  __shared__ int chunk_total;
+  const int b = blockIdx.x;
+  const MaskBlock B = m.mblocks[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int running = 0;
+  for (int base = 0; base < B.nw; base += 1024) {
+    const int w = base + threadIdx.x;
+    uint32_t u = w < B.nw ? m.cmask[B.cmask_off + w] : 0u;
+    const int c = __popc(u);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+      int ti = t;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, ti, off);
+        if (lane >= off) ti += v;
+      }
+      warp_tot[lane] = ti - t;  // exclusive prefix over warps
+      if (lane == 31) chunk_total = ti;
+    }
+    __syncthreads();
+    int pos = running + warp_tot[warp] + incl - c;
+    int32_t* list = m.list + B.list_off;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      list[pos++] = w * 32 + bit;
+      u &= u - 1u;
+    }
+    running += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) m.list_len[b] = running;
+}
+
+// 3. grid (ceil(max_nw / 8), num_blocks), 256 threads: warp -> one word of
+// list positions; for every row of the block, ballot the row's bit at each of
+// the 32 listed slots.
+__global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
+                                                         const uint32_t* __restrict__ mask) {
+  const int b = blockIdx.y;
+  const MaskBlock B = m.mblocks[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cw = blockIdx.x * 8 + warp;
+  const int U = m.list_len[b];
+  if (cw >= B.nw || cw * 32 >= U) return;
+  const int i = cw * 32 + lane;
+  const int slot = i < U ? m.list[B.list_off + i] : -1;
+  for (int r = B.r0; r < B.r1; ++r) {
+    bool bit = false;
+    if (slot >= 0) bit = ((mask[m.mask_word_indptr[r] + (slot >> 5)] >> (slot & 31)) & 1u) != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+    if (lane == 0) m.cmask[B.cmask_off + int64_t(r - B.r0) * B.nw + cw] = bal;
+  }
+}
+
+cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_words,
+                                cudaStream_t s) {
+  const int nb = p.num_mblocks, nw = p.mblock_max_nw;
+  if (nb == 0 || nw == 0) return cudaSuccess;
+  mask_union_kernel<<<dim3((nw + 31) / 32, nb), 256, 0, s>>>(p.dev, mask_words);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb), 256, 0, s>>>(p.dev, mask_words);
+  return cudaGetLastError();
+}
+
+}  // namespace pie

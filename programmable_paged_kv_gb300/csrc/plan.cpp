@@ -95,6 +95,9 @@ static void pinned_release(PinnedBlock* b) {
 struct HostPlan {
   int L = 0, N = 0, R = 0, G = 1, nq = 4, tc_nt = 1;
   std::vector<int32_t> ro_indptr, ro_idx;
+  std::vector<MaskBlock> mblocks;
+  int64_t list_total = 0, cmask_total = 0;
+  int mblock_max_nw = 0;
   bool has_mask = false, any_channel = false;
   std::vector<int32_t> row_lane, readout;
   std::vector<float> rope_freq;
@@ -291,6 +294,32 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   H.comb.assign(static_cast<size_t>(N) * Hkv, CombEntry{0, 0, 0, 0});
   H.dec.clear();
   H.tc.clear();
+  // masked passes: tensor-core lanes walk the compacted list of the slots
+  // their row block can see (one list per row block, shared by all kv heads)
+  H.mblocks.clear();
+  bool any_tc = false;
+  for (int l = 0; l < L; ++l) any_tc = any_tc || lane_tc(l);
+  std::vector<int32_t> block_of_row(H.has_mask && any_tc ? N : 0, -1);
+  H.list_total = H.cmask_total = 0;
+  H.mblock_max_nw = 0;
+  if (!block_of_row.empty()) {
+    for (int l = 0; l < L; ++l) {
+      if (!lane_tc(l)) continue;
+      const int r0 = M.row_indptr[l], r1 = M.row_indptr[l + 1];
+      const int nw = (M.kv_len[l] + 31) / 32;
+      for (int b0 = r0; b0 < r1; b0 += tc_rows) {
+        const int b1 = std::min(r1, b0 + tc_rows);
+        block_of_row[b0] = static_cast<int32_t>(H.mblocks.size());
+        H.mblocks.push_back(MaskBlock{l, b0, b1, nw, static_cast<int32_t>(H.list_total),
+                                      static_cast<int32_t>(H.cmask_total), 0, 0});
+        H.list_total += M.kv_len[l];
+        H.cmask_total += static_cast<int64_t>(b1 - b0) * nw;
+        H.mblock_max_nw = std::max(H.mblock_max_nw, nw);
+      }
+    }
+    if (H.list_total > INT32_MAX || H.cmask_total > INT32_MAX)
+      return fail(PIE_ERANGE, "masked pass too large for the compacted slot lists");
+  }
   int64_t part = 0;
   for (int l = 0; l < L; ++l) {
     const int r0 = M.row_indptr[l], r1 = M.row_indptr[l + 1], n = r1 - r0;
@@ -322,8 +351,9 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
         for (int c = 0; c < nchunks; ++c) {
           const int kb = c * chunk, ke = std::min(ext, kb + chunk);
           if (use_tc) {
+            const int32_t blk = block_of_row.empty() ? -1 : block_of_row[b0];
             H.tc.push_back(TcItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part),
-                                  direct ? 1 : 0});
+                                  direct ? 1 : 0, blk, c, nchunks, 0});
             part += direct ? 0 : stride * H.tc_nt;
           } else {
             H.dec.push_back(DecItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part), 0});
@@ -353,9 +383,9 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t row_indptr, positions, slots, kv_len, page_indptr, page_ids, fold_mode, fold_count,
-      row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb;
+      row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks;
   size_t copy_bytes;  // everything above
-  size_t part_o, part_ml;
+  size_t part_o, part_ml, list, cmask, list_len;
   size_t total;
 };
 
@@ -386,9 +416,13 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.dec = take(sizeof(DecItem) * H.dec.size());
   Y.tc = take(sizeof(TcItem) * H.tc.size());
   Y.comb = take(sizeof(CombEntry) * H.comb.size());
+  Y.mblocks = take(sizeof(MaskBlock) * H.mblocks.size());
   Y.copy_bytes = o;
   Y.part_o = take(sizeof(float) * static_cast<size_t>(H.num_part_slots) * D.head_dim);
   Y.part_ml = take(sizeof(float2) * static_cast<size_t>(H.num_part_slots));
+  Y.list = take(sizeof(int32_t) * static_cast<size_t>(H.list_total));
+  Y.cmask = take(sizeof(uint32_t) * static_cast<size_t>(H.cmask_total));
+  Y.list_len = take(sizeof(int32_t) * H.mblocks.size());
   Y.total = o;
   return Y;
 }
@@ -451,6 +485,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   put(Y.dec, H.dec.data(), sizeof(DecItem) * H.dec.size());
   put(Y.tc, H.tc.data(), sizeof(TcItem) * H.tc.size());
   put(Y.comb, H.comb.data(), sizeof(CombEntry) * H.comb.size());
+  put(Y.mblocks, H.mblocks.data(), sizeof(MaskBlock) * H.mblocks.size());
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (Y.copy_bytes > 0 &&
@@ -478,6 +513,8 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->num_dec_items = static_cast<int32_t>(H.dec.size());
   p->num_tc_items = static_cast<int32_t>(H.tc.size());
   p->tc_nt = H.tc_nt;
+  p->num_mblocks = static_cast<int32_t>(H.mblocks.size());
+  p->mblock_max_nw = H.mblock_max_nw;
   p->num_part_slots = H.num_part_slots;
   char* w = static_cast<char*>(dev_workspace);
   DevMeta& dm = p->dev;
@@ -500,6 +537,10 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.comb = reinterpret_cast<const CombEntry*>(w + Y.comb);
   dm.part_o = reinterpret_cast<float*>(w + Y.part_o);
   dm.part_ml = reinterpret_cast<float2*>(w + Y.part_ml);
+  dm.mblocks = reinterpret_cast<const MaskBlock*>(w + Y.mblocks);
+  dm.list = reinterpret_cast<int32_t*>(w + Y.list);
+  dm.cmask = reinterpret_cast<uint32_t*>(w + Y.cmask);
+  dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
   p->staging = blk;
   *out = p;
   return PIE_OK;
@@ -540,6 +581,7 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (plan->num_dec_items > 0) e = launch_attend_decode(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
+  if (e == cudaSuccess && plan->num_mblocks > 0) e = launch_mask_compact(*plan, mask_words, s);
   if (e == cudaSuccess && plan->num_tc_items > 0)
     e = launch_attend_tc(*plan, q_rot, k_pool, v_pool, mask_words, out_readout, lse_readout,
                          out_all, lse_all, status, s);
