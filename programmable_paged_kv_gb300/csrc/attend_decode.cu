@@ -138,30 +138,39 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
 
   if (warp == C::WARPS) {
     // ---------------- producer warp: TMA bulk copies of K/V pages ----------
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
-      const int64_t head_stride = int64_t(P) * D;  // elements per (page, kv head) block
-      for (int s = 0; s < nstages; ++s) {
-        const int st = s % C::STAGES, use = s / C::STAGES;
-        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1)) {
-          set_status(status, PIE_STATUS_TIMEOUT);
-          break;
-        }
-        const int sb = kb + s * kStageSlots;
-        const int se = min(sb + kStageSlots, ke);
-        const int p0 = sb / P, p1 = (se - 1) / P;
-        const uint32_t blk = uint32_t(P) * C::ROW_BYTES;
-        mbar_arrive_expect_tx(&full[st], 2u * blk * uint32_t(p1 - p0 + 1));
+    // Lane i copies page (stage start / P + i) of every stage; the page ids
+    // of the next stage are fetched while this one is issued, so no copy
+    // waits on a dependent global load.
+    const uint64_t pol = policy_evict_first();
+    const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
+    const int64_t head_stride = int64_t(P) * D;  // elements per (page, kv head) block
+    const uint32_t blk = uint32_t(P) * C::ROW_BYTES;
+    auto page_of = [&](int s) -> int64_t {
+      const int sb = kb + s * kStageSlots;
+      const int p0 = sb / P, p1 = (min(sb + kStageSlots, ke) - 1) / P;
+      return lane <= p1 - p0 ? int64_t(pages[p0 + lane]) : 0;
+    };
+    int64_t pid = nstages > 0 ? page_of(0) : 0;
+    for (int s = 0; s < nstages; ++s) {
+      const int st = s % C::STAGES, use = s / C::STAGES;
+      if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1)) {
+        if (lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
+        break;
+      }
+      const int sb = kb + s * kStageSlots;
+      const int se = min(sb + kStageSlots, ke);
+      const int p0 = sb / P, p1 = (se - 1) / P;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * blk * uint32_t(p1 - p0 + 1));
+      __syncwarp();
+      if (lane <= p1 - p0) {
         T* kdst = ring + size_t(st) * 2 * kStageSlots * D;
         T* vdst = kdst + kStageSlots * D;
-        for (int pg = p0; pg <= p1; ++pg) {
-          const int64_t src = (int64_t(pages[pg]) * Hkv + it.kv_head) * head_stride;
-          const int off = (pg * P - sb) * D;
-          bulk_g2s_hint(kdst + off, k_pool + src, blk, &full[st], pol);
-          bulk_g2s_hint(vdst + off, v_pool + src, blk, &full[st], pol);
-        }
+        const int64_t src = (pid * Hkv + it.kv_head) * head_stride;
+        const int off = ((p0 + lane) * P - sb) * D;
+        bulk_g2s_hint(kdst + off, k_pool + src, blk, &full[st], pol);
+        bulk_g2s_hint(vdst + off, v_pool + src, blk, &full[st], pol);
       }
+      if (s + 1 < nstages) pid = page_of(s + 1);
     }
     return;
   }

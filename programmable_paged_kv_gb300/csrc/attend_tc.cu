@@ -250,6 +250,31 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       }
       const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
       const int32_t* list = gather ? m.list + mb.list_off : nullptr;
+      // The TMA coordinates of a tile come from the page table (and, in
+      // gather mode, the slot list): every lane fetches its share, one tile
+      // ahead, so no copy waits on a chain of dependent global loads.
+      //   tile mode:   lane i -> page (ts / P + i) of the tile
+      //   gather mode: lane i -> listed slots ts + 4i .. ts + 4i + 3
+      int y[4];
+      auto coords = [&](int jj) {
+        const int ts = kb + jj * kTcTileSlots;
+        const int te = min(ts + kTcTileSlots, ke);
+        if (gather) {
+          const int rows = ((te - ts) + 15) & ~15;
+          if (4 * lane < rows) {
+            int sl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sl[e] = list[min(ts + 4 * lane + e, te - 1)];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              y[e] = (pages[sl[e] / P] * Hkv + it.kv_head) * P + sl[e] % P;
+          }
+        } else {
+          const int p0 = ts / P, p1 = (te - 1) / P;
+          if (lane <= p1 - p0) y[0] = (pages[p0 + lane] * Hkv + it.kv_head) * P;
+        }
+      };
+      coords(0);
       for (int j = 0; j < T; ++j) {
         const int st = j % NS;
         if (j >= NS && !mbar_wait(&S.kv_empty[st], ((j / NS) - 1) & 1)) {
@@ -266,12 +291,6 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
           if (lane == 0) mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(rows) * 128u * 4u);
           __syncwarp();
           if (4 * lane < rows) {
-            int y[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int slot = list[min(ts + 4 * lane + e, te - 1)];
-              y[e] = (pages[slot / P] * Hkv + it.kv_head) * P + slot % P;
-            }
             const int off = 4 * lane * 128;
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
@@ -281,20 +300,22 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
                           &S.kv_full[st], pol);
             }
           }
-        } else if (lane == 0) {
+        } else {
+          // one page (P slots: one box per half of d, K and V) per lane
           const int p0 = ts / P, p1 = (te - 1) / P;
-          mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
-          for (int pg = p0; pg <= p1; ++pg) {
-            // first row of (page, kv head) in the [page * Hkv + head][slot] view
-            const int y = (pages[pg] * Hkv + it.kv_head) * P;
-            const int off = (pg * P - ts) * 128;
+          if (lane == 0)
+            mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
+          __syncwarp();
+          if (lane <= p1 - p0) {
+            const int off = ((p0 + lane) * P - ts) * 128;
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
-              tma_2d(S.k[st][a] + off, &kmap, 64 * a, y, &S.kv_full[st], pol);
-              tma_2d(S.v[st][a] + off, &vmap, 64 * a, y, &S.kv_full[st], pol);
+              tma_2d(S.k[st][a] + off, &kmap, 64 * a, y[0], &S.kv_full[st], pol);
+              tma_2d(S.v[st][a] + off, &vmap, 64 * a, y[0], &S.kv_full[st], pol);
             }
           }
         }
+        if (j + 1 < T) coords(j + 1);
       }
     }
   } else if (warp == 1) {

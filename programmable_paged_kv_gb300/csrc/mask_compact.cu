@@ -105,11 +105,17 @@ __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
   if (cw >= B.nw || cw * 32 >= U) return;
   const int i = cw * 32 + lane;
   const int slot = i < U ? m.list[B.list_off + i] : -1;
-  for (int r = B.r0; r < B.r1; ++r) {
-    bool bit = false;
-    if (slot >= 0) bit = ((mask[m.mask_word_indptr[r] + (slot >> 5)] >> (slot & 31)) & 1u) != 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, bit);
-    if (lane == 0) m.cmask[B.cmask_off + int64_t(r - B.r0) * B.nw + cw] = bal;
+  // eight rows at a time so that their mask-word loads are in flight together
+  for (int r = B.r0; r < B.r1; r += 8) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      w[k] = (slot >= 0 && r + k < B.r1) ? mask[m.mask_word_indptr[r + k] + (slot >> 5)] : 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, ((w[k] >> (slot & 31)) & 1u) != 0);
+      if (lane == 0 && r + k < B.r1) m.cmask[B.cmask_off + int64_t(r + k - B.r0) * B.nw + cw] = bal;
+    }
   }
 }
 
