@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
         const float sc = vis ? part[e] : -INFINITY;
         const float m_new = fmaxf(m_run[e], warp_max_pairs(sc));
         const bool none = m_new == -INFINITY;
-        const float alpha = none ? 1.f : exp2f(m_run[e] - m_new);
-        const float p = vis ? exp2f(sc - m_new) : 0.f;
+        const float alpha = none ? 1.f : ex2(m_run[e] - m_new);
+        const float p = vis ? ex2(sc - m_new) : 0.f;
         l_run[e] = l_run[e] * alpha + warp_sum_pairs(p);
         m_run[e] = m_new;
         const int qq = (j & 1) * C::E + e;
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < C::WARPS; ++w) {
-        const float f = exp2f(mw[w * NQ + qq] - M);
+        const float f = ex2(mw[w * NQ + qq] - M);
         O = fmaf(f, ow[(w * NQ + qq) * D + c], O);
         Ls = fmaf(f, lw[w * NQ + qq], Ls);
       }
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
     for (int c = 0; c < ce.nchunks; ++c) {
       const int idx = ce.part_base + c * ce.stride + qi;
       const float2 ml = m.part_ml[idx];
-      const float f = exp2f(ml.x - M);
+      const float f = ex2(ml.x - M);
       Ls = fmaf(f, ml.y, Ls);
       const float* po = m.part_o + int64_t(idx) * D + lane * DPL;
 #pragma unroll

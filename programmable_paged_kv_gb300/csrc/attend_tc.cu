@@ -408,14 +408,14 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         const float m_tile = mx * scale_log2;  // scale > 0: max commutes with it
         float m_new = m_used;
         if (m_used == -INFINITY || m_tile > m_used + 8.f) m_new = fmaxf(m_used, m_tile);
-        const float alpha = (m_new == m_used) ? 1.f : exp2f(m_used - m_new);
+        const float alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
         const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
         float rs = 0.f;
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float p0 = exp2f(fmaf(s[2 * c], scale_log2, neg_m));
-          const float p1 = exp2f(fmaf(s[2 * c + 1], scale_log2, neg_m));
+          const float p0 = ex2(fmaf(s[2 * c], scale_log2, neg_m));
+          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, neg_m));
           rs += p0 + p1;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pk[c] = *reinterpret_cast<uint32_t*>(&h2);

@@ -178,6 +178,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx, subnormal results
+// flushed to zero; 2^-inf = 0).  Softmax weights feed a bf16 or fp32 product
+// whose tolerance is far above the instruction's error of a few ulp.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }

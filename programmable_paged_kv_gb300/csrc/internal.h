@@ -7,7 +7,7 @@
 
 #include <string>
 
-#include "../../include/pie_fwd.h"
+#include "pie_fwd.h"
 
 namespace pie {
 
