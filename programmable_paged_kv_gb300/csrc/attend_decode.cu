@@ -390,9 +390,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
   const int tgt = gw / Hq, h = gw % Hq;
   const bool is_ro = tgt < R;
   const int row = is_ro ? m.readout[tgt] : tgt - R;
-  const CombEntry ce = m.comb[int64_t(row) * Hkv + h / G];
+  const CombEntry ce = m.comb[int64_t(m.row_block[row]) * Hkv + h / G];
   if (ce.nchunks < 0) return;  // written directly by the tensor-core kernel
-  const int qi = ce.q_off + h % G;
+  const int qi = (row - ce.row0) * G + h % G;
   float M = -INFINITY;
   for (int c = 0; c < ce.nchunks; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
   float o[DPL];

@@ -77,7 +77,7 @@ __global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_
     const int ke = max(kb, min(ext, kb + kNoAllocChunk));
     items[i] = DecItem{l, g, l, 1, kb, ke, i * nq, 0};
   }
-  if (i < L * Hkv) comb[i] = CombEntry{i * MC * nq, MC, nq, 0};
+  if (i < L * Hkv) comb[i] = CombEntry{i * MC * nq, MC, nq, i / Hkv};  // block l = row l
   if (i < L) readout[i] = i;
 }
 
@@ -146,6 +146,7 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
   p.dev.dec_items = reinterpret_cast<const DecItem*>(sc + off_items);
   p.dev.comb = reinterpret_cast<const CombEntry*>(sc + off_comb);
   p.dev.readout = reinterpret_cast<const int32_t*>(sc + off_ro);
+  p.dev.row_block = p.dev.readout;  // one row per lane: row l is block l (identity)
   p.dev.part_ml = reinterpret_cast<float2*>(sc + off_ml);
   p.dev.part_o = reinterpret_cast<float*>(sc + off_o);
 

@@ -21,11 +21,12 @@ struct alignas(16) DecItem {
   int32_t kv_begin, kv_end, part_base, pad;
 };
 
-// How the combine step finds the partials of (row, kv head): chunk c of query
-// q lives at part_base + c * stride + q_off + (h % G).  nchunks < 0 marks rows
+// How the combine step finds the partials of a row block (the rows one work
+// item serves) and kv head: row r of the block, q head h, chunk c lives at
+// part_base + c * stride + (r - row0) * G + (h % G).  nchunks < 0 marks blocks
 // whose outputs the tensor-core kernel wrote directly (nothing to combine).
 struct alignas(16) CombEntry {
-  int32_t part_base, nchunks, stride, q_off;
+  int32_t part_base, nchunks, stride, row0;
 };
 
 // Work item of the tensor-core attention kernel: up to NT tiles of 128 query
@@ -78,7 +79,8 @@ struct DevMeta {
   const float* rope_freq;           // [d/2]
   const DecItem* dec_items;
   const TcItem* tc_items;
-  const CombEntry* comb;            // [N * Hkv]
+  const CombEntry* comb;            // [row blocks * Hkv]
+  const int32_t* row_block;         // [N] row block of each row
   float* part_o;                    // [num_part_slots][d] unnormalised
   float2* part_ml;                  // [num_part_slots] (max, sum), log2 domain
   const MaskBlock* mblocks;         // [num_mblocks] (masked passes with tensor-core lanes)

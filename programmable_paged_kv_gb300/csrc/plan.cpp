@@ -104,6 +104,7 @@ struct HostPlan {
   std::vector<DecItem> dec;
   std::vector<TcItem> tc;
   std::vector<CombEntry> comb;
+  std::vector<int32_t> row_block;
   int64_t num_part_slots = 0;
   int64_t total_pages = 0;
 };
@@ -204,16 +205,26 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   }
   // Hazard freedom (Pie review, Eq. (4)): the rows of one pass write
   // pairwise distinct physical slots.
+  // Checked with an open-addressing hash set of the physical targets
+  // (linear time; the table is reused across plans on a thread).
   {
-    std::vector<int64_t> tgt(N);
+    static thread_local std::vector<int64_t> table;
+    int bits = 6;
+    while ((int64_t(1) << bits) < 2 * static_cast<int64_t>(N)) ++bits;
+    const size_t size = size_t(1) << bits;
+    if (table.size() < size) table.resize(size);
+    std::fill(table.begin(), table.begin() + size, int64_t(-1));
     for (int r = 0; r < N; ++r) {
       const int l = H.row_lane[r], s = M.slots[r];
       const int64_t page = M.page_ids[M.page_indptr[l] + s / D.page_size];
-      tgt[r] = page * D.page_size + s % D.page_size;
+      const int64_t key = page * D.page_size + s % D.page_size;
+      size_t h = static_cast<size_t>((static_cast<uint64_t>(key) * 0x9E3779B97F4A7C15ull) >> (64 - bits));
+      while (table[h] != -1) {
+        if (table[h] == key) return fail(PIE_EINVAL, "two rows write the same physical slot");
+        h = (h + 1) & (size - 1);
+      }
+      table[h] = key;
     }
-    std::sort(tgt.begin(), tgt.end());
-    if (std::adjacent_find(tgt.begin(), tgt.end()) != tgt.end())
-      return fail(PIE_EINVAL, "two rows write the same physical slot");
   }
   H.has_mask = M.mask_word_indptr != nullptr;
   if (H.has_mask) {
@@ -291,7 +302,8 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   const int64_t tc_target = 4 * kTcTargetSms;
   const int64_t tc_ch = tc_units >= tc_target ? INT32_MAX
                         : std::max<int64_t>(512, (tc_total + tc_target - 1) / tc_target);
-  H.comb.assign(static_cast<size_t>(N) * Hkv, CombEntry{0, 0, 0, 0});
+  H.comb.clear();
+  H.row_block.assign(N, 0);
   H.dec.clear();
   H.tc.clear();
   // masked passes: tensor-core lanes walk the compacted list of the slots
@@ -327,27 +339,24 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
     const bool use_tc = lane_tc(l);
     const int blk_rows = use_tc ? tc_rows : rows_per_item;
     const int stride = use_tc ? kTcTileQueries : H.nq;
-    for (int g = 0; g < Hkv; ++g) {
-      for (int b0 = r0; b0 < r1; b0 += blk_rows) {
-        const int b1 = std::min(r1, b0 + blk_rows);
-        const int ext = extent(l, b0, b1);
-        int nchunks, chunk;
-        if (use_tc) {
-          nchunks = static_cast<int>(std::max<int64_t>(1, (ext + tc_ch / 2) / tc_ch));
-          chunk = ((ext + nchunks - 1) / nchunks + kTcTileSlots - 1) / kTcTileSlots * kTcTileSlots;
-          nchunks = std::max(1, (ext + chunk - 1) / std::max(1, chunk));
-        } else {
-          nchunks = (ext + CH - 1) / CH;
-          chunk = CH;
-        }
-        const bool direct = use_tc && nchunks == 1;
-        for (int r = b0; r < b1; ++r) {
-          CombEntry& e = H.comb[static_cast<size_t>(r) * Hkv + g];
-          e.part_base = static_cast<int32_t>(part);
-          e.nchunks = direct ? -1 : nchunks;
-          e.stride = use_tc ? stride * H.tc_nt : stride;
-          e.q_off = (r - b0) * G;
-        }
+    for (int b0 = r0; b0 < r1; b0 += blk_rows) {
+      const int b1 = std::min(r1, b0 + blk_rows);
+      const int32_t blk_id = static_cast<int32_t>(H.comb.size() / Hkv);
+      for (int r = b0; r < b1; ++r) H.row_block[r] = blk_id;
+      const int ext = extent(l, b0, b1);
+      int nchunks, chunk;
+      if (use_tc) {
+        nchunks = static_cast<int>(std::max<int64_t>(1, (ext + tc_ch / 2) / tc_ch));
+        chunk = ((ext + nchunks - 1) / nchunks + kTcTileSlots - 1) / kTcTileSlots * kTcTileSlots;
+        nchunks = std::max(1, (ext + chunk - 1) / std::max(1, chunk));
+      } else {
+        nchunks = (ext + CH - 1) / CH;
+        chunk = CH;
+      }
+      const bool direct = use_tc && nchunks == 1;
+      for (int g = 0; g < Hkv; ++g) {
+        H.comb.push_back(CombEntry{static_cast<int32_t>(part), direct ? -1 : nchunks,
+                                   use_tc ? stride * H.tc_nt : stride, b0});
         for (int c = 0; c < nchunks; ++c) {
           const int kb = c * chunk, ke = std::min(ext, kb + chunk);
           if (use_tc) {
@@ -383,7 +392,8 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t row_indptr, positions, slots, kv_len, page_indptr, page_ids, fold_mode, fold_count,
-      row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks;
+      row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks,
+      row_block;
   size_t copy_bytes;  // everything above
   size_t part_o, part_ml, list, cmask, list_len;
   size_t total;
@@ -416,6 +426,7 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.dec = take(sizeof(DecItem) * H.dec.size());
   Y.tc = take(sizeof(TcItem) * H.tc.size());
   Y.comb = take(sizeof(CombEntry) * H.comb.size());
+  Y.row_block = take(sizeof(int32_t) * H.row_block.size());
   Y.mblocks = take(sizeof(MaskBlock) * H.mblocks.size());
   Y.copy_bytes = o;
   Y.part_o = take(sizeof(float) * static_cast<size_t>(H.num_part_slots) * D.head_dim);
@@ -485,6 +496,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   put(Y.dec, H.dec.data(), sizeof(DecItem) * H.dec.size());
   put(Y.tc, H.tc.data(), sizeof(TcItem) * H.tc.size());
   put(Y.comb, H.comb.data(), sizeof(CombEntry) * H.comb.size());
+  put(Y.row_block, H.row_block.data(), sizeof(int32_t) * H.row_block.size());
   put(Y.mblocks, H.mblocks.data(), sizeof(MaskBlock) * H.mblocks.size());
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -535,6 +547,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.dec_items = reinterpret_cast<const DecItem*>(w + Y.dec);
   dm.tc_items = reinterpret_cast<const TcItem*>(w + Y.tc);
   dm.comb = reinterpret_cast<const CombEntry*>(w + Y.comb);
+  dm.row_block = reinterpret_cast<const int32_t*>(w + Y.row_block);
   dm.part_o = reinterpret_cast<float*>(w + Y.part_o);
   dm.part_ml = reinterpret_cast<float2*>(w + Y.part_ml);
   dm.mblocks = reinterpret_cast<const MaskBlock*>(w + Y.mblocks);
