@@ -55,16 +55,38 @@ struct __align__(1024) Smem {
   uint8_t v[NS][2][kHalfBytes];   // [stage][half of d][slot][128 B]
   uint64_t q_full;
   uint64_t kv_full[NS], kv_empty[NS];
-  uint64_t s_full[NT], p_full[NT], o_done[NT];
+  uint64_t s_full[2], p_full[2];  // per score buffer group (see sgroup)
+  uint64_t o_done[NT], mma_done;
   uint32_t tmem_base;
 };
 
 template <int NT>
 struct Cfg {
-  static constexpr int NS = NT == 1 ? 3 : 2;            // KV stages that fit beside Q
+  static constexpr int NS = NT == 1 ? 3 : 2;  // KV stages that fit beside Q
   static constexpr int kThreads = 64 + 128 * NT;
-  static constexpr uint32_t kTmemCols = NT == 1 ? 256 : 512;  // per tile: S/P [0,128), O [128,256)
+  static constexpr uint32_t kTmemCols = 512;
 };
+
+// TMEM columns: two query tiles -> tile t keeps S (then P) at 256t and O at
+// 256t + 128; one query tile -> S/P alternate between columns 0 and 128 from
+// one KV tile to the next and O sits at 256.
+template <int NT>
+__device__ __forceinline__ uint32_t s_col(int t, int j) {
+  return NT == 2 ? 256u * t : 128u * (j & 1);
+}
+template <int NT>
+__device__ __forceinline__ uint32_t o_col(int t) {
+  return NT == 2 ? 256u * t + 128u : 256u;
+}
+// the s_full / p_full barrier of (query tile t, KV tile j) and its phase parity
+template <int NT>
+__device__ __forceinline__ int sgroup(int t, int j) {
+  return NT == 2 ? t : (j & 1);
+}
+template <int NT>
+__device__ __forceinline__ uint32_t sphase(int j) {
+  return NT == 2 ? (j & 1) : ((j >> 1) & 1);
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start address, leading
 // and stride byte offsets in 16-byte units, descriptor version 1, layout
@@ -215,9 +237,12 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       mbar_init(&S.kv_full[i], 1);
       mbar_init(&S.kv_empty[i], 1);
     }
+    mbar_init(&S.mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.s_full[i], 1);
+      mbar_init(&S.p_full[i], 4);
+    }
     for (int t = 0; t < NT; ++t) {
-      mbar_init(&S.s_full[t], 1);
-      mbar_init(&S.p_full[t], 4);
       mbar_init(&S.o_done[t], 1);
     }
     fence_barrier_init();
@@ -323,36 +348,66 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     if (lane == 0 && T > 0) {
       constexpr uint32_t ID_S = idesc(128, 128, false);
       constexpr uint32_t ID_O = idesc(128, 128, true);
-      if (!mbar_wait(&S.q_full, 0)) bad = true;
-      for (int j = 0; j < T && !bad; ++j) {
+      // S_t(j) = Q_t K_j^T into its TMEM buffer (waits for K_j with t == 0)
+      auto issue_s = [&](int t, int j) -> bool {
         const int st = j % NS;
-        if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) { bad = true; break; }
-        fence_after();
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t a = sdesc(S.q[t][k >> 2] + (k & 3) * 32, 16, 1024);
-            const uint64_t b = sdesc(S.k[st][k >> 2] + (k & 3) * 32, 16, 1024);
-            mma_ss(tmem + 256 * t, a, b, ID_S, k > 0 ? 1u : 0u);
-          }
-          commit(&S.s_full[t]);
+        if (t == 0) {
+          if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) return false;
+          fence_after();
         }
+        const uint32_t d = tmem + s_col<NT>(t, j);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sdesc(S.q[t][k >> 2] + (k & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc(S.k[st][k >> 2] + (k & 3) * 32, 16, 1024);
+          mma_ss(d, a, b, ID_S, k > 0 ? 1u : 0u);
+        }
+        commit(&S.s_full[sgroup<NT>(t, j)]);
+        return true;
+      };
+      // O_t += P_t(j) V_j once the softmax group has stored P_t(j)
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!mbar_wait(&S.p_full[sgroup<NT>(t, j)], sphase<NT>(j))) return false;
+        fence_after();
+        const int st = j % NS;
         const int valid = min(kTcTileSlots, ke - (kb + j * kTcTileSlots));
         const int ksteps = (valid + 15) >> 4;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (!mbar_wait(&S.p_full[t], j & 1)) { bad = true; break; }
-          fence_after();
-          for (int k = 0; k < ksteps; ++k) {
-            const uint64_t b = sdesc(S.v[st][0] + k * 2048, kHalfBytes, 1024);
-            mma_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * k, b, ID_O,
-                   (j > 0 || k > 0) ? 1u : 0u);
-          }
-          commit(&S.o_done[t]);
+        for (int k = 0; k < ksteps; ++k) {
+          const uint64_t b = sdesc(S.v[st][0] + k * 2048, kHalfBytes, 1024);
+          mma_ts(tmem + o_col<NT>(t), tmem + s_col<NT>(t, j) + 8 * k, b, ID_O,
+                 (j > 0 || k > 0) ? 1u : 0u);
         }
-        commit(&S.kv_empty[st]);
+        commit(&S.o_done[t]);
+        return true;
+      };
+      // Issue order keeps the tensor pipe busy while softmax runs: with two
+      // query tiles, P_0 V and the next S_0 go between the two groups'
+      // softmax steps; with one, the score buffers alternate so the next
+      // tile's S is computed while this tile's softmax runs.  The pipe
+      // executes one thread's tcgen05.mma in order, so a buffer's P is always
+      // consumed before the next S overwrites it.
+      bool ok = mbar_wait(&S.q_full, 0);
+      if (NT == 2) {
+        ok = ok && issue_s(0, 0) && issue_s(1, 0);
+        for (int j = 0; j < T && ok; ++j) {
+          ok = issue_pv(0, j) && (j + 1 >= T || issue_s(0, j + 1)) && issue_pv(1, j);
+          if (!ok) break;
+          commit(&S.kv_empty[j % NS]);
+          ok = j + 1 >= T || issue_s(1, j + 1);
+        }
+      } else {
+        ok = ok && issue_s(0, 0) && (T < 2 || issue_s(0, 1));
+        for (int j = 0; j < T && ok; ++j) {
+          ok = issue_pv(0, j);
+          if (!ok) break;
+          commit(&S.kv_empty[j % NS]);
+          ok = j + 2 >= T || issue_s(0, j + 2);
+        }
       }
+      // every MMA must have finished before the TMEM is released
+      commit(&S.mma_done);
+      if (!mbar_wait(&S.mma_done, 0)) ok = false;
+      bad = !ok;
     }
   } else if (T > 0) {
     // ---------------- softmax groups: thread = query row ---------------------
@@ -372,8 +427,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     if (masked && valid_q)
       mrow = gather ? m.cmask + mb.cmask_off + int64_t(row - mb.r0) * mb.nw
                     : mask_words + m.mask_word_indptr[row];
-    const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + 256 * t;
-    const uint32_t tS = lane_base, tO = lane_base + 128;
+    const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
+    const uint32_t tO = lane_base + o_col<NT>(t);
     float m_used = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
       const int ts = kb + j * kTcTileSlots;
@@ -382,7 +437,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
 #pragma unroll
         for (int i = 0; i < 4; ++i) words[i] = ts + 32 * i < ke ? mrow[(ts >> 5) + i] : 0u;
       }
-      if (!mbar_wait(&S.s_full[t], j & 1)) { bad = true; break; }
+      const uint32_t tS = lane_base + s_col<NT>(t, j);
+      if (!mbar_wait(&S.s_full[sgroup<NT>(t, j)], sphase<NT>(j))) { bad = true; break; }
       fence_after();
       if (warp_live) {
         float s[128];
@@ -422,9 +478,16 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         }
         l_run = l_run * alpha + rs;
         m_used = m_new;
-        // P.V of the previous tile has completed (it precedes this tile's S
-        // in the in-order tensor pipe), so P may be replaced and O rescaled.
+        // This buffer's previous P was consumed before this tile's S was
+        // computed (in-order tensor pipe), so P may be stored now.  O is
+        // rescaled only after the previous tile's P.V has landed in it; the
+        // wait is taken at every tile so that this thread never falls two
+        // phases behind the barrier.
         tmem_st64(tS, pk);
+        if (j > 0) {
+          if (!mbar_wait(&S.o_done[t], (j - 1) & 1)) { bad = true; break; }
+          fence_after();
+        }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           float o[128];
           tmem_ld128(tO, o);
@@ -447,7 +510,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full[t]);
+      if (lane == 0) mbar_arrive(&S.p_full[sgroup<NT>(t, j)]);
     }
     if (!bad && !mbar_wait(&S.o_done[t], (T - 1) & 1)) bad = true;
     fence_after();
