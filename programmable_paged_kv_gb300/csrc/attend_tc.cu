@@ -447,35 +447,45 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         const bool all_vis = (ts + kTcTileSlots <= ke) &&
                              (mask_words ? ((words[0] & words[1] & words[2] & words[3]) == ~0u)
                                          : (ts + kTcTileSlots - 1 <= row_slot));
-        float mx = -INFINITY;
-        if (__all_sync(0xffffffffu, all_vis || !valid_q)) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        } else {
+        if (!__all_sync(0xffffffffu, all_vis || !valid_q)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int sa = ts + c;
             const bool vis = valid_q && sa < ke &&
                              (mask_words ? ((words[c >> 5] >> (c & 31)) & 1u) != 0 : sa <= row_slot);
             s[c] = vis ? s[c] : -INFINITY;
-            mx = fmaxf(mx, s[c]);
           }
         }
+        // row max: three-input max over four independent chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = max3(m4[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        }
+        const float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         const float m_tile = mx * scale_log2;  // scale > 0: max commutes with it
         float m_new = m_used;
         if (m_used == -INFINITY || m_tile > m_used + 8.f) m_new = fmaxf(m_used, m_tile);
         const float alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
         const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-        float rs = 0.f;
+        // p = 2^(s * scale - m) for a pair per packed FMA; row sum by packed
+        // adds into four pair accumulators
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], scale_log2, neg_m));
-          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, neg_m));
-          rs += p0 + p1;
+          float x0, x1;
+          ffma2(x0, x1, s[2 * c], s[2 * c + 1], scale_log2, scale_log2, neg_m, neg_m);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          fadd2(acc[2 * (c & 3)], acc[2 * (c & 3) + 1], p0, p1);
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pk[c] = *reinterpret_cast<uint32_t*>(&h2);
         }
+        fadd2(acc[0], acc[1], acc[2], acc[3]);
+        fadd2(acc[4], acc[5], acc[6], acc[7]);
+        fadd2(acc[0], acc[1], acc[4], acc[5]);
+        const float rs = acc[0] + acc[1];
         l_run = l_run * alpha + rs;
         m_used = m_new;
         // This buffer's previous P was consumed before this tile's S was
