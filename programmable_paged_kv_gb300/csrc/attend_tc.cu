@@ -5,24 +5,27 @@
 //
 // One CTA handles a work item: NT (1 or 2) tiles of 128 query vectors (the G
 // heads of a kv group for 128/G consecutive rows of one lane per tile,
-// head-minor) against one chunk of the lane's slots, in 128-slot KV tiles.
-// With NT = 2 both query tiles share every K/V tile, so the KV chunk is read
-// once for 256 query vectors.
+// head-minor) against one chunk of the lane's slots, in KV tiles of BN slots
+// (128 with one query tile, 64 with two, so that two score buffers per query
+// tile and every tile's O fit the 512 TMEM columns).  With NT = 2 both query
+// tiles share every K/V tile, so the chunk is read once for 256 query vectors.
 //   warp 0   TMA producer: the query tiles once (4-D tensor map over q_rot
 //            viewed as [N][Hkv][G][d]), then per KV tile the K and V blocks
 //            of every page in the tile (2-D tensor maps over the pools, one
 //            64-column box per half of d, 128-byte swizzle) into an NS-deep
-//            ring of stages;
-//   warp 1   allocates TMEM and, from one thread, issues for every KV tile
-//            S_t = Q_t K^T (M=128, N=128, operands in shared memory) for each
-//            query tile, then O_t += P_t V with P_t read from TMEM (it
-//            overwrites the first half of S_t's columns as packed bf16) and V
-//            used MN-major straight from its tile; tcgen05.commit arrives on
-//            mbarriers.  tcgen05.mma issued by one thread execute in order,
-//            so S_t of the next tile never overwrites P_t before P_t V reads
-//            it;
-//   warps 2+ one 4-warp softmax group per query tile: each thread owns one
-//            query row (its TMEM lane), loads its 128 scores with one
+//            ring of stages; in gather mode (masked passes) the rows of the
+//            listed slots with tile::gather4;
+//   warps 1..NT  one MMA issuer per query tile t (warp 1 also allocates the
+//            512 TMEM columns): from one thread, S_t = Q_t K^T (M=128, N=BN)
+//            into one of two score buffers and O_t += P_t V (M=128, N=128,
+//            K=BN) with P_t read from TMEM, where the softmax stored it over
+//            the first half of the score buffer.  Scores for KV tile j+2 are
+//            issued right after P.V of tile j (the in-order tensor pipe
+//            guarantees that P is read first), so the softmax of tile j+1
+//            never waits for them; two issuers keep both tiles' chains in
+//            flight at once;
+//   warps 1+NT.. one 4-warp softmax group per query tile: each thread owns one
+//            query row (its TMEM lane), loads its BN scores with one
 //            tcgen05.ld, applies the row's visibility (slot-causal or its
 //            mask words; tiles visible in full skip the per-column test),
 //            keeps the online max/sum in the log2 domain (the max used for
@@ -46,47 +49,41 @@ namespace pie {
 
 namespace tc {
 
-constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes: one half of d for one tile
+constexpr int kQHalf = 128 * 128;        // 128 query rows x 128 bytes (half of d)
 
-template <int NT, int NS>
-struct __align__(1024) Smem {
-  uint8_t q[NT][2][kHalfBytes];   // [query tile][half of d][query][128 B]
-  uint8_t k[NS][2][kHalfBytes];   // [stage][half of d][slot][128 B]
-  uint8_t v[NS][2][kHalfBytes];   // [stage][half of d][slot][128 B]
-  uint64_t q_full;
-  uint64_t kv_full[NS], kv_empty[NS];
-  uint64_t s_full[2], p_full[2];  // per score buffer group (see sgroup)
-  uint64_t o_done[NT], mma_done;
-  uint32_t tmem_base;
-};
-
+// Tile geometry per number of query tiles.  TMEM holds two score buffers per
+// query tile plus each tile's 128-column O: one query tile takes 128-slot KV
+// tiles (2 x 128 + 128 columns), two query tiles 64-slot ones (4 x 64 + 256).
 template <int NT>
 struct Cfg {
-  static constexpr int NS = NT == 1 ? 3 : 2;  // KV stages that fit beside Q
-  static constexpr int kThreads = 64 + 128 * NT;
+  static constexpr int BN = NT == 1 ? 128 : 64;     // KV slots per tile
+  static constexpr int kKvHalf = BN * 128;          // BN slot rows x 128 bytes (half of d)
+  static constexpr int NS = NT == 1 ? 3 : 4;        // KV stages beside the query tiles
+  static constexpr int kIssuers = NT;               // one MMA-issuing warp per query tile
+  static constexpr int kSoftmaxWarp0 = 1 + kIssuers;  // first softmax warp
+  static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * NT;
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// TMEM columns: two query tiles -> tile t keeps S (then P) at 256t and O at
-// 256t + 128; one query tile -> S/P alternate between columns 0 and 128 from
-// one KV tile to the next and O sits at 256.
 template <int NT>
-__device__ __forceinline__ uint32_t s_col(int t, int j) {
-  return NT == 2 ? 256u * t : 128u * (j & 1);
-}
-template <int NT>
-__device__ __forceinline__ uint32_t o_col(int t) {
-  return NT == 2 ? 256u * t + 128u : 256u;
-}
-// the s_full / p_full barrier of (query tile t, KV tile j) and its phase parity
-template <int NT>
-__device__ __forceinline__ int sgroup(int t, int j) {
-  return NT == 2 ? t : (j & 1);
-}
-template <int NT>
-__device__ __forceinline__ uint32_t sphase(int j) {
-  return NT == 2 ? (j & 1) : ((j >> 1) & 1);
-}
+struct __align__(1024) Smem {
+  static constexpr int NS = Cfg<NT>::NS, KVH = Cfg<NT>::kKvHalf;
+  uint8_t q[NT][2][kQHalf];    // [query tile][half of d][query][128 B]
+  uint8_t k[NS][2][KVH];       // [stage][half of d][slot][128 B]
+  uint8_t v[NS][2][KVH];       // [stage][half of d][slot][128 B]
+  uint64_t q_full;
+  uint64_t kv_full[NS], kv_empty[NS];
+  uint64_t s_full[NT][2], p_full[NT][2];  // per (query tile, score buffer)
+  uint64_t o_done[NT], mma_done[NT];
+  uint64_t tail_zero;  // the last tile's V rows past the visible end are zeroed
+  uint32_t tmem_base;
+};
+
+// TMEM columns: score buffer b of query tile t at (2t + b) BN (the softmax
+// stores P over its first BN/2 columns); O of query tile t at 256 + 128t.
+template <int BN>
+__device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(BN) * (2 * t + b); }
+__device__ __forceinline__ uint32_t o_col(int t) { return 256u + 128u * t; }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start address, leading
 // and stride byte offsets in 16-byte units, descriptor version 1, layout
@@ -149,6 +146,13 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* f) {
   for (int i = 0; i < 128; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* f) {
+  uint32_t r[64];
+  asm volatile(PIE_TMEM_LD64_ASM : PIE_TMEM_LD64_OUTS : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st128(uint32_t taddr, const float* f) {
   uint32_t r[128];
 #pragma unroll
@@ -156,8 +160,24 @@ __device__ __forceinline__ void tmem_st128(uint32_t taddr, const float* f) {
   asm volatile(PIE_TMEM_ST128_ASM ::"r"(taddr), PIE_TMEM_ST_INS : "memory");
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(PIE_TMEM_ST32_ASM ::"r"(taddr), PIE_TMEM_ST32_INS : "memory");
+}
+
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t* r) {
   asm volatile(PIE_TMEM_ST64_ASM ::"r"(taddr), PIE_TMEM_ST64_INS : "memory");
+}
+
+// BN fp32 scores of this thread's TMEM lane, and BN/2 packed bf16 pairs back
+template <int BN>
+__device__ __forceinline__ void load_scores(uint32_t taddr, float* f) {
+  if constexpr (BN == 128) tmem_ld128(taddr, f);
+  else tmem_ld64(taddr, f);
+}
+template <int BN>
+__device__ __forceinline__ void store_p(uint32_t taddr, const uint32_t* r) {
+  if constexpr (BN == 128) tmem_st64(taddr, r);
+  else tmem_st32(taddr, r);
 }
 
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -197,6 +217,27 @@ struct Out {
   float* lse_all;
 };
 
+// Row output: bf16 o / l to out_all and to every readout position of the row.
+__device__ __forceinline__ void write_row(const DevMeta& m, const Out& out, int Hq, int row,
+                                          int head, const uint4* packed, float lse) {
+  constexpr int D = 128;
+  if (out.out_all) {
+    uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) dst[c] = packed[c];
+  }
+  if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = lse;
+  for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
+    const int jj = m.ro_idx[r];
+    if (out.out_readout) {
+      uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dst[c] = packed[c];
+    }
+    if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = lse;
+  }
+}
+
 }  // namespace tc
 
 template <int NT>
@@ -207,42 +248,43 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kgmap,
     const __grid_constant__ CUtensorMap vgmap) {
   using namespace tc;
-  constexpr int NS = Cfg<NT>::NS;
+  constexpr int NS = Cfg<NT>::NS, BN = Cfg<NT>::BN, kKvHalf = Cfg<NT>::kKvHalf;
   constexpr int D = 128;
   constexpr float kLn2 = 0.6931471805599453f;
-  using SM = Smem<NT, NS>;
+  using SM = Smem<NT>;
   extern __shared__ uint8_t smem_raw[];
   SM& S = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcItem it = m.tc_items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // gather mode (masked passes): positions [kb, ke) of the row block's
-  // compacted visible-slot list, this item's share of its 128-entry tiles;
-  // otherwise slots [kb, ke) of the lane
+  // compacted visible-slot list, this item's share of its tiles; otherwise
+  // slots [kb, ke) of the lane
   const bool gather = it.block >= 0;
   int kb = it.kv_begin, ke = it.kv_end;
   MaskBlock mb{0, 0, 0, 0, 0, 0, 0, 0};
   if (gather) {
     mb = m.mblocks[it.block];
     const int U = m.list_len[it.block];
-    const int tiles = (U + kTcTileSlots - 1) / kTcTileSlots;
-    kb = (it.chunk * tiles / it.nchunks) * kTcTileSlots;
-    ke = min(U, ((it.chunk + 1) * tiles / it.nchunks) * kTcTileSlots);
+    const int tiles = (U + BN - 1) / BN;
+    kb = (it.chunk * tiles / it.nchunks) * BN;
+    ke = min(U, ((it.chunk + 1) * tiles / it.nchunks) * BN);
   }
-  const int T = ke > kb ? (ke - kb + kTcTileSlots - 1) / kTcTileSlots : 0;
+  const int T = ke > kb ? (ke - kb + BN - 1) / BN : 0;
   const int nqv = it.nrows * G;  // valid query vectors of the item
 
   if (threadIdx.x == 0) {
     mbar_init(&S.q_full, 1);
+    for (int t = 0; t < NT; ++t) mbar_init(&S.mma_done[t], 1);
+    mbar_init(&S.tail_zero, 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(&S.kv_full[i], 1);
-      mbar_init(&S.kv_empty[i], 1);
-    }
-    mbar_init(&S.mma_done, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.s_full[i], 1);
-      mbar_init(&S.p_full[i], 4);
+      mbar_init(&S.kv_empty[i], Cfg<NT>::kIssuers);  // released by every issuer's P.V
     }
     for (int t = 0; t < NT; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&S.s_full[t][b], 1);
+        mbar_init(&S.p_full[t][b], 4);
+      }
       mbar_init(&S.o_done[t], 1);
     }
     fence_barrier_init();
@@ -265,7 +307,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     if (T > 0) {
       const uint64_t pol = policy_evict_first();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&S.q_full, NT * 2 * kHalfBytes);
+        mbar_arrive_expect_tx(&S.q_full, NT * 2 * kQHalf);
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -282,8 +324,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       //   gather mode: lane i -> listed slots ts + 4i .. ts + 4i + 3
       int y[4];
       auto coords = [&](int jj) {
-        const int ts = kb + jj * kTcTileSlots;
-        const int te = min(ts + kTcTileSlots, ke);
+        const int ts = kb + jj * BN;
+        const int te = min(ts + BN, ke);
         if (gather) {
           const int rows = ((te - ts) + 15) & ~15;
           if (4 * lane < rows) {
@@ -306,8 +348,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
           bad = true;
           break;
         }
-        const int ts = kb + j * kTcTileSlots;
-        const int te = min(ts + kTcTileSlots, ke);
+        const int ts = kb + j * BN;
+        const int te = min(ts + BN, ke);
         if (gather) {
           // slot-granular: 4 listed slots per lane, K and V rows of both halves
           // of d; rows up to the next multiple of 16 repeat the last listed
@@ -342,76 +384,88 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         }
         if (j + 1 < T) coords(j + 1);
       }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ---------------------------------------------
-    if (lane == 0 && T > 0) {
-      constexpr uint32_t ID_S = idesc(128, 128, false);
-      constexpr uint32_t ID_O = idesc(128, 128, true);
-      // S_t(j) = Q_t K_j^T into its TMEM buffer (waits for K_j with t == 0)
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j % NS;
-        if (t == 0) {
-          if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) return false;
-          fence_after();
+      // The last tile's V rows between its last visible slot and the end of
+      // that 16-slot MMA step hold whatever the page held past kv_len: once
+      // the tile has landed they are zeroed here, before any issuer's last
+      // P.V (which waits on tail_zero).  Gather mode loads finite rows there.
+      const int tl = kb + (T - 1) * BN, vl = min(BN, ke - tl);
+      if (!gather && (vl & 15) && !bad) {
+        const int stl = (T - 1) % NS;
+        if (mbar_wait(&S.kv_full[stl], ((T - 1) / NS) & 1)) {
+          const int nr = ((vl + 15) & ~15) - vl;
+          for (int i = lane; i < nr * 16; i += 32) {
+            const int h = i / (nr * 8), rem = i % (nr * 8);
+            *reinterpret_cast<uint4*>(S.v[stl][h] + (vl + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        } else {
+          bad = true;
         }
-        const uint32_t d = tmem + s_col<NT>(t, j);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tail_zero);
+    }
+  } else if (warp < Cfg<NT>::kSoftmaxWarp0) {
+    // ---------------- MMA issuers: one warp per query tile ---------------------
+    // Each issuer keeps its own tile's chain (S, softmax, P.V, next S) in
+    // flight, so one tile's handoff waits overlap the other's MMAs in the
+    // shared tensor pipe.  Shared-memory descriptors are built once and
+    // advanced by constant increments (address field in 16-byte units).
+    if (lane == 0 && T > 0) {
+      const int t = warp - 1;
+      constexpr uint32_t ID_S = idesc(128, BN, false);
+      constexpr uint32_t ID_O = idesc(128, 128, true);
+      const uint64_t dq = sdesc(S.q[t][0], 16, 1024);              // + (kQHalf >> 4) per half
+      const uint64_t dk = sdesc(S.k[0][0], 16, 1024);              // + (2 kKvHalf >> 4) per stage
+      const uint64_t dv = sdesc(S.v[0][0], kKvHalf, 1024);         // + 128 per 16-slot step
+      const uint32_t tO = tmem + o_col(t);
+      // S_t(j) = Q_t K_j^T into score buffer j & 1
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % NS;
+        if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) return false;
+        fence_after();
+        const uint32_t d = tmem + s_col<BN>(t, j & 1);
+        const uint64_t bk = dk + uint64_t(st) * (2 * kKvHalf >> 4);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(S.q[t][k >> 2] + (k & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc(S.k[st][k >> 2] + (k & 3) * 32, 16, 1024);
-          mma_ss(d, a, b, ID_S, k > 0 ? 1u : 0u);
+          const uint64_t off = uint64_t((k >> 2) * (kQHalf >> 4) + (k & 3) * 2);
+          const uint64_t offk = uint64_t((k >> 2) * (kKvHalf >> 4) + (k & 3) * 2);
+          mma_ss(d, dq + off, bk + offk, ID_S, k > 0 ? 1u : 0u);
         }
-        commit(&S.s_full[sgroup<NT>(t, j)]);
+        commit(&S.s_full[t][j & 1]);
         return true;
       };
       // O_t += P_t(j) V_j once the softmax group has stored P_t(j)
-      auto issue_pv = [&](int t, int j) -> bool {
-        if (!mbar_wait(&S.p_full[sgroup<NT>(t, j)], sphase<NT>(j))) return false;
+      auto issue_pv = [&](int j) -> bool {
+        if (!mbar_wait(&S.p_full[t][j & 1], (j >> 1) & 1)) return false;
+        if (j == T - 1 && !mbar_wait(&S.tail_zero, 0)) return false;
         fence_after();
         const int st = j % NS;
-        const int valid = min(kTcTileSlots, ke - (kb + j * kTcTileSlots));
+        const int valid = min(BN, ke - (kb + j * BN));
         const int ksteps = (valid + 15) >> 4;
-        for (int k = 0; k < ksteps; ++k) {
-          const uint64_t b = sdesc(S.v[st][0] + k * 2048, kHalfBytes, 1024);
-          mma_ts(tmem + o_col<NT>(t), tmem + s_col<NT>(t, j) + 8 * k, b, ID_O,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        }
+        const uint64_t bv = dv + uint64_t(st) * (2 * kKvHalf >> 4);
+        const uint32_t ta = tmem + s_col<BN>(t, j & 1);
+        for (int k = 0; k < ksteps; ++k)
+          mma_ts(tO, ta + 8 * k, bv + uint64_t(k) * (2048 >> 4), ID_O, (j > 0 || k > 0) ? 1u : 0u);
         commit(&S.o_done[t]);
+        commit(&S.kv_empty[st]);
         return true;
       };
-      // Issue order keeps the tensor pipe busy while softmax runs: with two
-      // query tiles, P_0 V and the next S_0 go between the two groups'
-      // softmax steps; with one, the score buffers alternate so the next
-      // tile's S is computed while this tile's softmax runs.  The pipe
-      // executes one thread's tcgen05.mma in order, so a buffer's P is always
-      // consumed before the next S overwrites it.
       bool ok = mbar_wait(&S.q_full, 0);
-      if (NT == 2) {
-        ok = ok && issue_s(0, 0) && issue_s(1, 0);
-        for (int j = 0; j < T && ok; ++j) {
-          ok = issue_pv(0, j) && (j + 1 >= T || issue_s(0, j + 1)) && issue_pv(1, j);
-          if (!ok) break;
-          commit(&S.kv_empty[j % NS]);
-          ok = j + 1 >= T || issue_s(1, j + 1);
-        }
-      } else {
-        ok = ok && issue_s(0, 0) && (T < 2 || issue_s(0, 1));
-        for (int j = 0; j < T && ok; ++j) {
-          ok = issue_pv(0, j);
-          if (!ok) break;
-          commit(&S.kv_empty[j % NS]);
-          ok = j + 2 >= T || issue_s(0, j + 2);
-        }
+      for (int jj = 0; jj < 2 && jj < T && ok; ++jj) ok = issue_s(jj);
+      for (int j = 0; j < T && ok; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < T) ok = issue_s(j + 2);
       }
-      // every MMA must have finished before the TMEM is released
-      commit(&S.mma_done);
-      if (!mbar_wait(&S.mma_done, 0)) ok = false;
+      // every MMA of this issuer must have finished before TMEM is released
+      commit(&S.mma_done[t]);
+      if (!mbar_wait(&S.mma_done[t], 0)) ok = false;
       bad = !ok;
     }
   } else if (T > 0) {
     // ---------------- softmax groups: thread = query row ---------------------
-    const int t = (warp - 2) >> 2;      // query tile of this group
+    const int t = (warp - Cfg<NT>::kSoftmaxWarp0) >> 2;  // query tile of this group
     const int quad = warp & 3;          // TMEM lane quadrant of this warp
     const int qm = quad * 32 + lane;    // query row within the tile == TMEM lane
     const int q = t * kTcTileQueries + qm;
@@ -428,38 +482,43 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       mrow = gather ? m.cmask + mb.cmask_off + int64_t(row - mb.r0) * mb.nw
                     : mask_words + m.mask_word_indptr[row];
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
-    const uint32_t tO = lane_base + o_col<NT>(t);
+    const uint32_t tO = lane_base + o_col(t);
     float m_used = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
-      const int ts = kb + j * kTcTileSlots;
-      uint32_t words[4] = {~0u, ~0u, ~0u, ~0u};
+      const int ts = kb + j * BN;
+      const uint32_t tS = lane_base + s_col<BN>(t, j & 1);
+      constexpr int NW = BN / 32;  // mask words per tile
+      uint32_t words[NW];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) words[i] = ~0u;
       if (mrow) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) words[i] = ts + 32 * i < ke ? mrow[(ts >> 5) + i] : 0u;
+        for (int i = 0; i < NW; ++i) words[i] = ts + 32 * i < ke ? mrow[(ts >> 5) + i] : 0u;
       }
-      const uint32_t tS = lane_base + s_col<NT>(t, j);
-      if (!mbar_wait(&S.s_full[sgroup<NT>(t, j)], sphase<NT>(j))) { bad = true; break; }
+      if (!mbar_wait(&S.s_full[t][j & 1], (j >> 1) & 1)) { bad = true; break; }
       fence_after();
       if (warp_live) {
-        float s[128];
-        tmem_ld128(tS, s);
+        float s[BN];
+        load_scores<BN>(tS, s);
         // a tile every column of which every live row of the warp sees
-        const bool all_vis = (ts + kTcTileSlots <= ke) &&
-                             (mask_words ? ((words[0] & words[1] & words[2] & words[3]) == ~0u)
-                                         : (ts + kTcTileSlots - 1 <= row_slot));
+        uint32_t wand = ~0u;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) wand &= words[i];
+        const bool all_vis = (ts + BN <= ke) &&
+                             (masked ? (wand == ~0u) : (ts + BN - 1 <= row_slot));
         if (!__all_sync(0xffffffffu, all_vis || !valid_q)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < BN; ++c) {
             const int sa = ts + c;
             const bool vis = valid_q && sa < ke &&
-                             (mask_words ? ((words[c >> 5] >> (c & 31)) & 1u) != 0 : sa <= row_slot);
+                             (masked ? ((words[c >> 5] >> (c & 31)) & 1u) != 0 : sa <= row_slot);
             s[c] = vis ? s[c] : -INFINITY;
           }
         }
         // row max: three-input max over four independent chains
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
+        for (int c = 0; c < BN; c += 8) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) m4[i] = max3(m4[i], s[c + 2 * i], s[c + 2 * i + 1]);
         }
@@ -472,9 +531,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         // p = 2^(s * scale - m) for a pair per packed FMA; row sum by packed
         // adds into four pair accumulators
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[64];
+        uint32_t pk[BN / 2];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < BN / 2; ++c) {
           float x0, x1;
           ffma2(x0, x1, s[2 * c], s[2 * c + 1], scale_log2, scale_log2, neg_m, neg_m);
           const float p0 = ex2(x0), p1 = ex2(x1);
@@ -485,84 +544,62 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         fadd2(acc[0], acc[1], acc[2], acc[3]);
         fadd2(acc[4], acc[5], acc[6], acc[7]);
         fadd2(acc[0], acc[1], acc[4], acc[5]);
-        const float rs = acc[0] + acc[1];
-        l_run = l_run * alpha + rs;
+        l_run = l_run * alpha + (acc[0] + acc[1]);
         m_used = m_new;
-        // This buffer's previous P was consumed before this tile's S was
-        // computed (in-order tensor pipe), so P may be stored now.  O is
-        // rescaled only after the previous tile's P.V has landed in it; the
-        // wait is taken at every tile so that this thread never falls two
-        // phases behind the barrier.
-        tmem_st64(tS, pk);
+        // The buffer's previous P was read by P.V of tile j-2, which the
+        // tensor pipe executed before this tile's S, so P may be stored now.
+        store_p<BN>(tS, pk);
+        // O is rescaled only after P.V of tile j-1 has landed in it; the wait
+        // is taken at every tile so that this thread never falls two phases
+        // behind the barrier.
         if (j > 0) {
           if (!mbar_wait(&S.o_done[t], (j - 1) & 1)) { bad = true; break; }
           fence_after();
-        }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          float o[128];
-          tmem_ld128(tO, o);
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            float o[128];
+            tmem_ld128(tO, o);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) o[c] *= alpha;
-          tmem_st128(tO, o);
+            for (int c = 0; c < 128; ++c) o[c] *= alpha;
+            tmem_st128(tO, o);
+          }
         }
-      }
-      // last tile: zero the V rows between the last valid slot and the end of
-      // its 16-slot MMA step (they hold whatever the page held past kv_len)
-      const int valid = min(kTcTileSlots, ke - ts);
-      if (!gather && t == 0 && j == T - 1 && (valid & 15)) {
-        const int r0 = valid, nr = ((valid + 15) & ~15) - valid;
-        for (int i = threadIdx.x - 64; i < nr * 16; i += 128) {
-          const int h = i / (nr * 8), rem = i % (nr * 8);
-          *reinterpret_cast<uint4*>(S.v[j % NS][h] + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full[sgroup<NT>(t, j)]);
+      if (lane == 0) mbar_arrive(&S.p_full[t][j & 1]);
     }
-    if (!bad && !mbar_wait(&S.o_done[t], (T - 1) & 1)) bad = true;
-    fence_after();
     if (warp_live && !bad) {
-      float o[128];
-      tmem_ld128(tO, o);
-      if (valid_q) {
-        if (it.direct) {
-          const bool empty = !(l_run > 0.f);
-          const float inv = empty ? 0.f : 1.f / l_run;
-          const float lse = empty ? -INFINITY : (m_used + log2f(l_run)) * kLn2;
-          uint4 packed[16];
+      if (!mbar_wait(&S.o_done[t], (T - 1) & 1)) {
+        bad = true;
+      } else {
+        fence_after();
+        float o[128];
+        tmem_ld128(tO, o);
+        if (valid_q) {
+          if (it.direct) {
+            const bool empty = !(l_run > 0.f);
+            const float inv = empty ? 0.f : 1.f / l_run;
+            const float lse = empty ? -INFINITY : (m_used + log2f(l_run)) * kLn2;
+            uint4 packed[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            uint32_t w[4];
+            for (int c = 0; c < 16; ++c) {
+              uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
-              w[e] = *reinterpret_cast<uint32_t*>(&h2);
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h2 =
+                    __floats2bfloat162_rn(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
+                w[e] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              packed[c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            packed[c] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          if (out.out_all) {
-            uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
+            write_row(m, out, Hq, row, head, packed, lse);
+          } else {
+            float4* po = reinterpret_cast<float4*>(m.part_o + int64_t(it.part_base + q) * D);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dst[c] = packed[c];
+            for (int c = 0; c < 32; ++c)
+              po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            m.part_ml[it.part_base + q] = make_float2(m_used, l_run);
           }
-          if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = lse;
-          for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
-            const int jj = m.ro_idx[r];
-            if (out.out_readout) {
-              uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
-#pragma unroll
-              for (int c = 0; c < 16; ++c) dst[c] = packed[c];
-            }
-            if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = lse;
-          }
-        } else {
-          float4* po = reinterpret_cast<float4*>(m.part_o + int64_t(it.part_base + q) * D);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) po[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-          m.part_ml[it.part_base + q] = make_float2(m_used, l_run);
         }
       }
     }
@@ -573,20 +610,10 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     const int q = threadIdx.x;
     if (q < nqv) {
       if (it.direct) {
-        const int row = it.row0 + q / G, head = it.kv_head * G + q % G;
-        if (out.out_all) {
-          uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
-          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = -INFINITY;
-        for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
-          const int jj = m.ro_idx[r];
-          if (out.out_readout) {
-            uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
-            for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-          if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = -INFINITY;
-        }
+        uint4 zero[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) zero[c] = make_uint4(0u, 0u, 0u, 0u);
+        write_row(m, out, Hq, it.row0 + q / G, it.kv_head * G + q % G, zero, -INFINITY);
       } else {
         float* po = m.part_o + int64_t(it.part_base + q) * D;
         for (int c = 0; c < D; ++c) po[c] = 0.f;
@@ -642,7 +669,7 @@ static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words
                              uint32_t* status, const CUtensorMap& qm, const CUtensorMap& km,
                              const CUtensorMap& vm, const CUtensorMap& kgm,
                              const CUtensorMap& vgm, cudaStream_t s) {
-  const size_t smem = sizeof(tc::Smem<NT, tc::Cfg<NT>::NS>) + 1024;
+  const size_t smem = sizeof(tc::Smem<NT>) + 1024;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NT>,
