@@ -26,7 +26,7 @@ __all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _b
+    from .builder import build as _b
     return _b(force=force)
 
 

@@ -88,7 +88,7 @@ def load(path: str = LIB_PATH):
         return _lib
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library {path} is missing: run "
-                           "programmable_paged_kv_gb300.build.build() first")
+                           "programmable_paged_kv_gb300.builder.build() first")
     lib = C.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         f = getattr(lib, name)

@@ -74,7 +74,8 @@ struct __align__(1024) Smem {
   uint64_t q_full;
   uint64_t kv_full[NS], kv_empty[NS];
   uint64_t s_full[NT][2], p_full[NT][2];  // per (query tile, score buffer)
-  uint64_t o_done[NT], mma_done[NT];
+  uint64_t o_done[NT][2];  // P.V of tile j done, per (query tile, j & 1)
+  uint64_t mma_done[NT];
   uint64_t tail_zero;  // the last tile's V rows past the visible end are zeroed
   uint32_t tmem_base;
 };
@@ -285,7 +286,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         mbar_init(&S.s_full[t][b], 1);
         mbar_init(&S.p_full[t][b], 4);
       }
-      mbar_init(&S.o_done[t], 1);
+      mbar_init(&S.o_done[t][0], 1);
+      mbar_init(&S.o_done[t][1], 1);
     }
     fence_barrier_init();
   }
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         const uint32_t ta = tmem + s_col<BN>(t, j & 1);
         for (int k = 0; k < ksteps; ++k)
           mma_ts(tO, ta + 8 * k, bv + uint64_t(k) * (2048 >> 4), ID_O, (j > 0 || k > 0) ? 1u : 0u);
-        commit(&S.o_done[t]);
+        commit(&S.o_done[t][j & 1]);
         commit(&S.kv_empty[st]);
         return true;
       };
@@ -484,17 +486,22 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
     const uint32_t tO = lane_base + o_col(t);
     float m_used = -INFINITY, l_run = 0.f;
+    // the row's mask words of the next tile are loaded one tile ahead
+    constexpr int NW = BN / 32;  // mask words per tile
+    uint32_t wnext[NW];
+    auto load_words = [&](int jj) {
+      const int tt = kb + jj * BN;
+#pragma unroll
+      for (int i = 0; i < NW; ++i) wnext[i] = !mrow ? ~0u : (tt + 32 * i < ke ? mrow[(tt >> 5) + i] : 0u);
+    };
+    load_words(0);
     for (int j = 0; j < T; ++j) {
       const int ts = kb + j * BN;
       const uint32_t tS = lane_base + s_col<BN>(t, j & 1);
-      constexpr int NW = BN / 32;  // mask words per tile
       uint32_t words[NW];
 #pragma unroll
-      for (int i = 0; i < NW; ++i) words[i] = ~0u;
-      if (mrow) {
-#pragma unroll
-        for (int i = 0; i < NW; ++i) words[i] = ts + 32 * i < ke ? mrow[(ts >> 5) + i] : 0u;
-      }
+      for (int i = 0; i < NW; ++i) words[i] = wnext[i];
+      if (j + 1 < T) load_words(j + 1);
       if (!mbar_wait(&S.s_full[t][j & 1], (j >> 1) & 1)) { bad = true; break; }
       fence_after();
       if (warp_live) {
@@ -549,19 +556,19 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         // The buffer's previous P was read by P.V of tile j-2, which the
         // tensor pipe executed before this tile's S, so P may be stored now.
         store_p<BN>(tS, pk);
-        // O is rescaled only after P.V of tile j-1 has landed in it; the wait
-        // is taken at every tile so that this thread never falls two phases
-        // behind the barrier.
-        if (j > 0) {
-          if (!mbar_wait(&S.o_done[t], (j - 1) & 1)) { bad = true; break; }
+        // O is rescaled, by the warps whose rows need it, only after P.V of
+        // tile j-1 has landed in it.  The completion barriers of P.V form a
+        // ring of two (by j & 1): P.V of tile j+1 cannot complete before this
+        // group arrives on p_full for it, so a warp that skips waits never
+        // sees a barrier two phases ahead of the one it waits on.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!mbar_wait(&S.o_done[t][(j - 1) & 1], ((j - 1) >> 1) & 1)) { bad = true; break; }
           fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            float o[128];
-            tmem_ld128(tO, o);
+          float o[128];
+          tmem_ld128(tO, o);
 #pragma unroll
-            for (int c = 0; c < 128; ++c) o[c] *= alpha;
-            tmem_st128(tO, o);
-          }
+          for (int c = 0; c < 128; ++c) o[c] *= alpha;
+          tmem_st128(tO, o);
         }
       }
       fence_before();
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       if (lane == 0) mbar_arrive(&S.p_full[t][j & 1]);
     }
     if (warp_live && !bad) {
-      if (!mbar_wait(&S.o_done[t], (T - 1) & 1)) {
+      if (!mbar_wait(&S.o_done[t][(T - 1) & 1], ((T - 1) >> 1) & 1)) {
         bad = true;
       } else {
         fence_after();

@@ -25,6 +25,14 @@ def test_library_exports_every_header_function(lib):
         assert n in abi.SIGNATURES, n
 
 
+def test_build_can_be_called_again(lib):
+    # the package's build() stays the function after its builder module loads
+    import programmable_paged_kv_gb300 as pk
+    assert callable(pk.build)
+    pk.build()
+    assert callable(pk.build)
+
+
 def test_abi_version(lib):
     assert lib.pie_fwd_abi_version() == 100
 
