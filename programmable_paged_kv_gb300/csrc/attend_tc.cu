@@ -9,13 +9,15 @@
 // (128 with one query tile, 64 with two, so that two score buffers per query
 // tile and every tile's O fit the 512 TMEM columns).  With NT = 2 both query
 // tiles share every K/V tile, so the chunk is read once for 256 query vectors.
-//   warp 0   TMA producer: the query tiles once (4-D tensor map over q_rot
-//            viewed as [N][Hkv][G][d]), then per KV tile the K and V blocks
-//            of every page in the tile (2-D tensor maps over the pools, one
-//            64-column box per half of d, 128-byte swizzle) into an NS-deep
-//            ring of stages; in gather mode (masked passes) the rows of the
-//            listed slots with tile::gather4;
-//   warps 1..NT  one MMA issuer per query tile t (warp 1 also allocates the
+//   warps 0, 1  TMA producers, K and V: the query tiles once (4-D tensor map
+//            over q_rot viewed as [N][Hkv][G][d]), then per KV tile the K (V)
+//            block of every page in the tile (2-D tensor maps over the pools,
+//            one 64-column box per half of d, 128-byte swizzle) into an
+//            NS-deep ring of stages, each copy from its own lane (a warp's
+//            copies issue one after another); in gather mode (masked passes)
+//            the rows of the listed slots with tile::gather4.  K and V land on
+//            separate barriers, so scores wait for K only;
+//   warps 2..1+NT  one MMA issuer per query tile t (warp 2 also allocates the
 //            512 TMEM columns): from one thread, S_t = Q_t K^T (M=128, N=BN)
 //            into one of two score buffers and O_t += P_t V (M=128, N=128,
 //            K=BN) with P_t read from TMEM, where the softmax stored it over
@@ -24,7 +26,7 @@
 //            guarantees that P is read first), so the softmax of tile j+1
 //            never waits for them; two issuers keep both tiles' chains in
 //            flight at once;
-//   warps 1+NT.. one 4-warp softmax group per query tile: each thread owns one
+//   warps 2+NT.. one 4-warp softmax group per query tile: each thread owns one
 //            query row (its TMEM lane), loads its BN scores with one
 //            tcgen05.ld, applies the row's visibility (slot-causal or its
 //            mask words; tiles visible in full skip the per-column test),
@@ -59,8 +61,9 @@ struct Cfg {
   static constexpr int BN = NT == 1 ? 128 : 64;     // KV slots per tile
   static constexpr int kKvHalf = BN * 128;          // BN slot rows x 128 bytes (half of d)
   static constexpr int NS = NT == 1 ? 3 : 4;        // KV stages beside the query tiles
+  static constexpr int kIssuer0 = 2;                // warps 0, 1: K and V producers
   static constexpr int kIssuers = NT;               // one MMA-issuing warp per query tile
-  static constexpr int kSoftmaxWarp0 = 1 + kIssuers;  // first softmax warp
+  static constexpr int kSoftmaxWarp0 = kIssuer0 + kIssuers;  // first softmax warp
   static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * NT;
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -72,7 +75,7 @@ struct __align__(1024) Smem {
   uint8_t k[NS][2][KVH];       // [stage][half of d][slot][128 B]
   uint8_t v[NS][2][KVH];       // [stage][half of d][slot][128 B]
   uint64_t q_full;
-  uint64_t kv_full[NS], kv_empty[NS];
+  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
   uint64_t s_full[NT][2], p_full[NT][2];  // per (query tile, score buffer)
   uint64_t o_done[NT][2];  // P.V of tile j done, per (query tile, j & 1)
   uint64_t mma_done[NT];
@@ -278,7 +281,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     for (int t = 0; t < NT; ++t) mbar_init(&S.mma_done[t], 1);
     mbar_init(&S.tail_zero, 1);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&S.kv_full[i], 1);
+      mbar_init(&S.k_full[i], 1);
+      mbar_init(&S.v_full[i], 1);
       mbar_init(&S.kv_empty[i], Cfg<NT>::kIssuers);  // released by every issuer's P.V
     }
     for (int t = 0; t < NT; ++t) {
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     }
     fence_barrier_init();
   }
-  if (warp == 1 && T > 0) {
+  if (warp == Cfg<NT>::kIssuer0 && T > 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&S.tmem_base)),
                  "r"(Cfg<NT>::kTmemCols)
@@ -304,11 +308,20 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   const uint32_t tmem = S.tmem_base;
   bool bad = false;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ------------------------------------------
+  if (warp < Cfg<NT>::kIssuer0) {
+    // ---------------- TMA producers: warp 0 loads K, warp 1 loads V ----------
+    // A warp's TMA copies issue one after another, so every copy of a tile
+    // comes from its own lane and the two tensors from two warps.
+    //   tile mode:   lane 2i + a -> page (ts / P + i) of the tile, half a of d
+    //                (at most BN / P <= 16 pages)
+    //   gather mode: lane o (and o + 32 for 128-slot tiles) -> rows 4(o/2) ..
+    //                4(o/2) + 3 of the tile, half o % 2 of d, one gather4 each
+    // The copies' pool rows come from the page table (tile mode) or the pool
+    // rows of the listed slots (gather mode), fetched one tile ahead.
+    const bool is_v = warp == 1;
     if (T > 0) {
       const uint64_t pol = policy_evict_first();
-      if (lane == 0) {
+      if (!is_v && lane == 0) {
         mbar_arrive_expect_tx(&S.q_full, NT * 2 * kQHalf);
 #pragma unroll
         for (int t = 0; t < NT; ++t)
@@ -317,30 +330,31 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
             tma_4d(S.q[t][a], &qmap, 64 * a, 0, it.kv_head, it.row0 + t * (kTcTileQueries / G),
                    &S.q_full);
       }
+      const CUtensorMap* map = gather ? (is_v ? &vgmap : &kgmap) : (is_v ? &vmap : &kmap);
+      uint64_t* full = is_v ? S.v_full : S.k_full;
       const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
-      const int32_t* list = gather ? m.list + mb.list_off : nullptr;
-      // The TMA coordinates of a tile come from the page table (and, in
-      // gather mode, the slot list): every lane fetches its share, one tile
-      // ahead, so no copy waits on a chain of dependent global loads.
-      //   tile mode:   lane i -> page (ts / P + i) of the tile
-      //   gather mode: lane i -> listed slots ts + 4i .. ts + 4i + 3
-      int y[4];
+      const int32_t* lrow = gather ? m.lrow + mb.list_off : nullptr;
+      const int hrow = it.kv_head * P;  // row offset of this kv head within a page
+      constexpr int GOPS = BN / 64;     // gather4 copies per lane and tile
+      int y[GOPS][4];
       auto coords = [&](int jj) {
         const int ts = kb + jj * BN;
         const int te = min(ts + BN, ke);
         if (gather) {
           const int rows = ((te - ts) + 15) & ~15;
-          if (4 * lane < rows) {
-            int sl[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sl[e] = list[min(ts + 4 * lane + e, te - 1)];
+          for (int i = 0; i < GOPS; ++i) {
+            const int r0 = 4 * ((lane + 32 * i) >> 1);
+            if (r0 < rows) {
+              // rows past the last listed slot repeat it (finite data for
+              // the zero-weight columns of the last 16-slot MMA step)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              y[e] = (pages[sl[e] / P] * Hkv + it.kv_head) * P + sl[e] % P;
+              for (int e = 0; e < 4; ++e) y[i][e] = lrow[min(ts + r0 + e, te - 1)] + hrow;
+            }
           }
         } else {
           const int p0 = ts / P, p1 = (te - 1) / P;
-          if (lane <= p1 - p0) y[0] = (pages[p0 + lane] * Hkv + it.kv_head) * P;
+          if ((lane >> 1) <= p1 - p0) y[0][0] = (pages[p0 + (lane >> 1)] * Hkv + it.kv_head) * P;
         }
       };
       coords(0);
@@ -352,61 +366,52 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         }
         const int ts = kb + j * BN;
         const int te = min(ts + BN, ke);
+        uint8_t* dst = is_v ? S.v[st][0] : S.k[st][0];  // half a at + a * kKvHalf
         if (gather) {
-          // slot-granular: 4 listed slots per lane, K and V rows of both halves
-          // of d; rows up to the next multiple of 16 repeat the last listed
-          // slot so that every row a P.V step reads holds finite data
           const int rows = ((te - ts) + 15) & ~15;
-          if (lane == 0) mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(rows) * 128u * 4u);
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(rows) * 128u * 2u);
           __syncwarp();
-          if (4 * lane < rows) {
-            const int off = 4 * lane * 128;
 #pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              tma_gather4(S.k[st][a] + off, &kgmap, 64 * a, y[0], y[1], y[2], y[3],
-                          &S.kv_full[st], pol);
-              tma_gather4(S.v[st][a] + off, &vgmap, 64 * a, y[0], y[1], y[2], y[3],
-                          &S.kv_full[st], pol);
-            }
+          for (int i = 0; i < GOPS; ++i) {
+            const int o = lane + 32 * i, a = o & 1, r0 = 4 * (o >> 1);
+            if (r0 < rows)
+              tma_gather4(dst + a * kKvHalf + r0 * 128, map, 64 * a, y[i][0], y[i][1], y[i][2],
+                          y[i][3], &full[st], pol);
           }
         } else {
-          // one page (P slots: one box per half of d, K and V) per lane
           const int p0 = ts / P, p1 = (te - 1) / P;
-          if (lane == 0)
-            mbar_arrive_expect_tx(&S.kv_full[st], uint32_t(p1 - p0 + 1) * P * 128u * 4u);
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(p1 - p0 + 1) * P * 128u * 2u);
           __syncwarp();
-          if (lane <= p1 - p0) {
-            const int off = ((p0 + lane) * P - ts) * 128;
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              tma_2d(S.k[st][a] + off, &kmap, 64 * a, y[0], &S.kv_full[st], pol);
-              tma_2d(S.v[st][a] + off, &vmap, 64 * a, y[0], &S.kv_full[st], pol);
-            }
-          }
+          const int pg = lane >> 1, a = lane & 1;
+          if (pg <= p1 - p0)
+            tma_2d(dst + a * kKvHalf + ((p0 + pg) * P - ts) * 128, map, 64 * a, y[0][0], &full[st],
+                   pol);
         }
         if (j + 1 < T) coords(j + 1);
       }
-      // The last tile's V rows between its last visible slot and the end of
-      // that 16-slot MMA step hold whatever the page held past kv_len: once
-      // the tile has landed they are zeroed here, before any issuer's last
-      // P.V (which waits on tail_zero).  Gather mode loads finite rows there.
-      const int tl = kb + (T - 1) * BN, vl = min(BN, ke - tl);
-      if (!gather && (vl & 15) && !bad) {
-        const int stl = (T - 1) % NS;
-        if (mbar_wait(&S.kv_full[stl], ((T - 1) / NS) & 1)) {
-          const int nr = ((vl + 15) & ~15) - vl;
-          for (int i = lane; i < nr * 16; i += 32) {
-            const int h = i / (nr * 8), rem = i % (nr * 8);
-            *reinterpret_cast<uint4*>(S.v[stl][h] + (vl + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+      if (is_v) {
+        // The last tile's V rows between its last visible slot and the end of
+        // that 16-slot MMA step hold whatever the page held past kv_len: once
+        // the tile has landed they are zeroed here, before any issuer's last
+        // P.V (which waits on tail_zero).  Gather mode loads finite rows there.
+        const int tl = kb + (T - 1) * BN, vl = min(BN, ke - tl);
+        if (!gather && (vl & 15) && !bad) {
+          const int stl = (T - 1) % NS;
+          if (mbar_wait(&S.v_full[stl], ((T - 1) / NS) & 1)) {
+            const int nr = ((vl + 15) & ~15) - vl;
+            for (int i = lane; i < nr * 16; i += 32) {
+              const int h = i / (nr * 8), rem = i % (nr * 8);
+              *reinterpret_cast<uint4*>(S.v[stl][h] + (vl + rem / 8) * 128 + (rem % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          } else {
+            bad = true;
           }
-          fence_proxy_async_smem();
-        } else {
-          bad = true;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.tail_zero);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tail_zero);
     }
   } else if (warp < Cfg<NT>::kSoftmaxWarp0) {
     // ---------------- MMA issuers: one warp per query tile ---------------------
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     // shared tensor pipe.  Shared-memory descriptors are built once and
     // advanced by constant increments (address field in 16-byte units).
     if (lane == 0 && T > 0) {
-      const int t = warp - 1;
+      const int t = warp - Cfg<NT>::kIssuer0;
       constexpr uint32_t ID_S = idesc(128, BN, false);
       constexpr uint32_t ID_O = idesc(128, 128, true);
       const uint64_t dq = sdesc(S.q[t][0], 16, 1024);              // + (kQHalf >> 4) per half
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       // S_t(j) = Q_t K_j^T into score buffer j & 1
       auto issue_s = [&](int j) -> bool {
         const int st = j % NS;
-        if (!mbar_wait(&S.kv_full[st], (j / NS) & 1)) return false;
+        if (!mbar_wait(&S.k_full[st], (j / NS) & 1)) return false;
         fence_after();
         const uint32_t d = tmem + s_col<BN>(t, j & 1);
         const uint64_t bk = dk + uint64_t(st) * (2 * kKvHalf >> 4);
@@ -441,9 +446,10 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       // O_t += P_t(j) V_j once the softmax group has stored P_t(j)
       auto issue_pv = [&](int j) -> bool {
         if (!mbar_wait(&S.p_full[t][j & 1], (j >> 1) & 1)) return false;
+        const int st = j % NS;
+        if (!mbar_wait(&S.v_full[st], (j / NS) & 1)) return false;
         if (j == T - 1 && !mbar_wait(&S.tail_zero, 0)) return false;
         fence_after();
-        const int st = j % NS;
         const int valid = min(BN, ke - (kb + j * BN));
         const int ksteps = (valid + 15) >> 4;
         const uint64_t bv = dv + uint64_t(st) * (2 * kKvHalf >> 4);
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   if (bad) set_status(status, PIE_STATUS_TIMEOUT);
   fence_before();
   __syncthreads();
-  if (warp == 1 && T > 0) {
+  if (warp == Cfg<NT>::kIssuer0 && T > 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(Cfg<NT>::kTmemCols)

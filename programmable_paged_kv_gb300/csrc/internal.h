@@ -85,6 +85,9 @@ struct DevMeta {
   float2* part_ml;                  // [num_part_slots] (max, sum), log2 domain
   const MaskBlock* mblocks;         // [num_mblocks] (masked passes with tensor-core lanes)
   int32_t* list;                    // compacted visible-slot lists (scratch)
+  int32_t* lrow;                    // page * Hkv * P + slot % P of each listed slot: its
+                                    //   row in the pools viewed as [rows][d] is this
+                                    //   plus kv_head * P (scratch)
   uint32_t* cmask;                  // rows' masks over the lists (scratch)
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
 };

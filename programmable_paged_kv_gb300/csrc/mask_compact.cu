@@ -11,10 +11,11 @@
 //   2. the compacted list of the slots set in the union, ascending, and its
 //      length;
 //   3. each row's mask re-expressed over that list (bit i of a row's word
-//      i/32 = the row sees list[i]).
-// The tensor-core kernel then walks 128-entry tiles of the list, gathering
-// the K/V rows of those slots, and tests visibility with the re-expressed
-// words exactly as it tests plain mask words.  The union words are kept in
+//      i/32 = the row sees list[i]), and the pool row of every listed slot
+//      (its page looked up once here, not by every kv head's item).
+// The tensor-core kernel then walks tiles of the list, gathering the K/V
+// rows of those slots, and tests visibility with the re-expressed words
+// exactly as it tests plain mask words.  The union words are kept in
 // the first row of the block's re-expressed mask area until step 3
 // overwrites it.
 
@@ -94,9 +95,10 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
 
 // 3. grid (ceil(max_nw / 8), num_blocks), 256 threads: warp -> one word of
 // list positions; for every row of the block, ballot the row's bit at each of
-// the 32 listed slots.
+// the 32 listed slots.  Each thread also writes its listed slot's pool row.
 __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
-                                                         const uint32_t* __restrict__ mask) {
+                                                         const uint32_t* __restrict__ mask,
+                                                         int Hkv, int P) {
   const int b = blockIdx.y;
   const MaskBlock B = m.mblocks[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -105,6 +107,8 @@ __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
   if (cw >= B.nw || cw * 32 >= U) return;
   const int i = cw * 32 + lane;
   const int slot = i < U ? m.list[B.list_off + i] : -1;
+  if (slot >= 0)
+    m.lrow[B.list_off + i] = m.page_ids[m.page_indptr[B.lane] + slot / P] * Hkv * P + slot % P;
   // eight rows at a time so that their mask-word loads are in flight together
   for (int r = B.r0; r < B.r1; r += 8) {
     uint32_t w[8];
@@ -129,7 +133,8 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
   mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb), 256, 0, s>>>(p.dev, mask_words);
+  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb), 256, 0, s>>>(p.dev, mask_words, p.desc.num_kv_heads,
+                                                           p.desc.page_size);
   return cudaGetLastError();
 }
 

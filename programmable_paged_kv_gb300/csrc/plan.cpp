@@ -270,8 +270,10 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
     for (int r = r0; r < r1; ++r) mx = std::max(mx, M.slots[r]);
     return std::min(kv, mx + 1);
   };
-  const bool tc_ok =
-      g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128 && kTcTileQueries % G == 0;
+  // (the tensor-core kernel addresses pool rows with 32-bit TMA coordinates)
+  const bool tc_ok = g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128 &&
+                     kTcTileQueries % G == 0 &&
+                     static_cast<int64_t>(M.num_pool_pages) * Hkv * D.page_size <= INT32_MAX;
   auto lane_tc = [&](int l) {
     return tc_ok && (M.row_indptr[l + 1] - M.row_indptr[l]) * G >= kTcMinQueries;
   };
@@ -395,7 +397,7 @@ struct Layout {
       row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks,
       row_block;
   size_t copy_bytes;  // everything above
-  size_t part_o, part_ml, list, cmask, list_len;
+  size_t part_o, part_ml, list, lrow, cmask, list_len;
   size_t total;
 };
 
@@ -432,6 +434,7 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.part_o = take(sizeof(float) * static_cast<size_t>(H.num_part_slots) * D.head_dim);
   Y.part_ml = take(sizeof(float2) * static_cast<size_t>(H.num_part_slots));
   Y.list = take(sizeof(int32_t) * static_cast<size_t>(H.list_total));
+  Y.lrow = take(sizeof(int32_t) * static_cast<size_t>(H.list_total));
   Y.cmask = take(sizeof(uint32_t) * static_cast<size_t>(H.cmask_total));
   Y.list_len = take(sizeof(int32_t) * H.mblocks.size());
   Y.total = o;
@@ -552,6 +555,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.part_ml = reinterpret_cast<float2*>(w + Y.part_ml);
   dm.mblocks = reinterpret_cast<const MaskBlock*>(w + Y.mblocks);
   dm.list = reinterpret_cast<int32_t*>(w + Y.list);
+  dm.lrow = reinterpret_cast<int32_t*>(w + Y.lrow);
   dm.cmask = reinterpret_cast<uint32_t*>(w + Y.cmask);
   dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
   p->staging = blk;
