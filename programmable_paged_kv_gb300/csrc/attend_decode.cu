@@ -44,13 +44,19 @@ struct DecCfg {
   static constexpr int THREADS = (WARPS + 1) * 32;
   static constexpr int ROW_BYTES = D * sizeof(T);
   static constexpr int STAGE_BYTES = 2 * kStageSlots * ROW_BYTES;  // K + V
-  static constexpr int STAGES = (98304 / STAGE_BYTES) < 2 ? 2
-                                : (98304 / STAGE_BYTES) > 4 ? 4 : (98304 / STAGE_BYTES);
+  // a 64 KB ring (2 to 4 stages): HBM latency needs far less in flight per
+  // SM than three CTAs' rings, and three resident CTAs (15 warps) hide the
+  // compute warps' latencies better than deeper rings
+  static constexpr int STAGES = (65536 / STAGE_BYTES) < 2 ? 2
+                                : (65536 / STAGE_BYTES) > 4 ? 4 : (65536 / STAGE_BYTES);
   static constexpr int PBUF_FLOATS = WARPS * kWarpSlots * NQ;
   static constexpr int ABUF_FLOATS = WARPS * NQ;
   static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES +
                                  sizeof(float) * (PBUF_FLOATS + ABUF_FLOATS) +
                                  sizeof(uint64_t) * 2 * STAGES;
+  // resident CTAs per SM the registers are capped for (NQ = 8 keeps its
+  // registers; shared memory decides the rest)
+  static constexpr int MIN_BLOCKS = NQ >= 8 ? 1 : (SMEM <= 70000 ? 3 : (SMEM <= 110000 ? 2 : 1));
   static_assert(E == NQ / 2, "reduction layout assumes E = NQ / 2");
   static_assert(kWarpSlots % RPS == 0, "unit must hold whole steps");
   static_assert(size_t(WARPS) * NQ * (D + 2) * 4 <= size_t(STAGES) * STAGE_BYTES,
@@ -108,8 +114,29 @@ __device__ __forceinline__ void load_dpl(const T* p, float* f) {
   }
 }
 
+// NQ probabilities of one slot from the per-warp buffer (16-byte aligned for
+// NQ >= 4, 8-byte for NQ = 2) as vector loads.
+template <int NQ>
+__device__ __forceinline__ void load_probs(const float* p, float* f) {
+  if constexpr (NQ == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    f[0] = v.x;
+    f[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NQ; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + i);
+      f[i] = v.x;
+      f[i + 1] = v.y;
+      f[i + 2] = v.z;
+      f[i + 3] = v.w;
+    }
+  }
+}
+
 template <typename T, int D, int NQ>
-__global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kernel(
+__global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::MIN_BLOCKS)
+    attend_decode_kernel(
     DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const T* __restrict__ q_rot,
     const T* __restrict__ k_pool, const T* __restrict__ v_pool,
     const uint32_t* __restrict__ mask_words, uint32_t* status) {
@@ -138,9 +165,11 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
 
   if (warp == C::WARPS) {
     // ---------------- producer warp: TMA bulk copies of K/V pages ----------
-    // Lane i copies page (stage start / P + i) of every stage; the page ids
-    // of the next stage are fetched while this one is issued, so no copy
-    // waits on a dependent global load.
+    // Lanes 2i and 2i + 1 copy the K and the V block of page (stage start /
+    // P + i) of every stage (a warp's copies issue one after another, so
+    // each comes from its own lane); the page ids of the next stage are
+    // fetched while this one is issued, so no copy waits on a dependent
+    // global load.
     const uint64_t pol = policy_evict_first();
     const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
     const int64_t head_stride = int64_t(P) * D;  // elements per (page, kv head) block
@@ -148,7 +177,7 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
     auto page_of = [&](int s) -> int64_t {
       const int sb = kb + s * kStageSlots;
       const int p0 = sb / P, p1 = (min(sb + kStageSlots, ke) - 1) / P;
-      return lane <= p1 - p0 ? int64_t(pages[p0 + lane]) : 0;
+      return (lane >> 1) <= p1 - p0 ? int64_t(pages[p0 + (lane >> 1)]) : 0;
     };
     int64_t pid = nstages > 0 ? page_of(0) : 0;
     for (int s = 0; s < nstages; ++s) {
@@ -162,13 +191,12 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
       const int p0 = sb / P, p1 = (se - 1) / P;
       if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * blk * uint32_t(p1 - p0 + 1));
       __syncwarp();
-      if (lane <= p1 - p0) {
-        T* kdst = ring + size_t(st) * 2 * kStageSlots * D;
-        T* vdst = kdst + kStageSlots * D;
+      if ((lane >> 1) <= p1 - p0) {
+        const bool is_v = lane & 1;
+        T* dst = ring + size_t(st) * 2 * kStageSlots * D + (is_v ? kStageSlots * D : 0);
         const int64_t src = (pid * Hkv + it.kv_head) * head_stride;
-        const int off = ((p0 + lane) * P - sb) * D;
-        bulk_g2s_hint(kdst + off, k_pool + src, blk, &full[st], pol);
-        bulk_g2s_hint(vdst + off, v_pool + src, blk, &full[st], pol);
+        const int off = ((p0 + (lane >> 1)) * P - sb) * D;
+        bulk_g2s_hint(dst + off, (is_v ? v_pool : k_pool) + src, blk, &full[st], pol);
       }
       if (s + 1 < nstages) pid = page_of(s + 1);
     }
@@ -237,12 +265,14 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
       for (int t = 0; t < C::STEPS; ++t) {
         float kf[C::EPL];
         unpack16<T>(*reinterpret_cast<const uint4*>(Ks + (t * C::RPS + rg) * D + j * C::EPL), kf);
+        // pairs of d per packed FMA, the two halves added at the end
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
-          float a = 0.f;
+          float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int e = 0; e < C::EPL; ++e) a = fmaf(qr[qq][e], kf[e], a);
-          part[t * NQ + qq] = a;
+          for (int e = 0; e < C::EPL; e += 2)
+            ffma2(a0, a1, qr[qq][e], qr[qq][e + 1], kf[e], kf[e + 1], a0, a1);
+          part[t * NQ + qq] = a0 + a1;
         }
       }
       TReduce<C::NV, C::LPR / 2>::run(part, j);
@@ -280,12 +310,14 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS) attend_decode_kerne
         float vf[C::DPL];
         load_dpl<T, C::DPL>(Vs + sl * D + lane * C::DPL, vf);
         float pq[NQ];
-#pragma unroll
-        for (int qq = 0; qq < NQ; ++qq) pq[qq] = my_p[sl * NQ + qq];
+        load_probs<NQ>(my_p + sl * NQ, pq);
+        // pairs of output elements per packed FMA
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
-          for (int c = 0; c < C::DPL; ++c) acc[qq][c] = fmaf(pq[qq], vf[c], acc[qq][c]);
+          for (int c = 0; c < C::DPL; c += 2)
+            ffma2(acc[qq][c], acc[qq][c + 1], pq[qq], pq[qq], vf[c], vf[c + 1], acc[qq][c],
+                  acc[qq][c + 1]);
       }
       __syncwarp();
     }
