@@ -109,6 +109,7 @@ struct pie_fwd_plan {
   int32_t tc_nt;             // query tiles per tensor-core item (1 or 2)
   int32_t num_mblocks;       // masked row blocks (0 unless masked tensor-core lanes)
   int32_t mblock_max_nw;     // largest nw over the masked row blocks
+  int32_t mblock_max_rows;   // most rows in a masked row block
   int64_t num_part_slots;
   pie::DevMeta dev;
   pie::PinnedBlock* staging;

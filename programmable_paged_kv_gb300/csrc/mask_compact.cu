@@ -33,8 +33,17 @@ __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
   const int w = blockIdx.x * 32 + lane;
   if (blockIdx.x * 32 >= B.nw) return;
   uint32_t acc = 0;
-  if (w < B.nw)
-    for (int r = B.r0 + warp; r < B.r1; r += 8) acc |= mask[m.mask_word_indptr[r] + w];
+  if (w < B.nw) {
+    // eight of the warp's rows per step, their loads in flight together
+    for (int r = B.r0 + warp; r < B.r1; r += 64) {
+      uint32_t x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        x[k] = r + 8 * k < B.r1 ? mask[m.mask_word_indptr[r + 8 * k] + w] : 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc |= x[k];
+    }
+  }
   part[warp][lane] = acc;
   __syncthreads();
   if (warp == 0 && w < B.nw) {
@@ -80,12 +89,17 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
       if (lane == 31) chunk_total = ti;
     }
     __syncthreads();
-    int pos = running + warp_tot[warp] + incl - c;
+    // the warp writes its 32 words' entries one word at a time: lane i
+    // stores bit i of the word at its rank, so every store is coalesced
+    const int pos = running + warp_tot[warp] + incl - c;
     int32_t* list = m.list + B.list_off;
-    while (u) {
-      const int bit = __ffs(u) - 1;
-      list[pos++] = w * 32 + bit;
-      u &= u - 1u;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t uk = __shfl_sync(0xffffffffu, u, k);
+      if (uk == 0u) continue;  // uniform across the warp
+      const int pk = __shfl_sync(0xffffffffu, pos, k);
+      const int wk = __shfl_sync(0xffffffffu, w, k);
+      if ((uk >> lane) & 1u) list[pk + __popc(uk & below)] = wk * 32 + lane;
     }
     running += chunk_total;
     __syncthreads();
@@ -93,9 +107,11 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
   if (threadIdx.x == 0) m.list_len[b] = running;
 }
 
-// 3. grid (ceil(max_nw / 8), num_blocks), 256 threads: warp -> one word of
-// list positions; for every row of the block, ballot the row's bit at each of
-// the 32 listed slots.  Each thread also writes its listed slot's pool row.
+// 3. grid (ceil(max_nw / 8), num_blocks, row groups), 256 threads: warp ->
+// one word of list positions and 16 rows of the block; for each row, ballot
+// the row's bit at each of the 32 listed slots (all 16 rows' loads in flight
+// together).  The first row group's threads also write their listed slots'
+// pool rows.
 __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
                                                          const uint32_t* __restrict__ mask,
                                                          int Hkv, int P) {
@@ -106,20 +122,19 @@ __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
   const int U = m.list_len[b];
   if (cw >= B.nw || cw * 32 >= U) return;
   const int i = cw * 32 + lane;
+  const int r0 = B.r0 + 16 * blockIdx.z;
+  if (r0 >= B.r1) return;
   const int slot = i < U ? m.list[B.list_off + i] : -1;
-  if (slot >= 0)
+  if (slot >= 0 && blockIdx.z == 0)
     m.lrow[B.list_off + i] = m.page_ids[m.page_indptr[B.lane] + slot / P] * Hkv * P + slot % P;
-  // eight rows at a time so that their mask-word loads are in flight together
-  for (int r = B.r0; r < B.r1; r += 8) {
-    uint32_t w[8];
+  uint32_t w[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      w[k] = (slot >= 0 && r + k < B.r1) ? mask[m.mask_word_indptr[r + k] + (slot >> 5)] : 0u;
+  for (int k = 0; k < 16; ++k)
+    w[k] = (slot >= 0 && r0 + k < B.r1) ? mask[m.mask_word_indptr[r0 + k] + (slot >> 5)] : 0u;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, ((w[k] >> (slot & 31)) & 1u) != 0);
-      if (lane == 0 && r + k < B.r1) m.cmask[B.cmask_off + int64_t(r + k - B.r0) * B.nw + cw] = bal;
-    }
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, ((w[k] >> (slot & 31)) & 1u) != 0);
+    if (lane == 0 && r0 + k < B.r1) m.cmask[B.cmask_off + int64_t(r0 + k - B.r0) * B.nw + cw] = bal;
   }
 }
 
@@ -133,8 +148,9 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
   mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb), 256, 0, s>>>(p.dev, mask_words, p.desc.num_kv_heads,
-                                                           p.desc.page_size);
+  const int row_groups = (p.mblock_max_rows + 15) / 16;
+  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb, row_groups), 256, 0, s>>>(
+      p.dev, mask_words, p.desc.num_kv_heads, p.desc.page_size);
   return cudaGetLastError();
 }
 

@@ -97,7 +97,7 @@ struct HostPlan {
   std::vector<int32_t> ro_indptr, ro_idx;
   std::vector<MaskBlock> mblocks;
   int64_t list_total = 0, cmask_total = 0;
-  int mblock_max_nw = 0;
+  int mblock_max_nw = 0, mblock_max_rows = 0;
   bool has_mask = false, any_channel = false;
   std::vector<int32_t> row_lane, readout;
   std::vector<float> rope_freq;
@@ -315,7 +315,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   for (int l = 0; l < L; ++l) any_tc = any_tc || lane_tc(l);
   std::vector<int32_t> block_of_row(H.has_mask && any_tc ? N : 0, -1);
   H.list_total = H.cmask_total = 0;
-  H.mblock_max_nw = 0;
+  H.mblock_max_nw = H.mblock_max_rows = 0;
   if (!block_of_row.empty()) {
     for (int l = 0; l < L; ++l) {
       if (!lane_tc(l)) continue;
@@ -329,6 +329,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
         H.list_total += M.kv_len[l];
         H.cmask_total += static_cast<int64_t>(b1 - b0) * nw;
         H.mblock_max_nw = std::max(H.mblock_max_nw, nw);
+        H.mblock_max_rows = std::max(H.mblock_max_rows, b1 - b0);
       }
     }
     if (H.list_total > INT32_MAX || H.cmask_total > INT32_MAX)
@@ -530,6 +531,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->tc_nt = H.tc_nt;
   p->num_mblocks = static_cast<int32_t>(H.mblocks.size());
   p->mblock_max_nw = H.mblock_max_nw;
+  p->mblock_max_rows = H.mblock_max_rows;
   p->num_part_slots = H.num_part_slots;
   char* w = static_cast<char*>(dev_workspace);
   DevMeta& dm = p->dev;
