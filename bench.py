@@ -14,8 +14,11 @@ Reported (one JSON line on rank 0):
                resident in HBM, CUDA events around exactly K steps;
   e2e          the same metric with q/k/v copied from pinned host memory and
                the readout copied back to the host inside every step;
-  roofline     achieved HBM GB/s of the attention call (algorithmic bytes /
-               measured duration) against the measured copy bandwidth;
+  roofline     achieved HBM GB/s of the split-KV attention kernel
+               (algorithmic bytes / its duration, from CUDA events that the
+               library records on the launch stream right around it) against
+               the measured copy bandwidth; the whole attend call (kernel +
+               combine) is reported beside it;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 `--impl reference` times the CPU oracle itself as the reference arm.
 """
@@ -271,7 +274,8 @@ def run_reference(args, ws, rank):
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, ws, rank, local, pg):
     import torch
-    from programmable_paged_kv_gb300 import ForwardPlan, build, make_desc, make_meta, runner
+    from programmable_paged_kv_gb300 import (ForwardPlan, build, make_desc, make_meta, runner,
+                                             set_timing_events)
     from programmable_paged_kv_gb300.abi import load
     torch.cuda.set_device(local)
     build()
@@ -297,21 +301,32 @@ def run_ours(args, ws, rank, local, pg):
     q_rot = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
     out = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((L, Hq), dtype=torch.float32, device=dev)
-    metas = [make_meta(pass_meta(t), NP) for t in range(total_steps)]
+    # metadata and accounting of every step, prepared before any timed region
+    passes = [pass_meta(t) for t in range(total_steps)]
+    metas = [make_meta(p, NP) for p in passes]
+    acct = [(attended_tokens(p), step_alg_bytes(p, desc), attend_alg_bytes(p, desc))
+            for p in passes]
     from programmable_paged_kv_gb300 import workspace_bytes
     ws_bytes = max(workspace_bytes(cdesc, metas[t]) for t in (0, total_steps - 1))
     workspace = torch.empty(ws_bytes + 4096, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
+    # the attention kernel alone (recorded by the library around its launch)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
     live = []
 
-    def step(t, q, k, v, timed_ev=None):
+    def step(t, q, k, v, timed_ev=None, kernel_ev=None):
         plan = ForwardPlan(cdesc, metas[t], workspace=workspace)
         plan.append_kv(q, k, v, q_rot, k_pool, v_pool, frozen, status)
         if timed_ev is not None:
             timed_ev[0].record(stream)
+        if kernel_ev is not None:
+            set_timing_events(*kernel_ev)
         plan.attend(q_rot, k_pool, v_pool, None, out, lse, None, None, status)
+        if kernel_ev is not None:
+            set_timing_events()
         if timed_ev is not None:
             timed_ev[1].record(stream)
         plan.fold(frozen, None, status)
@@ -336,11 +351,10 @@ def run_ours(args, ws, rank, local, pg):
     bytes_attend = 0
     t_start.record(stream)
     for i in range(K):
-        p = pass_meta(t)
-        tokens += attended_tokens(p)
-        bytes_step += step_alg_bytes(p, desc)
-        bytes_attend += attend_alg_bytes(p, desc)
-        step(t, q_d[t % NB], k_d[t % NB], v_d[t % NB], ev[i])
+        tokens += acct[t][0]
+        bytes_step += acct[t][1]
+        bytes_attend += acct[t][2]
+        step(t, q_d[t % NB], k_d[t % NB], v_d[t % NB], ev[i], kev[i])
         t += 1
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -348,6 +362,7 @@ def run_ours(args, ws, rank, local, pg):
     barrier(pg)
     el_ms = t_start.elapsed_time(t_end)
     attend_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
     el_max = max_over_ranks(pg, el_ms)
     tokens_all = sum_over_ranks(pg, tokens)
     value = tokens_all / (el_max / 1e3)
@@ -382,7 +397,7 @@ def run_ours(args, ws, rank, local, pg):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        e_tok += attended_tokens(pass_meta(t))
+        e_tok += acct[t][0]
         e2e_step(t)
         t += 1
     e1.record(stream)
@@ -399,7 +414,8 @@ def run_ours(args, ws, rank, local, pg):
         return
     hbm, peak_kind = peaks()
     att_s = sum(attend_ms) / len(attend_ms) / 1e3
-    achieved = (bytes_attend / K) / att_s / 1e9
+    ker_s = sum(kernel_ms) / len(kernel_ms) / 1e3
+    achieved = (bytes_attend / K) / ker_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": Wm,
         "ms_per_step": el_max / K, "higher_is_better": True, "scaling": "weak",
@@ -412,9 +428,12 @@ def run_ours(args, ws, rank, local, pg):
         "gpu_launches": 4 * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": profiled_traffic(),
-                     "kernel": "pie_fwd_attend (split-KV attention + combine)",
+                     "kernel": "attend_decode_kernel (split-KV attention; events recorded "
+                               "by the library around its launch)",
                      "peak_kind": peak_kind, "alg_bytes_per_launch": bytes_attend / K,
-                     "launch_ms": att_s * 1e3,
+                     "launch_ms": ker_s * 1e3,
+                     "attend_call_ms": att_s * 1e3,
+                     "attend_call_frac": (bytes_attend / K) / att_s / 1e9 / hbm,
                      "step_alg_gbs": (bytes_step / K) / (el_max / K / 1e3) / 1e9},
         "e2e": {"value": e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -488,7 +507,8 @@ def run_workload(args, local):
     """Time one pass of another configuration (first pass of its scenario);
     frozen lengths are restored before every step so each step is identical."""
     import torch
-    from programmable_paged_kv_gb300 import ForwardPlan, build, make_desc, make_meta, runner
+    from programmable_paged_kv_gb300 import (ForwardPlan, build, make_desc, make_meta, runner,
+                                             set_timing_events)
     torch.cuda.set_device(local)
     build()
     sc = WORKLOADS[args.workload](args.seed)
@@ -520,15 +540,19 @@ def run_workload(args, local):
     K, Wm = args.steps, args.warmup
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
 
-    def step(e=None):
+    def step(e=None, ke=None):
         frozen.copy_(frozen0, non_blocking=True)
         plan = ForwardPlan(desc, meta, workspace=ws)
         plan.append_kv(q, k, v, q_rot, pools.k, pools.v, frozen, status)
         if e is not None:
             e[0].record(stream)
+            set_timing_events(*ke)
         plan.attend(q_rot, pools.k, pools.v, mw, out, lse, None, None, status)
         if e is not None:
+            set_timing_events()
             e[1].record(stream)
         plan.fold(frozen, chan, status)
         live.append(plan)
@@ -545,13 +569,15 @@ def run_workload(args, local):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(K):
-        step(ev[i])
+        step(ev[i], kev[i])
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     el = t0.elapsed_time(t1) / 1e3
     att = sorted(a.elapsed_time(b) for a, b in ev)
     att_med = att[len(att) // 2] / 1e3
+    ker = sorted(a.elapsed_time(b) for a, b in kev)
+    ker_med = ker[len(ker) // 2] / 1e3
     tok, byts, flops = pass_accounting(p, d)
     hbm, kind = peaks()
     try:
@@ -565,7 +591,11 @@ def run_workload(args, local):
             "attend_alg_bytes": byts, "attend_alg_flops": flops,
             "attend_hbm_gbs": byts / att_med / 1e9, "attend_hbm_frac": byts / att_med / 1e9 / hbm,
             "attend_tflops": flops / att_med / 1e12, "attend_tensor_frac": flops / att_med / 1e12 / tf,
-            "attend_roofline_frac": t_roof / att_med, "status": int(status.item()),
+            "attend_roofline_frac": t_roof / att_med,
+            "kernel_ms_median": ker_med * 1e3,
+            "kernel_hbm_frac": byts / ker_med / 1e9 / hbm,
+            "kernel_tensor_frac": flops / ker_med / 1e12 / tf,
+            "status": int(status.item()),
             "peaks": {"hbm_gbs": hbm, "bf16_tflops": tf, "kind": kind}}
     if clk:
         line["clocks"] = clk

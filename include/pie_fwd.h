@@ -188,6 +188,16 @@ void pie_fwd_plan_destroy(pie_fwd_plan_t* plan);
 /* Message for the calling thread's most recent error ("" if none). */
 const char* pie_fwd_last_error(void);
 
+/* Measurement hook (no counterpart on the Pie pages: it only lets a caller
+ * time the attention kernels apart from the rest of a call).  After
+ * pie_fwd_set_timing_events(start, stop) with two timing-enabled cudaEvent_t
+ * handles, every pie_fwd_attend call made by the calling thread records
+ * `start` on its stream right before its attention kernels (split-KV and/or
+ * tensor-core) and `stop` right after them; the mask pre-pass and the
+ * combine step fall outside.  The events stay caller-owned; (NULL, NULL)
+ * turns the hook off.  Returns PIE_EINVAL when exactly one is NULL. */
+int pie_fwd_set_timing_events(void* start_event, void* stop_event);
+
 /* ABI version of this header (major * 100 + minor). */
 int pie_fwd_abi_version(void);
 

@@ -20,6 +20,7 @@ from .abi import (PIE_BF16, PIE_F32, PIE_FOLD_ALL, PIE_FOLD_CHANNEL, PIE_FOLD_CO
                   PIE_STATUS_FROZEN_WRITE, PIE_STATUS_TIMEOUT, PieError)
 
 __all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes", "build",
+           "set_timing_events",
            "PIE_F32", "PIE_BF16", "PIE_FOLD_NONE", "PIE_FOLD_ALL", "PIE_FOLD_COUNT",
            "PIE_FOLD_CHANNEL", "PIE_STATUS_FROZEN_WRITE", "PIE_STATUS_FOLD_CLAMP",
            "PIE_STATUS_FOLD_GAP", "PIE_STATUS_TIMEOUT"]
@@ -75,6 +76,18 @@ def workspace_bytes(desc: abi.pie_fwd_desc, meta: _HostMeta) -> int:
     abi.check(abi.load().pie_fwd_workspace_bytes(C.byref(desc), C.byref(meta.c), C.byref(n)),
               "pie_fwd_workspace_bytes")
     return int(n.value)
+
+
+def set_timing_events(start=None, stop=None) -> None:
+    """Have later attend calls on this thread record two timing-enabled
+    torch.cuda.Event objects right around their attention kernels
+    (pie_fwd_set_timing_events); no arguments turns it off."""
+    for e in (start, stop):
+        if e is not None and not e.cuda_event:
+            e.record()  # the CUDA event is created at its first record
+    abi.check(abi.load().pie_fwd_set_timing_events(start.cuda_event if start is not None else None,
+                                                   stop.cuda_event if stop is not None else None),
+              "pie_fwd_set_timing_events")
 
 
 def _ptr(t, what: str, required: bool = True):

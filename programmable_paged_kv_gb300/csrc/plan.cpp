@@ -170,9 +170,17 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   }
   const int64_t total_pages = M.page_indptr[L];
   if (total_pages > 0 && !M.page_ids) return fail(PIE_EINVAL, "page_ids missing");
-  for (int64_t i = 0; i < total_pages; ++i)
-    if (M.page_ids[i] < 0 || M.page_ids[i] >= M.num_pool_pages)
+  {
+    // range of the page ids (one branch-free pass the compiler vectorizes)
+    int32_t lo = 0, hi = 0;
+    if (total_pages > 0) lo = hi = M.page_ids[0];
+    for (int64_t i = 0; i < total_pages; ++i) {
+      lo = std::min(lo, M.page_ids[i]);
+      hi = std::max(hi, M.page_ids[i]);
+    }
+    if (total_pages > 0 && (lo < 0 || hi >= M.num_pool_pages))
       return fail(PIE_ERANGE, "page id outside the pool");
+  }
 
   H.L = L;
   H.N = N;
@@ -450,11 +458,28 @@ extern "C" {
 
 const char* pie_fwd_last_error(void) { return g_last_error.c_str(); }
 
-int pie_fwd_abi_version(void) { return 100; }
+int pie_fwd_abi_version(void) { return 101; }
+
+static thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+int pie_fwd_set_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(PIE_EINVAL, "timing events: give both or neither");
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return PIE_OK;
+}
+
+// One host plan per calling thread, reused so that its vectors keep their
+// capacity from one pass to the next (build_host_plan resets every field).
+static HostPlan& thread_host_plan() {
+  static thread_local HostPlan H;
+  return H;
+}
 
 int pie_fwd_workspace_bytes(const pie_fwd_desc* desc, const pie_fwd_meta* meta, size_t* bytes) {
   if (!bytes) return fail(PIE_EINVAL, "bytes is NULL");
-  HostPlan H;
+  HostPlan& H = thread_host_plan();
   int rc = build_host_plan(desc, meta, H);
   if (rc != PIE_OK) return rc;
   *bytes = make_layout(*desc, H).total;
@@ -465,7 +490,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
                  size_t ws_bytes, void* stream, pie_fwd_plan_t** out) {
   if (!out) return fail(PIE_EINVAL, "out is NULL");
   *out = nullptr;
-  HostPlan H;
+  HostPlan& H = thread_host_plan();
   int rc = build_host_plan(desc, meta, H);
   if (rc != PIE_OK) return rc;
   const pie_fwd_meta& M = *meta;
@@ -599,11 +624,14 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
     return fail(PIE_EINVAL, "attend: out_readout (or out_all) is required");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (plan->num_dec_items > 0) e = launch_attend_decode(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
-  if (e == cudaSuccess && plan->num_mblocks > 0) e = launch_mask_compact(*plan, mask_words, s);
+  if (plan->num_mblocks > 0) e = launch_mask_compact(*plan, mask_words, s);
+  if (e == cudaSuccess && g_ev_start) e = cudaEventRecord(g_ev_start, s);
+  if (e == cudaSuccess && plan->num_dec_items > 0)
+    e = launch_attend_decode(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
   if (e == cudaSuccess && plan->num_tc_items > 0)
     e = launch_attend_tc(*plan, q_rot, k_pool, v_pool, mask_words, out_readout, lse_readout,
                          out_all, lse_all, status, s);
+  if (e == cudaSuccess && g_ev_stop) e = cudaEventRecord(g_ev_stop, s);
   if (e == cudaSuccess) e = launch_combine(*plan, out_readout, lse_readout, out_all, lse_all, s);
   if (e != cudaSuccess) return fail(PIE_ECUDA, std::string("attend launch: ") + cudaGetErrorString(e));
   return PIE_OK;

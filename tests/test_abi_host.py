@@ -34,7 +34,12 @@ def test_build_can_be_called_again(lib):
 
 
 def test_abi_version(lib):
-    assert lib.pie_fwd_abi_version() == 100
+    assert lib.pie_fwd_abi_version() == 101
+
+
+def test_timing_events_need_both_or_neither(lib):
+    assert lib.pie_fwd_set_timing_events(C.c_void_p(1), None) != 0
+    assert lib.pie_fwd_set_timing_events(None, None) == 0
 
 
 def _ws(desc, p, num_pool_pages):
