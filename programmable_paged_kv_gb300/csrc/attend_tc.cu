@@ -14,8 +14,9 @@
 //            block of every page in the tile (2-D tensor maps over the pools,
 //            one 64-column box per half of d, 128-byte swizzle) into an
 //            NS-deep ring of stages, each copy from its own lane (a warp's
-//            copies issue one after another); in gather mode (masked passes)
-//            the rows of the listed slots with tile::gather4.  K and V land on
+//            copies issue one after another); in masked passes, whole pages
+//            of a page-granular slot list the same way, and the rows of a
+//            slot-granular list with tile::gather4.  K and V land on
 //            separate barriers, so scores wait for K only;
 //   warps 2..1+NT  one MMA issuer per query tile t (warp 2 also allocates the
 //            512 TMEM columns): from one thread, S_t = Q_t K^T (M=128, N=BN)
@@ -275,6 +276,10 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   }
   const int T = ke > kb ? (ke - kb + BN - 1) / BN : 0;
   const int nqv = it.nrows * G;  // valid query vectors of the item
+  // a page-granular list (whole pages, in list order) loads like the lane's
+  // own pages; a slot-granular one is gathered row by row
+  const bool page_list = gather && m.list_mode[it.block] != 0;
+  const bool row_gather = gather && !page_list;
 
   if (threadIdx.x == 0) {
     mbar_init(&S.q_full, 1);
@@ -312,12 +317,13 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     // ---------------- TMA producers: warp 0 loads K, warp 1 loads V ----------
     // A warp's TMA copies issue one after another, so every copy of a tile
     // comes from its own lane and the two tensors from two warps.
-    //   tile mode:   lane 2i + a -> page (ts / P + i) of the tile, half a of d
+    //   pages (the lane's own, or a page-granular list):
+    //                lane 2i + a -> page (ts / P + i) of the tile, half a of d
     //                (at most BN / P <= 16 pages)
-    //   gather mode: lane o (and o + 32 for 128-slot tiles) -> rows 4(o/2) ..
+    //   row gather:  lane o (and o + 32 for 128-slot tiles) -> rows 4(o/2) ..
     //                4(o/2) + 3 of the tile, half o % 2 of d, one gather4 each
-    // The copies' pool rows come from the page table (tile mode) or the pool
-    // rows of the listed slots (gather mode), fetched one tile ahead.
+    // The copies' pool rows come from the page table or the pool rows of the
+    // listed slots, fetched one tile ahead.
     const bool is_v = warp == 1;
     if (T > 0) {
       const uint64_t pol = policy_evict_first();
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
             tma_4d(S.q[t][a], &qmap, 64 * a, 0, it.kv_head, it.row0 + t * (kTcTileQueries / G),
                    &S.q_full);
       }
-      const CUtensorMap* map = gather ? (is_v ? &vgmap : &kgmap) : (is_v ? &vmap : &kmap);
+      const CUtensorMap* map = row_gather ? (is_v ? &vgmap : &kgmap) : (is_v ? &vmap : &kmap);
       uint64_t* full = is_v ? S.v_full : S.k_full;
       const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
       const int32_t* lrow = gather ? m.lrow + mb.list_off : nullptr;
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
       auto coords = [&](int jj) {
         const int ts = kb + jj * BN;
         const int te = min(ts + BN, ke);
-        if (gather) {
+        if (row_gather) {
           const int rows = ((te - ts) + 15) & ~15;
 #pragma unroll
           for (int i = 0; i < GOPS; ++i) {
@@ -354,7 +360,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
           }
         } else {
           const int p0 = ts / P, p1 = (te - 1) / P;
-          if ((lane >> 1) <= p1 - p0) y[0][0] = (pages[p0 + (lane >> 1)] * Hkv + it.kv_head) * P;
+          if ((lane >> 1) <= p1 - p0)
+            y[0][0] = page_list ? lrow[ts + (lane >> 1) * P] + hrow
+                                : (pages[p0 + (lane >> 1)] * Hkv + it.kv_head) * P;
         }
       };
       coords(0);
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         const int ts = kb + j * BN;
         const int te = min(ts + BN, ke);
         uint8_t* dst = is_v ? S.v[st][0] : S.k[st][0];  // half a at + a * kKvHalf
-        if (gather) {
+        if (row_gather) {
           const int rows = ((te - ts) + 15) & ~15;
           if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(rows) * 128u * 2u);
           __syncwarp();
@@ -393,9 +401,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
         // The last tile's V rows between its last visible slot and the end of
         // that 16-slot MMA step hold whatever the page held past kv_len: once
         // the tile has landed they are zeroed here, before any issuer's last
-        // P.V (which waits on tail_zero).  Gather mode loads finite rows there.
+        // P.V (which waits on tail_zero).  Row gathers load finite rows there.
         const int tl = kb + (T - 1) * BN, vl = min(BN, ke - tl);
-        if (!gather && (vl & 15) && !bad) {
+        if (!row_gather && (vl & 15) && !bad) {
           const int stl = (T - 1) % NS;
           if (mbar_wait(&S.v_full[stl], ((T - 1) / NS) & 1)) {
             const int nr = ((vl + 15) & ~15) - vl;

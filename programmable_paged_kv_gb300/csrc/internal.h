@@ -90,6 +90,7 @@ struct DevMeta {
                                     //   plus kv_head * P (scratch)
   uint32_t* cmask;                  // rows' masks over the lists (scratch)
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
+  int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
 };
 
 struct PinnedBlock;

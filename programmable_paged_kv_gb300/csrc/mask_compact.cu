@@ -56,19 +56,59 @@ __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
   }
 }
 
-// 2. one CTA of 1024 threads per block: prefix count of the union's set bits
-// and the slot list.
-__global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
+// Block-wide sum over the 1024 threads (every thread calls it).
+__device__ __forceinline__ int block_sum_1024(int v, int* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();  // red may still be read from a previous call
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = lane < 32 ? red[lane] : 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Pages (P-bit groups) of a union word with at least one set slot.
+__device__ __forceinline__ int pages_set(uint32_t u, int P) {
+  int n = 0;
+  for (int g = 0; g < 32; g += P) n += ((u >> g) & ((P == 32) ? 0xFFFFFFFFu : ((1u << P) - 1u))) != 0;
+  return n;
+}
+
+// 2. one CTA of 1024 threads per block: the list of the block's visible
+// slots and its length.  When the pages holding a visible slot add at most a
+// quarter to the visible slots (a window: long runs), the list is
+// page-granular -- every slot below kv_len of each such page, in page order,
+// so the tensor-core kernel can load whole pages with one box copy each;
+// otherwise (scattered slots, e.g. TOVA) it lists only the visible slots,
+// which the kernel gathers row by row.  Both are ascending.
+__global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P) {
   __shared__ int warp_tot[32];
+  __shared__ int red[32];
   __shared__ int chunk_total;
   const int b = blockIdx.x;
   const MaskBlock B = m.mblocks[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv = m.kv_len[B.lane];
+  // pass 1: visible slots and pages with a visible slot
+  int cs = 0, cp = 0;
+  for (int w = threadIdx.x; w < B.nw; w += 1024) {
+    const uint32_t u = m.cmask[B.cmask_off + w];
+    cs += __popc(u);
+    cp += pages_set(u, P);
+  }
+  const int n_slots = block_sum_1024(cs, red);
+  const int n_pages = block_sum_1024(cp, red);
+  const bool page_mode = n_slots > 0 && int64_t(n_pages) * P * 4 <= int64_t(n_slots) * 5;
+  int32_t* list = m.list + B.list_off;
+  // pass 2: exclusive prefix over words of the entries each word contributes
   int running = 0;
   for (int base = 0; base < B.nw; base += 1024) {
     const int w = base + threadIdx.x;
-    uint32_t u = w < B.nw ? m.cmask[B.cmask_off + w] : 0u;
-    const int c = __popc(u);
+    const uint32_t u = w < B.nw ? m.cmask[B.cmask_off + w] : 0u;
+    const int c = page_mode ? pages_set(u, P) : __popc(u);
     int incl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -89,22 +129,45 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m) {
       if (lane == 31) chunk_total = ti;
     }
     __syncthreads();
-    // the warp writes its 32 words' entries one word at a time: lane i
-    // stores bit i of the word at its rank, so every store is coalesced
     const int pos = running + warp_tot[warp] + incl - c;
-    int32_t* list = m.list + B.list_off;
-    const uint32_t below = (1u << lane) - 1u;
-    for (int k = 0; k < 32; ++k) {
-      const uint32_t uk = __shfl_sync(0xffffffffu, u, k);
-      if (uk == 0u) continue;  // uniform across the warp
-      const int pk = __shfl_sync(0xffffffffu, pos, k);
-      const int wk = __shfl_sync(0xffffffffu, w, k);
-      if ((uk >> lane) & 1u) list[pk + __popc(uk & below)] = wk * 32 + lane;
+    if (page_mode) {
+      // the word's pages with a visible slot: all of their slots below kv_len
+      int k = 0;
+      for (int g = 0; g < 32; g += P) {
+        const uint32_t grp = (u >> g) & ((P == 32) ? 0xFFFFFFFFu : ((1u << P) - 1u));
+        if (grp == 0u) continue;
+        const int s0 = w * 32 + g;
+        for (int off = 0; off < P && s0 + off < kv; ++off) list[(pos + k) * P + off] = s0 + off;
+        ++k;
+      }
+    } else {
+      // the warp writes its 32 words' entries one word at a time: lane i
+      // stores bit i of the word at its rank, so every store is coalesced
+      const uint32_t below = (1u << lane) - 1u;
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t uk = __shfl_sync(0xffffffffu, u, k);
+        if (uk == 0u) continue;  // uniform across the warp
+        const int pk = __shfl_sync(0xffffffffu, pos, k);
+        const int wk = __shfl_sync(0xffffffffu, w, k);
+        if ((uk >> lane) & 1u) list[pk + __popc(uk & below)] = wk * 32 + lane;
+      }
     }
     running += chunk_total;
     __syncthreads();
   }
-  if (threadIdx.x == 0) m.list_len[b] = running;
+  if (threadIdx.x == 0) {
+    // page mode: the last listed page is cut at kv_len when it is the lane's
+    // last, partly filled page (its slots at/after kv_len are never listed)
+    int len = page_mode ? running * P : running;
+    if (page_mode && (kv % P) != 0) {
+      const int last_page = (kv - 1) / P;
+      const uint32_t u = m.cmask[B.cmask_off + (last_page * P) / 32];
+      const int g = (last_page * P) % 32;
+      if (((u >> g) & ((P == 32) ? 0xFFFFFFFFu : ((1u << P) - 1u))) != 0u) len -= P - (kv % P);
+    }
+    m.list_len[b] = len;
+    m.list_mode[b] = page_mode ? 1 : 0;
+  }
 }
 
 // 3. grid (ceil(max_nw / 8), num_blocks, row groups), 256 threads: warp ->
@@ -145,7 +208,7 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
   mask_union_kernel<<<dim3((nw + 31) / 32, nb), 256, 0, s>>>(p.dev, mask_words);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev);
+  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev, p.desc.page_size);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int row_groups = (p.mblock_max_rows + 15) / 16;

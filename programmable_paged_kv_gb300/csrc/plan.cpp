@@ -406,7 +406,7 @@ struct Layout {
       row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks,
       row_block;
   size_t copy_bytes;  // everything above
-  size_t part_o, part_ml, list, lrow, cmask, list_len;
+  size_t part_o, part_ml, list, lrow, cmask, list_len, list_mode;
   size_t total;
 };
 
@@ -446,6 +446,7 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.lrow = take(sizeof(int32_t) * static_cast<size_t>(H.list_total));
   Y.cmask = take(sizeof(uint32_t) * static_cast<size_t>(H.cmask_total));
   Y.list_len = take(sizeof(int32_t) * H.mblocks.size());
+  Y.list_mode = take(sizeof(int32_t) * H.mblocks.size());
   Y.total = o;
   return Y;
 }
@@ -585,6 +586,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.lrow = reinterpret_cast<int32_t*>(w + Y.lrow);
   dm.cmask = reinterpret_cast<uint32_t*>(w + Y.cmask);
   dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
+  dm.list_mode = reinterpret_cast<int32_t*>(w + Y.list_mode);
   p->staging = blk;
   *out = p;
   return PIE_OK;

@@ -104,6 +104,29 @@ def test_shape_variants(var):
         compare_scenario(sc, gpu, orc)
 
 
+# Masked passes on the tensor-core path: window masks (the pre-pass lists
+# whole pages) and TOVA masks (it lists single slots), one and two query
+# tiles per item, every page size, the last page cut by kv_len.
+MASKED_VARIANTS = {
+    "window_one_tile_p8": (W.Desc(32, 8, 128, 8, W.BF16),
+                           dict(kind="window", lanes=2, kv=700, rows=24, window=200)),
+    "window_two_tiles_p32": (W.Desc(32, 8, 128, 32, W.BF16),
+                             dict(kind="window", lanes=2, kv=1000, rows=40, window=250)),
+    "tova_one_tile_p16": (W.Desc(32, 8, 128, 16, W.BF16),
+                          dict(kind="tova", lanes=2, kv=900, rows=24)),
+    "window_g1_two_tiles_p16": (W.Desc(8, 8, 128, 16, W.BF16),
+                                dict(kind="window", lanes=2, kv=777, rows=150, window=200)),
+}
+
+
+@pytest.mark.parametrize("var", list(MASKED_VARIANTS))
+def test_masked_list_modes(var):
+    desc, kw = MASKED_VARIANTS[var]
+    sc = W.masked_long(5, desc=desc, **kw)
+    gpu, orc = _run_both(sc)
+    compare_scenario(sc, gpu, orc)
+
+
 # ---------------------------------------------------------------- edge cases
 def _one_pass_scenario(desc, p, frozen0, pool_pages_n, fill_slots):
     """Scenario around one hand-made pass; fill_slots[l] cached slots random."""
