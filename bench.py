@@ -456,7 +456,8 @@ def pass_accounting(p, desc):
     """(attended tokens, attention algorithmic bytes, attention FLOPs) of a
     pass with default or mask visibility.  Bytes count each distinct visible
     physical KV slot once per kv head (shared prefix pages once), q_rot read,
-    readout rows written, mask words and page-table entries read."""
+    every row's output (o and lse) and the readout rows written, mask words
+    and page-table entries read."""
     b = W.ELEM_BYTES[desc.dtype]
     d, hq, hkv, P = desc.head_dim, desc.num_q_heads, desc.num_kv_heads, desc.page_size
     vis_count = 0
@@ -489,7 +490,7 @@ def pass_accounting(p, desc):
     R = p.readout.size if p.readout is not None else int((np.diff(p.row_indptr) > 0).sum())
     npages = int(sum((int(k) + P - 1) // P for k in p.kv_len))
     byts = (distinct * hkv * 2 * d * b + p.num_rows * hq * d * b + R * hq * (d * b + 4)
-            + mask_bytes + npages * 4)
+            + p.num_rows * hq * (d * b + 4) + mask_bytes + npages * 4)
     flops = 4 * d * hq * vis_count
     return vis_count, byts, flops
 
@@ -504,8 +505,9 @@ WORKLOADS = {
 
 
 def run_workload(args, local):
-    """Time one pass of another configuration (first pass of its scenario);
-    frozen lengths are restored before every step so each step is identical."""
+    """Time one pass of another configuration (first pass of its scenario):
+    every row's output and the readout rows; frozen lengths are restored
+    before every step so each step is identical."""
     import torch
     from programmable_paged_kv_gb300 import (ForwardPlan, build, make_desc, make_meta, runner,
                                              set_timing_events)
@@ -533,6 +535,10 @@ def run_workload(args, local):
     plan0.close()
     out = torch.empty((R, Hq, D), dtype=tdt, device="cuda")
     lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+    # every row's attention output (what the next layer of a model reads),
+    # besides the readout rows
+    out_all = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+    lse_all = torch.empty((N, Hq), dtype=torch.float32, device="cuda")
     mw = None if p.mask_words is None else torch.from_numpy(p.mask_words.view(np.int32)).cuda()
     chan = None if p.channel is None else torch.from_numpy(p.channel.astype(np.int32)).cuda()
     stream = torch.cuda.current_stream()
@@ -550,7 +556,7 @@ def run_workload(args, local):
         if e is not None:
             e[0].record(stream)
             set_timing_events(*ke)
-        plan.attend(q_rot, pools.k, pools.v, mw, out, lse, None, None, status)
+        plan.attend(q_rot, pools.k, pools.v, mw, out, lse, out_all, lse_all, status)
         if e is not None:
             set_timing_events()
             e[1].record(stream)

@@ -411,9 +411,9 @@ cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, con
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv, int G, int N,
-                                                      int R, int with_all, T* out_readout,
-                                                      float* lse_readout, T* out_all,
-                                                      float* lse_all) {
+                                                      int R, int with_all, int tc_bn,
+                                                      T* out_readout, float* lse_readout,
+                                                      T* out_all, float* lse_all) {
   constexpr int DPL = D / 32;
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -425,14 +425,18 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
   const CombEntry ce = m.comb[int64_t(m.row_block[row]) * Hkv + h / G];
   if (ce.nchunks < 0) return;  // written directly by the tensor-core kernel
   const int qi = (row - ce.row0) * G + h % G;
+  // a masked tensor-core block uses as many chunks as its list length gives
+  const int nch = ce.mblock < 0 ? ce.nchunks
+                                : masked_chunks((m.list_len[ce.mblock] + tc_bn - 1) / tc_bn,
+                                                ce.nchunks, *m.mask_tiles, Hkv);
   float M = -INFINITY;
-  for (int c = 0; c < ce.nchunks; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
   float o[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) o[e] = 0.f;
   float Ls = 0.f;
   if (M != -INFINITY) {
-    for (int c = 0; c < ce.nchunks; ++c) {
+    for (int c = 0; c < nch; ++c) {
       const int idx = ce.part_base + c * ce.stride + qi;
       const float2 ml = m.part_ml[idx];
       const float f = ex2(ml.x - M);
@@ -464,7 +468,8 @@ static cudaError_t launch_comb(const pie_fwd_plan_t& p, void* out_readout, float
   if (warps == 0) return cudaSuccess;
   combine_kernel<T, D><<<int((warps + 3) / 4), 128, 0, s>>>(
       p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
-      static_cast<T*>(out_readout), lse_readout, static_cast<T*>(out_all), lse_all);
+      tc_kv_tile(p.tc_nt), static_cast<T*>(out_readout), lse_readout, static_cast<T*>(out_all),
+      lse_all);
   return cudaGetLastError();
 }
 

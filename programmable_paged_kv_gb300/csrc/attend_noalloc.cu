@@ -77,7 +77,7 @@ __global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_
     const int ke = max(kb, min(ext, kb + kNoAllocChunk));
     items[i] = DecItem{l, g, l, 1, kb, ke, i * nq, 0};
   }
-  if (i < L * Hkv) comb[i] = CombEntry{i * MC * nq, MC, nq, i / Hkv};  // block l = row l
+  if (i < L * Hkv) comb[i] = CombEntry{i * MC * nq, MC, nq, i / Hkv, -1, 0, 0, 0};  // block l = row l
   if (i < L) readout[i] = i;
 }
 

@@ -59,7 +59,7 @@ constexpr int kQHalf = 128 * 128;        // 128 query rows x 128 bytes (half of 
 // tiles (2 x 128 + 128 columns), two query tiles 64-slot ones (4 x 64 + 256).
 template <int NT>
 struct Cfg {
-  static constexpr int BN = NT == 1 ? 128 : 64;     // KV slots per tile
+  static constexpr int BN = tc_kv_tile(NT);         // KV slots per tile
   static constexpr int kKvHalf = BN * 128;          // BN slot rows x 128 bytes (half of d)
   static constexpr int NS = NT == 1 ? 3 : 4;        // KV stages beside the query tiles
   static constexpr int kIssuer0 = 2;                // warps 0, 1: K and V producers
@@ -271,8 +271,12 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     mb = m.mblocks[it.block];
     const int U = m.list_len[it.block];
     const int tiles = (U + BN - 1) / BN;
-    kb = (it.chunk * tiles / it.nchunks) * BN;
-    ke = min(U, ((it.chunk + 1) * tiles / it.nchunks) * BN);
+    // the chunks this unit uses now that its list length is known; the
+    // provisioned items past them have nothing to do and write nothing
+    const int nch = masked_chunks(tiles, it.nchunks, *m.mask_tiles, Hkv);
+    if (it.chunk >= nch) return;
+    kb = (it.chunk * tiles / nch) * BN;
+    ke = min(U, ((it.chunk + 1) * tiles / nch) * BN);
   }
   const int T = ke > kb ? (ke - kb + BN - 1) / BN : 0;
   const int nqv = it.nrows * G;  // valid query vectors of the item

@@ -25,8 +25,12 @@ struct alignas(16) DecItem {
 // item serves) and kv head: row r of the block, q head h, chunk c lives at
 // part_base + c * stride + (r - row0) * G + (h % G).  nchunks < 0 marks blocks
 // whose outputs the tensor-core kernel wrote directly (nothing to combine).
+// mblock >= 0 marks a masked row block on the tensor-core path: nchunks is
+// then only the chunks provisioned, and the chunks used come from its list
+// length (masked_chunks).
 struct alignas(16) CombEntry {
   int32_t part_base, nchunks, stride, row0;
+  int32_t mblock, pad0, pad1, pad2;
 };
 
 // Work item of the tensor-core attention kernel: up to NT tiles of 128 query
@@ -60,6 +64,26 @@ constexpr int kStageSlots = 64;   // slots per pipeline stage of the decode kern
 constexpr int kWarpSlots = 16;    // slots per compute warp per stage
 constexpr int kTcTileSlots = 128; // slots per KV tile of the tensor-core kernel
 constexpr int kTcTileQueries = 128;
+constexpr int kTcTargetSms = 152;  // SMs of the part the item counts are sized for
+
+// KV slots per tile of the tensor-core kernel with nt query tiles per item
+// (two score buffers per query tile and every tile's O share 512 TMEM columns)
+constexpr int tc_kv_tile(int nt) { return nt == 1 ? 128 : 64; }
+
+// Chunks a masked tensor-core unit (row block x kv head) splits its list
+// into: its share of one wave of kTcTargetSms items, in proportion to its
+// KV tiles among all masked units' (total_tiles counts each row block's tiles
+// once; every block has Hkv units), at least 1 and at most the provisioned
+// items and its tiles.  The kernel and the combine step both use it.
+__host__ __device__ inline int masked_chunks(int tiles, int provisioned, int total_tiles, int Hkv) {
+  if (tiles <= 1) return 1;
+  const long long want =
+      static_cast<long long>(tiles) * kTcTargetSms / (static_cast<long long>(total_tiles > 0 ? total_tiles : 1) * Hkv);
+  long long n = want < 1 ? 1 : want;
+  if (n > provisioned) n = provisioned;
+  if (n > tiles) n = tiles;
+  return static_cast<int>(n);
+}
 
 // Device pointers into the caller's workspace, filled by the planner.
 struct DevMeta {
@@ -91,6 +115,7 @@ struct DevMeta {
   uint32_t* cmask;                  // rows' masks over the lists (scratch)
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
   int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
+  int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
 };
 
 struct PinnedBlock;

@@ -9,7 +9,8 @@
 // row block (the rows one tensor-core item serves) three small kernels build
 //   1. the union of the rows' mask words (bits at or past kv_len cleared);
 //   2. the compacted list of the slots set in the union, ascending, and its
-//      length;
+//      length (and the KV tiles of all blocks' lists, which set how many
+//      chunks each block's items split it into);
 //   3. each row's mask re-expressed over that list (bit i of a row's word
 //      i/32 = the row sees list[i]), and the pool row of every listed slot
 //      (its page looked up once here, not by every kv head's item).
@@ -28,6 +29,7 @@ namespace pie {
 __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
                                                          const uint32_t* __restrict__ mask) {
   __shared__ uint32_t part[8][32];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *m.mask_tiles = 0;
   const MaskBlock B = m.mblocks[blockIdx.y];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * 32 + lane;
@@ -84,7 +86,7 @@ __device__ __forceinline__ int pages_set(uint32_t u, int P) {
 // so the tensor-core kernel can load whole pages with one box copy each;
 // otherwise (scattered slots, e.g. TOVA) it lists only the visible slots,
 // which the kernel gathers row by row.  Both are ascending.
-__global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P) {
+__global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P, int BN) {
   __shared__ int warp_tot[32];
   __shared__ int red[32];
   __shared__ int chunk_total;
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P) {
     }
     m.list_len[b] = len;
     m.list_mode[b] = page_mode ? 1 : 0;
+    atomicAdd(m.mask_tiles, (len + BN - 1) / BN);  // KV tiles of all blocks' lists
   }
 }
 
@@ -208,7 +211,7 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
   mask_union_kernel<<<dim3((nw + 31) / 32, nb), 256, 0, s>>>(p.dev, mask_words);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev, p.desc.page_size);
+  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev, p.desc.page_size, tc_kv_tile(p.tc_nt));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int row_groups = (p.mblock_max_rows + 15) / 16;

@@ -138,7 +138,6 @@ static int choose_chunk(int64_t total_slots_x_heads) {
 // tensor-core kernel (bf16 only).
 static bool g_tc_enabled = true;
 constexpr int kTcMinQueries = 16;
-constexpr int kTcTargetSms = 152;  // SMs of the part the item counts are sized for
 
 static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, HostPlan& H) {
   if (!desc || !meta) return fail(PIE_EINVAL, "desc and meta are required");
@@ -366,8 +365,9 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
       }
       const bool direct = use_tc && nchunks == 1;
       for (int g = 0; g < Hkv; ++g) {
+        const int32_t mblk = (use_tc && !block_of_row.empty()) ? block_of_row[b0] : -1;
         H.comb.push_back(CombEntry{static_cast<int32_t>(part), direct ? -1 : nchunks,
-                                   use_tc ? stride * H.tc_nt : stride, b0});
+                                   use_tc ? stride * H.tc_nt : stride, b0, mblk, 0, 0, 0});
         for (int c = 0; c < nchunks; ++c) {
           const int kb = c * chunk, ke = std::min(ext, kb + chunk);
           if (use_tc) {
@@ -406,7 +406,7 @@ struct Layout {
       row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks,
       row_block;
   size_t copy_bytes;  // everything above
-  size_t part_o, part_ml, list, lrow, cmask, list_len, list_mode;
+  size_t part_o, part_ml, list, lrow, cmask, list_len, list_mode, mask_tiles;
   size_t total;
 };
 
@@ -447,6 +447,7 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.cmask = take(sizeof(uint32_t) * static_cast<size_t>(H.cmask_total));
   Y.list_len = take(sizeof(int32_t) * H.mblocks.size());
   Y.list_mode = take(sizeof(int32_t) * H.mblocks.size());
+  Y.mask_tiles = take(H.mblocks.empty() ? 0 : sizeof(int32_t));
   Y.total = o;
   return Y;
 }
@@ -587,6 +588,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.cmask = reinterpret_cast<uint32_t*>(w + Y.cmask);
   dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
   dm.list_mode = reinterpret_cast<int32_t*>(w + Y.list_mode);
+  dm.mask_tiles = reinterpret_cast<int32_t*>(w + Y.mask_tiles);
   p->staging = blk;
   *out = p;
   return PIE_OK;
