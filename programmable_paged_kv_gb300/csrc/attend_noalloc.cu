@@ -139,6 +139,7 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
   p.nq = nq;
   p.num_dec_items = static_cast<int32_t>(n_items);
   p.num_part_slots = static_cast<int64_t>(n_parts);
+  p.num_comb_merge = L * Hkv;
   p.dev.slots = slots;
   p.dev.kv_len = kv_len;
   p.dev.page_indptr = page_indptr;

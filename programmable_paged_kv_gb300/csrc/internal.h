@@ -137,6 +137,7 @@ struct pie_fwd_plan {
   int32_t mblock_max_nw;     // largest nw over the masked row blocks
   int32_t mblock_max_rows;   // most rows in a masked row block
   int64_t num_part_slots;
+  int32_t num_comb_merge;    // combine entries with chunks to merge (0: no combine launch)
   pie::DevMeta dev;
   pie::PinnedBlock* staging;
 };

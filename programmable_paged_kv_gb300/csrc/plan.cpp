@@ -106,6 +106,7 @@ struct HostPlan {
   std::vector<CombEntry> comb;
   std::vector<int32_t> row_block;
   int64_t num_part_slots = 0;
+  int32_t num_comb_merge = 0;
   int64_t total_pages = 0;
 };
 
@@ -312,6 +313,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   const int64_t tc_ch = tc_units >= tc_target ? INT32_MAX
                         : std::max<int64_t>(512, (tc_total + tc_target - 1) / tc_target);
   H.comb.clear();
+  H.num_comb_merge = 0;
   H.row_block.assign(N, 0);
   H.dec.clear();
   H.tc.clear();
@@ -368,6 +370,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
         const int32_t mblk = (use_tc && !block_of_row.empty()) ? block_of_row[b0] : -1;
         H.comb.push_back(CombEntry{static_cast<int32_t>(part), direct ? -1 : nchunks,
                                    use_tc ? stride * H.tc_nt : stride, b0, mblk, 0, 0, 0});
+        if (!direct) ++H.num_comb_merge;
         for (int c = 0; c < nchunks; ++c) {
           const int kb = c * chunk, ke = std::min(ext, kb + chunk);
           if (use_tc) {
@@ -560,6 +563,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->mblock_max_nw = H.mblock_max_nw;
   p->mblock_max_rows = H.mblock_max_rows;
   p->num_part_slots = H.num_part_slots;
+  p->num_comb_merge = H.num_comb_merge;
   char* w = static_cast<char*>(dev_workspace);
   DevMeta& dm = p->dev;
   dm.row_indptr = reinterpret_cast<const int32_t*>(w + Y.row_indptr);
@@ -636,7 +640,8 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
     e = launch_attend_tc(*plan, q_rot, k_pool, v_pool, mask_words, out_readout, lse_readout,
                          out_all, lse_all, status, s);
   if (e == cudaSuccess && g_ev_stop) e = cudaEventRecord(g_ev_stop, s);
-  if (e == cudaSuccess) e = launch_combine(*plan, out_readout, lse_readout, out_all, lse_all, s);
+  if (e == cudaSuccess && plan->num_comb_merge > 0)
+    e = launch_combine(*plan, out_readout, lse_readout, out_all, lse_all, s);
   if (e != cudaSuccess) return fail(PIE_ECUDA, std::string("attend launch: ") + cudaGetErrorString(e));
   return PIE_OK;
 }
