@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
-                             "masked_tova", "decode_pass"],
+                             "masked_tova", "decode_pass", "readout_topk"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
     ap.add_argument("--pool-pages", type=int, default=65536,
@@ -610,11 +610,68 @@ def run_workload(args, local):
     print(json.dumps(line))
 
 
+def run_readout(args, local):
+    """Time the readout distribution epilogue: the top-256 tokens of the
+    next-token distribution of 64 readout rows over a 128,256-token
+    vocabulary (fp32 synthetic logits), p, Z and lse.  Eight distinct logits
+    buffers (262 MB, more than L2) are cycled so every step reads from HBM."""
+    import torch
+    from programmable_paged_kv_gb300 import build, readout_topk, readout_topk_workspace_bytes
+    from programmable_paged_kv_gb300.abi import PIE_F32
+    torch.cuda.set_device(local)
+    build()
+    R, V, K = 64, 128256, 256
+    NB = 8
+    bufs = [torch.from_numpy(W.readout_logits(args.seed + i, R, V)).cuda() for i in range(NB)]
+    ids = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    probs = torch.empty((R, K), dtype=torch.float32, device="cuda")
+    z = torch.empty(R, dtype=torch.float32, device="cuda")
+    lse = torch.empty(R, dtype=torch.float32, device="cuda")
+    ws = torch.empty(readout_topk_workspace_bytes(PIE_F32, R, V, K), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    Kst, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        readout_topk(bufs[i % NB], K, ids, probs, z, lse, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(Kst)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(Kst):
+        ev[i][0].record(stream)
+        readout_topk(bufs[(Wm + i) % NB], K, ids, probs, z, lse, workspace=ws)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    call = sorted(a.elapsed_time(b) for a, b in ev)
+    med = call[len(call) // 2] / 1e3
+    byts = R * V * 4 + R * K * 8 + R * 8
+    hbm, kind = peaks()
+    line = {"workload": "readout_topk", "metric": "readout rows/s (top-256 of a 128,256-token "
+            "distribution, p, Z, lse)", "unit": "rows/s", "value": R / med,
+            "ms_per_step": t0.elapsed_time(t1) / Kst, "steps": Kst, "warmup": Wm,
+            "call_ms_median": med * 1e3, "alg_bytes": byts,
+            "hbm_gbs": byts / med / 1e9, "hbm_frac": byts / med / 1e9 / hbm,
+            "config": {"rows": R, "vocab": V, "k": K, "dtype": "f32",
+                       "l2": "8 logits buffers cycled (262 MB)"},
+            "peaks": {"hbm_gbs": hbm, "kind": kind}}
+    if clk:
+        line["clocks"] = clk
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     ws, rank, local, pg = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.workload == "readout_topk":
+        run_readout(args, local)
     elif args.workload != "decode_batch":
         run_workload(args, local)
     else:

@@ -188,6 +188,33 @@ void pie_fwd_plan_destroy(pie_fwd_plan_t* plan);
 /* Message for the calling thread's most recent error ("" if none). */
 const char* pie_fwd_last_error(void);
 
+/* Readout distribution epilogue (the review "Pie: Who Should Control the
+ * LLM Generation Loop?", section 7, Eq. (6)-(7): the serving system returns
+ * the K most probable tokens of the next-token distribution, K = 256 by
+ * default, and the mass Z they keep; 1 - Z is the total-variation distance
+ * of Eq. (7) when a client renormalises them).
+ *   logits : device, `rows` rows of `vocab` logits of `dtype` (PIE_F32 or
+ *            PIE_BF16), row r at logits + r * ld elements; rows start on
+ *            16-byte boundaries (logits 16-byte aligned, ld * element size a
+ *            multiple of 16); finite values or -inf.
+ *   ids    : device int32 [rows][k]: for each row the k tokens of largest
+ *            p = softmax(logits row) (temperature 1), largest first, equal
+ *            logits by smaller token id first.
+ *   probs  : device fp32 [rows][k]: p of those tokens (not renormalised).
+ *   z      : device fp32 [rows] or NULL: Z = the sum of the row's probs.
+ *   lse    : device fp32 [rows] or NULL: log(sum_v exp(logit_v)).
+ *   workspace : device, 256-byte aligned, at least
+ *            pie_fwd_readout_topk_workspace_bytes() bytes, caller-owned.
+ * Supported: 1 <= k <= 256, k <= vocab <= 262,144 (PIE_EUNSUPPORTED
+ * beyond); PIE_EINVAL for a bad dtype, NULL logits/ids/probs, ld < vocab or
+ * misaligned rows; PIE_ENOSPACE for a short workspace.  Two kernels on
+ * `stream`; no host synchronization. */
+int pie_fwd_readout_topk_workspace_bytes(int32_t dtype, int32_t rows, int32_t vocab, int32_t k,
+                                         size_t* bytes);
+int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t rows, int32_t vocab,
+                         int64_t ld, int32_t k, int32_t* ids, float* probs, float* z,
+                         float* lse, void* workspace, size_t ws_bytes, void* stream);
+
 /* Measurement hook (no counterpart on the Pie pages: it only lets a caller
  * time the attention kernels apart from the rest of a call).  After
  * pie_fwd_set_timing_events(start, stop) with two timing-enabled cudaEvent_t

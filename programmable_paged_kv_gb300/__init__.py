@@ -20,7 +20,7 @@ from .abi import (PIE_BF16, PIE_F32, PIE_FOLD_ALL, PIE_FOLD_CHANNEL, PIE_FOLD_CO
                   PIE_STATUS_FROZEN_WRITE, PIE_STATUS_TIMEOUT, PieError)
 
 __all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes", "build",
-           "set_timing_events",
+           "set_timing_events", "readout_topk", "readout_topk_workspace_bytes",
            "PIE_F32", "PIE_BF16", "PIE_FOLD_NONE", "PIE_FOLD_ALL", "PIE_FOLD_COUNT",
            "PIE_FOLD_CHANNEL", "PIE_STATUS_FROZEN_WRITE", "PIE_STATUS_FOLD_CLAMP",
            "PIE_STATUS_FOLD_GAP", "PIE_STATUS_TIMEOUT"]
@@ -88,6 +88,33 @@ def set_timing_events(start=None, stop=None) -> None:
     abi.check(abi.load().pie_fwd_set_timing_events(start.cuda_event if start is not None else None,
                                                    stop.cuda_event if stop is not None else None),
               "pie_fwd_set_timing_events")
+
+
+def readout_topk_workspace_bytes(dtype: int, rows: int, vocab: int, k: int) -> int:
+    n = C.c_size_t(0)
+    abi.check(abi.load().pie_fwd_readout_topk_workspace_bytes(dtype, rows, vocab, k, C.byref(n)),
+              "pie_fwd_readout_topk_workspace_bytes")
+    return int(n.value)
+
+
+def readout_topk(logits, k: int, ids, probs, z=None, lse=None, workspace=None, stream=None):
+    """pie_fwd_readout_topk on a 2-D CUDA tensor of logits (float32 or
+    bfloat16, rows of stride logits.stride(0)); ids int32 and probs float32
+    [rows, k], z and lse float32 [rows] or None."""
+    import torch
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D tensor with unit column stride")
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    dtype = PIE_BF16 if logits.dtype == torch.bfloat16 else PIE_F32
+    rows, vocab = logits.shape
+    if workspace is None:
+        need = readout_topk_workspace_bytes(dtype, rows, vocab, k)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=logits.device)
+    abi.check(abi.load().pie_fwd_readout_topk(
+        logits.data_ptr(), dtype, rows, vocab, logits.stride(0), k, _ptr(ids, "ids"),
+        _ptr(probs, "probs"), _ptr(z, "z", False), _ptr(lse, "lse", False),
+        _ptr(workspace, "workspace"), workspace.numel(), _stream(stream)), "pie_fwd_readout_topk")
 
 
 def _ptr(t, what: str, required: bool = True):

@@ -128,3 +128,25 @@ def test_empty_pass_plans(lib):
                q=z, k=z, v=z)
     rc, n = _ws(desc, p, 0)
     assert rc == abi.PIE_OK and n >= 0
+
+
+def test_readout_refuses_bad_calls_before_any_launch(lib):
+    n = C.c_size_t(0)
+    ws = lib.pie_fwd_readout_topk_workspace_bytes
+    assert ws(abi.PIE_F32, 64, 128256, 256, C.byref(n)) == abi.PIE_OK and n.value > 0
+    assert ws(abi.PIE_F32, 4, 1000, 0, C.byref(n)) == abi.PIE_EINVAL        # k < 1
+    assert ws(abi.PIE_F32, 4, 100, 101, C.byref(n)) == abi.PIE_EINVAL       # k > vocab
+    assert ws(7, 4, 1000, 8, C.byref(n)) == abi.PIE_EINVAL                  # dtype
+    assert ws(abi.PIE_F32, 4, 1000, 257, C.byref(n)) == abi.PIE_EUNSUPPORTED
+    assert ws(abi.PIE_BF16, 4, 262145, 8, C.byref(n)) == abi.PIE_EUNSUPPORTED
+    assert ws(abi.PIE_BF16, 4, 262144, 8, C.byref(n)) == abi.PIE_OK
+    # rows that do not start on 16-byte boundaries (fp32, ld 1001) and a NULL
+    # output are refused before anything is launched (the pointers are never
+    # dereferenced)
+    p = C.c_void_p(4096)
+    assert lib.pie_fwd_readout_topk(p, abi.PIE_F32, 2, 1001, 1001, 8, p, p, None, None, p, 1 << 20,
+                                    None) == abi.PIE_EINVAL
+    assert lib.pie_fwd_readout_topk(p, abi.PIE_F32, 2, 1000, 1000, 8, None, p, None, None, p, 1 << 20,
+                                    None) == abi.PIE_EINVAL
+    assert lib.pie_fwd_readout_topk(p, abi.PIE_F32, 2, 1000, 1000, 8, p, p, None, None, p, 16,
+                                    None) == abi.PIE_ENOSPACE

@@ -453,6 +453,20 @@ def small(name: str, seed: int = 0) -> Scenario:
     raise ValueError(name)
 
 
+def readout_logits(seed: int, rows: int, vocab: int, spikes: int = 8,
+                   scale: float = 2.0) -> np.ndarray:
+    """Synthetic next-token logits for the readout epilogue, float32 [rows,
+    vocab]: N(0, scale) per token plus `spikes` tokens per row raised by
+    U[6, 14] (a peaked distribution, like a language model's; no trained
+    weights)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    x = rng.normal(0.0, scale, size=(rows, vocab)).astype(np.float32)
+    for r in range(rows):
+        idx = rng.choice(vocab, size=min(spikes, vocab), replace=False)
+        x[r, idx] += rng.uniform(6.0, 14.0, size=idx.size).astype(np.float32)
+    return x
+
+
 FULL = {
     "tiny": lambda seed=0: tiny(seed),
     "decode_batch": lambda seed=0: decode_batch(seed),
