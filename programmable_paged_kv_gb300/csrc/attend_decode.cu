@@ -1,8 +1,6 @@
 // Step 2-3 of a ForwardPass for lanes with few query vectors per kv head
 // (decode rows, short drafts): split-KV grouped-query attention over paged
-// K/V (Pie "The forward pass": State geometry kv_len; Attention masks), and
-// the combine step that merges the split partial softmax states and gathers
-// the readout rows (section Readouts).
+// K/V (Pie "The forward pass": State geometry kv_len; Attention masks).
 //
 // Decode attention is bound by HBM: every visible slot's K and V head rows
 // are read once and used by the NQ query vectors of the GQA group.  The
@@ -22,14 +20,13 @@
 //     from a per-warp shared buffer.
 // Scores are kept in the log2 domain (q pre-scaled by sm_scale * log2 e).
 // Each work item writes one partial (max, sum, unnormalised output) per
-// query vector; the combine kernel merges an item's chunks.
+// query vector; the combine kernel (combine.cu) merges an item's chunks.
 
 #include "common.cuh"
 
 namespace pie {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T, int D, int NQ>
 struct DecCfg {
@@ -401,86 +398,6 @@ cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, con
               : launch_dec_nq<float, 128>(p, q_rot, k_pool, v_pool, mask_words, status, s);
   return bf ? launch_dec_nq<__nv_bfloat16, 64>(p, q_rot, k_pool, v_pool, mask_words, status, s)
             : launch_dec_nq<float, 64>(p, q_rot, k_pool, v_pool, mask_words, status, s);
-}
-
-// ---------------------------------------------------------------------------
-// Combine: one warp per (target row, q head).  Targets [0, R) are the readout
-// rows (written to out_readout / lse_readout); targets [R, R + N) are all rows
-// (out_all / lse_all) when requested.  Merges the chunks' (max, sum, output)
-// in the log2 domain; an empty visible set gives o = 0 and lse = -inf.
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv, int G, int N,
-                                                      int R, int with_all, int tc_bn,
-                                                      T* out_readout, float* lse_readout,
-                                                      T* out_all, float* lse_all) {
-  constexpr int DPL = D / 32;
-  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int targets = R + (with_all ? N : 0);
-  if (gw >= targets * Hq) return;
-  const int tgt = gw / Hq, h = gw % Hq;
-  const bool is_ro = tgt < R;
-  const int row = is_ro ? m.readout[tgt] : tgt - R;
-  const CombEntry ce = m.comb[int64_t(m.row_block[row]) * Hkv + h / G];
-  if (ce.nchunks < 0) return;  // written directly by the tensor-core kernel
-  const int qi = (row - ce.row0) * G + h % G;
-  // a masked tensor-core block uses as many chunks as its list length gives
-  const int nch = ce.mblock < 0 ? ce.nchunks
-                                : masked_chunks((m.list_len[ce.mblock] + tc_bn - 1) / tc_bn,
-                                                ce.nchunks, *m.mask_tiles, Hkv);
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
-  float o[DPL];
-#pragma unroll
-  for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-  float Ls = 0.f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nch; ++c) {
-      const int idx = ce.part_base + c * ce.stride + qi;
-      const float2 ml = m.part_ml[idx];
-      const float f = ex2(ml.x - M);
-      Ls = fmaf(f, ml.y, Ls);
-      const float* po = m.part_o + int64_t(idx) * D + lane * DPL;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[e] = fmaf(f, po[e], o[e]);
-    }
-  }
-  const bool empty = !(Ls > 0.f);
-  const float inv = empty ? 0.f : 1.f / Ls;
-  const float lse = empty ? -INFINITY : (M + log2f(Ls)) * kLn2;
-  T* dst = is_ro ? out_readout : out_all;
-  float* ldst = is_ro ? lse_readout : lse_all;
-  const int64_t orow = is_ro ? tgt : row;
-  if (dst) {
-    T* d = dst + (orow * Hq + h) * D + lane * DPL;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) d[e] = Elem<T>::from_f(o[e] * inv);
-  }
-  if (ldst && lane == 0) ldst[orow * Hq + h] = lse;
-}
-
-template <typename T, int D>
-static cudaError_t launch_comb(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
-                               void* out_all, float* lse_all, cudaStream_t s) {
-  const int with_all = (out_all || lse_all) ? 1 : 0;
-  const int64_t warps = int64_t(p.R + (with_all ? p.N : 0)) * p.desc.num_q_heads;
-  if (warps == 0) return cudaSuccess;
-  combine_kernel<T, D><<<int((warps + 3) / 4), 128, 0, s>>>(
-      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
-      tc_kv_tile(p.tc_nt), static_cast<T*>(out_readout), lse_readout, static_cast<T*>(out_all),
-      lse_all);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,
-                           void* out_all, float* lse_all, cudaStream_t s) {
-  const bool bf = p.desc.dtype == PIE_BF16;
-  if (p.desc.head_dim == 128)
-    return bf ? launch_comb<__nv_bfloat16, 128>(p, out_readout, lse_readout, out_all, lse_all, s)
-              : launch_comb<float, 128>(p, out_readout, lse_readout, out_all, lse_all, s);
-  return bf ? launch_comb<__nv_bfloat16, 64>(p, out_readout, lse_readout, out_all, lse_all, s)
-            : launch_comb<float, 64>(p, out_readout, lse_readout, out_all, lse_all, s);
 }
 
 }  // namespace pie
