@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
-                             "masked_tova", "decode_pass", "readout_topk"],
+                             "masked_tova", "decode_pass", "readout_topk", "decode_loop"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
     ap.add_argument("--pool-pages", type=int, default=65536,
@@ -665,6 +665,95 @@ def run_readout(args, local):
     print(json.dumps(line))
 
 
+def run_decode_loop(args, local):
+    """Time the decode loop that runs ahead of the host: the decode batch (64
+    lanes, C ~ U[512, 4096]) for K single-token steps in one
+    pie_fwd_decode_loop call (geometry and work items from frozen_len on the
+    device, no host plan per token), directly and as a replayed CUDA graph of
+    the same call (frozen_len reset inside the graph, so every replay is the
+    same K steps)."""
+    import torch
+    from programmable_paged_kv_gb300 import build, decode_loop, decode_loop_workspace_bytes, make_desc
+    torch.cuda.set_device(local)
+    build()
+    K, Wm = args.steps, args.warmup
+    NP = args.pool_pages
+    d, C, lane_pages, pass_meta = W.decode_loop_meta(seed=args.seed, steps=K + 1, num_pool_pages=NP)
+    desc = make_desc(d)
+    L, Hq, Hkv, D = 64, d.num_q_heads, d.num_kv_heads, d.head_dim
+    p0 = pass_meta(0)
+    torch.manual_seed(1000 + args.seed)
+    shape = (NP, Hkv, d.page_size, D)
+    k_pool = torch.randn(shape, dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.randn(shape, dtype=torch.bfloat16, device="cuda")
+    q = torch.randn((K, L, Hq, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.randn((K, L, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    v = torch.randn((K, L, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    q_rot = torch.empty((L, Hq, D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((K, L, Hq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((K, L, Hq), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    page_indptr = torch.from_numpy(p0.page_indptr.astype(np.int32)).cuda()
+    page_ids = torch.from_numpy(p0.page_ids.astype(np.int32)).cuda()
+    maxp = int(np.diff(p0.page_indptr).max())
+    frozen0 = torch.from_numpy(C.astype(np.int32)).cuda()
+    frozen = frozen0.clone()
+    ws = torch.empty(decode_loop_workspace_bytes(desc, L, maxp), dtype=torch.uint8, device="cuda")
+    tokens = sum(attended_tokens(pass_meta(t)) for t in range(K))
+    byts = sum(attend_alg_bytes(pass_meta(t), d) for t in range(K))
+    stream = torch.cuda.current_stream()
+
+    def call():
+        frozen.copy_(frozen0)
+        decode_loop(desc, page_indptr, page_ids, maxp, frozen, q, k, v, q_rot, k_pool, v_pool, out,
+                    lse, status, workspace=ws)
+
+    for _ in range(Wm):
+        call()
+    torch.cuda.synchronize()
+    reps = 5
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    direct_s = e0.elapsed_time(e1) / 1e3 / reps
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        call()
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    graph_s = e0.elapsed_time(e1) / 1e3 / reps
+    hbm, kind = peaks()
+    line = {"workload": "decode_loop", "metric": METRIC, "unit": UNIT,
+            "value": tokens / graph_s, "value_direct": tokens / direct_s,
+            "ms_per_step": graph_s / K * 1e3, "ms_per_step_direct": direct_s / K * 1e3,
+            "steps": K, "warmup": Wm, "status": int(status.item()),
+            "attend_alg_gbs": byts / graph_s / 1e9, "hbm_frac_whole_step": byts / graph_s / 1e9 / hbm,
+            "config": {"lanes": L, "kv_len": "C+t+1, C~U[512,4096]", "pool_pages": NP,
+                       "step": "geometry+RoPE/scatter+attend+combine+fold on the device"},
+            "peaks": {"hbm_gbs": hbm, "kind": kind}}
+    if clk:
+        line["clocks"] = clk
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     ws, rank, local, pg = dist_setup()
@@ -672,6 +761,8 @@ def main():
         run_reference(args, ws, rank)
     elif args.workload == "readout_topk":
         run_readout(args, local)
+    elif args.workload == "decode_loop":
+        run_decode_loop(args, local)
     elif args.workload != "decode_batch":
         run_workload(args, local)
     else:

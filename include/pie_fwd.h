@@ -76,6 +76,7 @@ extern "C" {
 #define PIE_STATUS_FOLD_CLAMP 2u   /* a channel count outside [0, n] was clamped          */
 #define PIE_STATUS_FOLD_GAP 8u     /* a folding lane's first slot != its frozen length    */
 #define PIE_STATUS_TIMEOUT 16u     /* a kernel's bounded wait expired; outputs invalid    */
+#define PIE_STATUS_LOOP_FULL 64u     /* decode loop: a lane had no slot left for a token   */
 #define PIE_STATUS_NOALLOC_TRUNC 32u /* no-allocation decode: a kv_len above max_kv_len was
                                         cut to max_kv_len                                   */
 
@@ -214,6 +215,39 @@ int pie_fwd_readout_topk_workspace_bytes(int32_t dtype, int32_t rows, int32_t vo
 int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t rows, int32_t vocab,
                          int64_t ld, int32_t k, int32_t* ids, float* probs, float* z,
                          float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* Decode loop that runs ahead of the host ("The forward pass", Pipelines and
+ * frames: run_ahead keeps a repeating decode pass in flight on the GPU).
+ * Runs `steps` single-row passes per lane on `stream`; step t of lane l is
+ * the folding() geometry of one new token (State geometry): position = slot
+ * = frozen_len[l], kv_len = frozen_len[l] + 1, fold all (frozen_len[l] += 1).
+ * The geometry and the work items are derived on the device from
+ * frozen_len, so the call builds no host plan per token, allocates nothing,
+ * never synchronizes the host and may be captured in a CUDA graph.
+ *   page_indptr [L+1], page_ids: device, the lanes' page lists (as in
+ *            pie_fwd_meta); each lane's capacity is its pages x page_size.
+ *   max_pages_per_lane: host, a bound on every lane's page count (sizes the
+ *            work-item grid and the workspace).
+ *   frozen_len [L]: device int32, read and advanced on the device.
+ *   q [steps][L][Hq][d], k, v [steps][L][Hkv][d]: device, per-step inputs
+ *            of the pass dtype; q_rot [L][Hq][d]: device scratch (the last
+ *            step's rotated queries on return).
+ *   out [steps][L][Hq][d] (pass dtype), lse [steps][L][Hq] (fp32, or NULL):
+ *            each step's attention output of every lane.
+ *   workspace: device, 256-byte aligned, at least
+ *            pie_fwd_decode_loop_workspace_bytes(); status: device uint32 or
+ *            NULL.
+ * A lane with no slot left (frozen_len >= its capacity) writes nothing, gets
+ * o = 0 and lse = -inf, does not advance, and sets PIE_STATUS_LOOP_FULL.
+ * Errors as pie_fwd_plan / pie_fwd_append_kv for shapes and pointers. */
+int pie_fwd_decode_loop_workspace_bytes(const pie_fwd_desc* desc, int32_t num_lanes,
+                                        int32_t max_pages_per_lane, size_t* bytes);
+int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, int32_t steps,
+                        const int32_t* page_indptr, const int32_t* page_ids,
+                        int32_t max_pages_per_lane, int32_t* frozen_len, const void* q,
+                        const void* k, const void* v, void* q_rot, void* k_pool, void* v_pool,
+                        void* out, float* lse, void* workspace, size_t ws_bytes,
+                        uint32_t* status, void* stream);
 
 /* Measurement hook (no counterpart on the Pie pages: it only lets a caller
  * time the attention kernels apart from the rest of a call).  After

@@ -21,6 +21,7 @@ from .abi import (PIE_BF16, PIE_F32, PIE_FOLD_ALL, PIE_FOLD_CHANNEL, PIE_FOLD_CO
 
 __all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes", "build",
            "set_timing_events", "readout_topk", "readout_topk_workspace_bytes",
+           "decode_loop", "decode_loop_workspace_bytes",
            "PIE_F32", "PIE_BF16", "PIE_FOLD_NONE", "PIE_FOLD_ALL", "PIE_FOLD_COUNT",
            "PIE_FOLD_CHANNEL", "PIE_STATUS_FROZEN_WRITE", "PIE_STATUS_FOLD_CLAMP",
            "PIE_STATUS_FOLD_GAP", "PIE_STATUS_TIMEOUT"]
@@ -88,6 +89,32 @@ def set_timing_events(start=None, stop=None) -> None:
     abi.check(abi.load().pie_fwd_set_timing_events(start.cuda_event if start is not None else None,
                                                    stop.cuda_event if stop is not None else None),
               "pie_fwd_set_timing_events")
+
+
+def decode_loop_workspace_bytes(desc: abi.pie_fwd_desc, num_lanes: int, max_pages_per_lane: int) -> int:
+    n = C.c_size_t(0)
+    abi.check(abi.load().pie_fwd_decode_loop_workspace_bytes(C.byref(desc), num_lanes,
+                                                             max_pages_per_lane, C.byref(n)),
+              "pie_fwd_decode_loop_workspace_bytes")
+    return int(n.value)
+
+
+def decode_loop(desc: abi.pie_fwd_desc, page_indptr, page_ids, max_pages_per_lane: int,
+                frozen_len, q, k, v, q_rot, k_pool, v_pool, out, lse=None, status=None,
+                workspace=None, stream=None):
+    """pie_fwd_decode_loop: q [steps, L, Hq, d], k/v [steps, L, Hkv, d], out
+    like q; page_indptr / page_ids / frozen_len int32 CUDA tensors."""
+    import torch
+    steps, L = int(q.shape[0]), int(q.shape[1])
+    if workspace is None:
+        need = decode_loop_workspace_bytes(desc, L, max_pages_per_lane)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    abi.check(abi.load().pie_fwd_decode_loop(
+        C.byref(desc), L, steps, _ptr(page_indptr, "page_indptr"), _ptr(page_ids, "page_ids"),
+        max_pages_per_lane, _ptr(frozen_len, "frozen_len"), _ptr(q, "q"), _ptr(k, "k"),
+        _ptr(v, "v"), _ptr(q_rot, "q_rot"), _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
+        _ptr(out, "out"), _ptr(lse, "lse", False), _ptr(workspace, "workspace"), workspace.numel(),
+        _ptr(status, "status", False), _stream(stream)), "pie_fwd_decode_loop")
 
 
 def readout_topk_workspace_bytes(dtype: int, rows: int, vocab: int, k: int) -> int:

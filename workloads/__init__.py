@@ -330,6 +330,25 @@ def decode_loop_meta(seed: int = 0, lanes: int = 64, steps: int = 64, c_lo: int 
     return desc, C, lane_pages, pass_meta
 
 
+def decode_loop(seed: int = 0, lanes: int = 64, steps: int = 8, c_lo: int = 512,
+                c_hi: int = 4096, num_pool_pages: int = 65536, desc: Optional[Desc] = None,
+                spare: int = 0) -> Scenario:
+    """The decode batch as `steps` single-row passes with q/k/v: pass t puts
+    each lane's row at position/slot C+t, reads C+t+1 slots and folds it.
+    Each lane's pages hold C + steps + spare slots (rounded up to pages)."""
+    desc = desc or Desc(32, 8, 128, 16, BF16)
+    r_meta, r_data = _rngs(seed, 2)
+    C = r_meta.integers(c_lo, c_hi + 1, size=lanes).astype(np.int32)
+    counts = [_pages_for(int(c) + steps + spare, desc.page_size) for c in C]
+    lane_pages = _permuted_pool(r_meta, num_pool_pages, counts)
+    passes = [_lane_pass(desc, [([int(c) + t], [int(c) + t]) for c in C], lane_pages, C + t + 1,
+                         [FOLD_ALL] * lanes, r_data) for t in range(steps)]
+    pool_pages = np.sort(np.concatenate(lane_pages))
+    k0, v0 = _fill_pool_init(desc, pool_pages, lane_pages, C, r_data)
+    return Scenario("decode_loop", desc, num_pool_pages, pool_pages, k0, v0, C.copy(), passes,
+                    recipe=f"{lanes} lanes x {steps} single-row steps, C ~ U[{c_lo},{c_hi}]")
+
+
 # ---- configuration 3: guidance lane pairs ---------------------------------------
 def guidance_pairs(seed: int = 0, pairs: int = 32, prefix: int = 1024, prefill: int = 64,
                    decodes: int = 16, num_pool_pages: int = 4096,
