@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
-                             "masked_tova", "decode_pass", "readout_topk", "decode_loop"],
+                             "masked_tova", "decode_pass", "readout_topk", "decode_loop",
+                             "adapters_decode", "adapters_prefill"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
     ap.add_argument("--pool-pages", type=int, default=65536,
@@ -665,6 +666,128 @@ def run_readout(args, local):
     print(json.dumps(line))
 
 
+ADAPTER_SHAPES = {
+    # the decode batch's 64 lanes x 1 row, and the guidance-pair prefill's 64
+    # lanes x 64 rows, at the q site of a 32 x 128-head model (4096 -> 4096)
+    "adapters_decode": dict(rows=[1] * 64, sites=64),
+    "adapters_prefill": dict(rows=[64] * 64, sites=8),
+}
+
+
+def adapter_alg_bytes(site) -> int:
+    """Bytes one apply must move: x of the adapted rows, y of those rows read
+    and written, and A, B, IA3 and scale of every adapter in use (the fp32
+    partial sums of A x, about 1% at these sizes, are not counted)."""
+    adapted = 0
+    for l, a in enumerate(site.adapter_of_lane):
+        if a >= 0:
+            adapted += int(site.row_indptr[l + 1] - site.row_indptr[l])
+    d_in, d_out, r = site.x.shape[1], site.y.shape[1], site.rank
+    used = len({int(a) for a in site.adapter_of_lane if a >= 0})
+    per_ad = 2 * (r * d_in + d_out * r) + (2 * d_out if site.ia3 is not None else 0) + 4
+    return adapted * (2 * d_in + 4 * d_out) + used * per_ad, adapted
+
+
+def adapter_oracle_rate(site, seconds: float):
+    """The oracle on a bounded sample: whole lanes of the same site, repeated
+    until `seconds` of CPU time; returns adapted rows per second."""
+    import oracle.adapters as OA
+    f64 = lambda b: W.bf16_bits_to_f32(b).astype(np.float64)
+    x, y, A, B = f64(site.x), f64(site.y), f64(site.lora_a), f64(site.lora_b)
+    s = None if site.ia3 is None else f64(site.ia3)
+    _, rows = adapter_alg_bytes(site)
+    total, reps = 0.0, 0
+    while total < seconds or reps == 0:
+        t0 = time.perf_counter()
+        OA.apply_adapters(x, y, site.row_indptr, site.adapter_of_lane, A, B,
+                          site.scale.astype(np.float64), s)
+        total += time.perf_counter() - t0
+        reps += 1
+    return rows * reps / total, reps, total
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS may use (all cores when that cannot be read)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_adapters(args, local):
+    """Time the per-lane adapters at one projection site (LoRA rank 16 and
+    IA3, 16 adapters, every 8th lane without one), site after site: `sites`
+    distinct sets of weights, x and y (more than L2 together) are cycled, as
+    a model's layers would be, so every call reads from HBM."""
+    import torch
+    from programmable_paged_kv_gb300 import AdapterPlan, build, runner
+    torch.cuda.set_device(local)
+    build()
+    shape = ADAPTER_SHAPES[args.workload]
+    sites = [W.adapter_site(args.seed + i, shape["rows"]) for i in range(shape["sites"])]
+    dev = lambda a: runner.to_device(a, W.BF16)
+    bufs = [(dev(st.x), dev(st.y), dev(st.lora_a), dev(st.lora_b),
+             torch.from_numpy(st.scale).cuda(), dev(st.ia3)) for st in sites]
+    plan = AdapterPlan(sites[0].row_indptr, sites[0].adapter_of_lane, len(sites[0].scale), 16)
+    # every site shares the lanes' adapter ids (one pass, many sites)
+    for st in sites[1:]:
+        st.adapter_of_lane = sites[0].adapter_of_lane
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    NB, Kst, Wm = len(bufs), args.steps, args.warmup
+    for i in range(Wm):
+        plan.apply(*bufs[i % NB][:2], *bufs[i % NB][2:], status=status)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(Kst)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(Kst):
+        b = bufs[(Wm + i) % NB]
+        ev[i][0].record(stream)
+        plan.apply(b[0], b[1], b[2], b[3], b[4], b[5], status=status)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert int(status.item()) == 0, f"status {int(status.item())}"
+    call = sorted(a.elapsed_time(c) for a, c in ev)
+    med = call[len(call) // 2] / 1e3
+    byts, rows = adapter_alg_bytes(sites[0])
+    hbm, kind = peaks()
+    line = {"workload": args.workload,
+            "metric": "adapted rows/s (LoRA r16 + IA3 at a 4096 -> 4096 projection site)",
+            "unit": "rows/s", "value": rows / med, "ms_per_step": med * 1e3,
+            "steps": Kst, "warmup": Wm, "call_ms_median": med * 1e3,
+            "call_ms_mean": sum(call) / len(call), "alg_bytes": byts,
+            "gpu_launches": 2 * Kst,
+            "roofline": {"bound": "hbm", "achieved": byts / med / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": byts / med / 1e9 / hbm, "traffic": None, "peak_kind": kind},
+            "config": {"lanes": len(shape["rows"]), "rows": int(sites[0].row_indptr[-1]),
+                       "adapted_rows": rows, "d_in": 4096, "d_out": 4096, "rank": 16,
+                       "adapters": 16, "dtype": "bf16", "recipe": sites[0].recipe,
+                       "l2": f"{NB} sites cycled "
+                             f"({NB * (byts + 2 * 16 * 4096 * 16 * 2) / 1e6:.0f} MB)"}}
+    if clk:
+        line["clocks"] = clk
+    if not args.no_cpu_baseline:
+        rate, reps, secs = adapter_oracle_rate(sites[0], min(args.cpu_seconds, 8.0))
+        line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"the whole site, {reps} applies in {secs:.1f} s "
+                                          "(numpy fp64 matrix products)"}
+    print(json.dumps(line))
+    plan.close()
+
+
 def run_decode_loop(args, local):
     """Time the decode loop that runs ahead of the host: the decode batch (64
     lanes, C ~ U[512, 4096]) for K single-token steps in one
@@ -763,6 +886,8 @@ def main():
         run_readout(args, local)
     elif args.workload == "decode_loop":
         run_decode_loop(args, local)
+    elif args.workload in ADAPTER_SHAPES:
+        run_adapters(args, local)
     elif args.workload != "decode_batch":
         run_workload(args, local)
     else:

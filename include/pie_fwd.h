@@ -249,6 +249,60 @@ int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, int32_t ste
                         void* out, float* lse, void* workspace, size_t ws_bytes,
                         uint32_t* status, void* stream);
 
+/* Per-lane adapters at a projection site ("The forward pass", section
+ * Adapters: an adapter is a function of a projection's input x and base
+ * output y, LoRA adds b (a x), IA3 scales y, and requests in one batch may
+ * use different adapters).  Every row of lane l takes adapter
+ * a = adapter_of_lane[l] (-1: none) and becomes
+ *     y' = (y + scale[a] * B_a (A_a x)) * s_a      (elementwise in s_a)
+ * with A_a = lora_a[a] [rank][d_in], B_a = lora_b[a] [d_out][rank] and
+ * s_a = ia3[a] [d_out] (all ones when ia3 is NULL).  y is updated in place;
+ * rows of lanes without an adapter are not touched.  Products and sums are
+ * fp32 (A_a x on the tensor cores from bf16 operands), y' is rounded to bf16
+ * once.
+ *
+ * A plan cuts the lanes' rows into tiles of up to 128 consecutive rows of one
+ * lane; it depends only on the lanes, so one plan serves every site and layer
+ * of a pass (q, k, v, o, gate_up, down), each with its own weights and dims.
+ *   row_indptr [L+1], adapter_of_lane [L]: HOST arrays, read during the call
+ *            and not retained; rows of lane l are [row_indptr[l], row_indptr[l+1]).
+ *   max_rank: the largest rank any apply of this plan will use.
+ *   dev_workspace: device, 256-byte aligned, at least
+ *            pie_fwd_adapter_workspace_bytes(); holds the tiles (one
+ *            host-to-device copy queued on `stream`) and the fp32 partial
+ *            sums of A_a x.  Applies of one plan share that scratch: issue them
+ *            on one stream (or otherwise ordered).
+ * Errors: PIE_EINVAL (NULL arrays, row_indptr[0] != 0 or not monotone),
+ * PIE_ERANGE (adapter id outside [-1, num_adapters)), PIE_EUNSUPPORTED
+ * (max_rank not in {0, 8, 16, 32, 64}), PIE_ENOSPACE (short workspace). */
+typedef struct pie_fwd_adapter_plan pie_fwd_adapter_plan_t;
+int pie_fwd_adapter_workspace_bytes(int32_t num_lanes, const int32_t* row_indptr,
+                                    int32_t max_rank, size_t* bytes);
+int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
+                         const int32_t* adapter_of_lane, int32_t num_adapters, int32_t max_rank,
+                         void* dev_workspace, size_t ws_bytes, void* stream,
+                         pie_fwd_adapter_plan_t** out);
+/* Number of tiles of a plan (rows of lanes with an adapter, 128 per tile). */
+int32_t pie_fwd_adapter_plan_num_tiles(const pie_fwd_adapter_plan_t* plan);
+/* Apply the adapters at one site.
+ *   x: device bf16 [num_rows][d_in]; y: device bf16 [num_rows][d_out], both
+ *            contiguous and 16-byte aligned.
+ *   lora_a: device bf16 [num_adapters][rank][d_in]; lora_b: device bf16
+ *            [num_adapters][d_out][rank]; scale: device fp32 [num_adapters];
+ *            ia3: device bf16 [num_adapters][d_out] or NULL.  With rank 0 only
+ *            the IA3 scaling runs (x, lora_a, lora_b, scale may be NULL).
+ *   status: device uint32 or NULL (PIE_STATUS_TIMEOUT).
+ * Supported: dtype PIE_BF16, rank in {0, 8, 16, 32, 64} and <= max_rank,
+ * d_in a multiple of 64, d_out a multiple of 256 (PIE_EUNSUPPORTED / ERANGE
+ * otherwise); PIE_EINVAL for NULL or misaligned required pointers.  Up to two
+ * kernels on `stream`; no host synchronization. */
+int pie_fwd_adapter_apply(const pie_fwd_adapter_plan_t* plan, int32_t dtype, int32_t d_in,
+                          int32_t d_out, int32_t rank, const void* x, void* y, const void* lora_a,
+                          const void* lora_b, const float* scale, const void* ia3,
+                          uint32_t* status, void* stream);
+/* Release a plan (its staging memory is reused once its upload completed). */
+void pie_fwd_adapter_plan_destroy(pie_fwd_adapter_plan_t* plan);
+
 /* Measurement hook (no counterpart on the Pie pages: it only lets a caller
  * time the attention kernels apart from the rest of a call).  After
  * pie_fwd_set_timing_events(start, stop) with two timing-enabled cudaEvent_t

@@ -218,3 +218,72 @@ class ForwardPlan:
             self.close()
         except Exception:
             pass
+
+
+def adapter_workspace_bytes(row_indptr, max_rank: int = 16) -> int:
+    """pie_fwd_adapter_workspace_bytes for host lanes (row_indptr [L+1])."""
+    ri = np.ascontiguousarray(row_indptr, dtype=np.int32)
+    n = C.c_size_t(0)
+    abi.check(abi.load().pie_fwd_adapter_workspace_bytes(len(ri) - 1, ri.ctypes.data, max_rank,
+                                                          C.byref(n)),
+              "pie_fwd_adapter_workspace_bytes")
+    return int(n.value)
+
+
+class AdapterPlan:
+    """Per-lane adapters of one pass (pie_fwd_adapter_plan): the lanes' rows
+    cut into tiles, planned once and applied at any number of projection
+    sites with apply().
+
+    row_indptr [L+1] and adapter_of_lane [L] are host integer arrays
+    (adapter -1: none); workspace is an optional uint8 CUDA tensor of at least
+    adapter_workspace_bytes(), allocated here when omitted."""
+
+    def __init__(self, row_indptr, adapter_of_lane, num_adapters: int, max_rank: int = 16,
+                 workspace=None, stream=None):
+        import torch
+        self.lib = abi.load()
+        ri = np.ascontiguousarray(row_indptr, dtype=np.int32)
+        al = np.ascontiguousarray(adapter_of_lane, dtype=np.int32)
+        if len(al) != len(ri) - 1:
+            raise ValueError("adapter_of_lane needs one entry per lane")
+        if workspace is None:
+            need = adapter_workspace_bytes(ri, max_rank)
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        self.workspace = workspace
+        h = C.c_void_p()
+        abi.check(self.lib.pie_fwd_adapter_plan(
+            len(al), ri.ctypes.data, al.ctypes.data, num_adapters, max_rank,
+            _ptr(workspace, "workspace"), workspace.numel(), _stream(stream), C.byref(h)),
+            "pie_fwd_adapter_plan")
+        self.handle = h
+        self.num_tiles = int(self.lib.pie_fwd_adapter_plan_num_tiles(h))
+
+    def apply(self, x, y, lora_a=None, lora_b=None, scale=None, ia3=None, status=None,
+              stream=None):
+        """y (bf16 [N, d_out], updated in place) += scale[a] B_a (A_a x), then
+        scaled by ia3[a]; lora_a [n_ad, r, d_in], lora_b [n_ad, d_out, r],
+        scale fp32 [n_ad], ia3 [n_ad, d_out] or None; lora_a None means rank 0
+        (IA3 only)."""
+        import torch
+        if y.dtype != torch.bfloat16:
+            raise ValueError("adapters are built for bfloat16")
+        d_out = y.shape[1]
+        rank = 0 if lora_a is None else lora_a.shape[1]
+        d_in = x.shape[1] if x is not None else (lora_a.shape[2] if lora_a is not None else 64)
+        abi.check(self.lib.pie_fwd_adapter_apply(
+            self.handle, PIE_BF16, d_in, d_out, rank, _ptr(x, "x", False), _ptr(y, "y"),
+            _ptr(lora_a, "lora_a", False), _ptr(lora_b, "lora_b", False),
+            _ptr(scale, "scale", False), _ptr(ia3, "ia3", False), _ptr(status, "status", False),
+            _stream(stream)), "pie_fwd_adapter_apply")
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.pie_fwd_adapter_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

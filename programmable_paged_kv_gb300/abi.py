@@ -81,6 +81,14 @@ SIGNATURES = {
                                        C.c_void_p, C.c_size_t, C.c_void_p]),
     "pie_fwd_decode_attend_noalloc": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32, C.c_int32,
                                                 _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pie_fwd_adapter_workspace_bytes": (C.c_int, [C.c_int32, _P, C.c_int32,
+                                                  C.POINTER(C.c_size_t)]),
+    "pie_fwd_adapter_plan": (C.c_int, [C.c_int32, _P, _P, C.c_int32, C.c_int32, _P, C.c_size_t,
+                                       _P, C.POINTER(C.c_void_p)]),
+    "pie_fwd_adapter_plan_num_tiles": (C.c_int32, [_P]),
+    "pie_fwd_adapter_apply": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
+                                        _P, _P, _P, _P, _P, _P]),
+    "pie_fwd_adapter_plan_destroy": (None, [_P]),
 }
 
 

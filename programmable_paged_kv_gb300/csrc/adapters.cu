@@ -1,0 +1,548 @@
+// Per-lane adapters at a projection site (Pie "The forward pass", section
+// Adapters).  Every row of lane l takes the lane's adapter a: a LoRA pair
+// A_a [r][d_in], B_a [d_out][r] with a scale c_a, and an optional IA3 vector
+// s_a [d_out]:
+//     y' = (y + c_a B_a (A_a x)) * s_a          (elementwise in s_a)
+// written over y in place; rows of lanes without an adapter keep y.
+//
+// The rows are cut into tiles of up to 128 consecutive rows of one lane
+// (planned once per pass, reused at every site and layer), and each site
+// runs two kernels:
+//   shrink  t = A_a x on the tensor cores.  The adapter's rank is the MMA's
+//           M side and the tile's rows its N side (rounded up to 16), so a
+//           one-row decode lane costs a 16-column tile, not a 128-row one.
+//           A_a fills the first r of the 128 operand rows; the rows after it
+//           read whatever follows in shared memory, and their accumulator
+//           lanes are never read.  A CTA covers one range of d_in for one
+//           tile: warp 0 streams 64-column chunks of A_a and of the tile's x
+//           rows (2-D tensor maps, 128-byte swizzle, each box copied from its
+//           own lane) through a 4-deep ring, one thread of warp 1 issues four
+//           K=16 MMAs per chunk into a TMEM accumulator [r lanes x N
+//           columns], and the first r/32 warps store the fp32 partial sums of
+//           their range.
+//   expand  y' = (y + c_a B_a t) * s_a on the CUDA cores in fp32: one CTA per
+//           (tile, 256 output columns), one column per thread.  The tile's y
+//           rows arrive by 1-D bulk copies in groups of 16 rows, t (the
+//           partial sums added up and scaled by c_a) sits in shared memory,
+//           each thread keeps its column's row of B_a in registers, and every
+//           finished group goes back to y by bulk stores.
+// The expand moves 4 bytes of y per output for r multiply-adds and is bound
+// by HBM, so it stays off the tensor cores; the shrink does r multiply-adds
+// per 2 bytes of x, the contraction that needs them.  Every wait is bounded
+// in time (PIE_STATUS_TIMEOUT).
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+#include "tc_util.cuh"
+
+namespace pie {
+namespace ad {
+
+constexpr int kTileRows = 128;   // rows per tile (the MMA's largest N used here)
+constexpr int kChunk = 64;       // d_in columns per ring stage: one 128-byte swizzle row
+constexpr int kStages = 4;       // shrink ring depth
+constexpr int kMaxSplits = 8;    // d_in ranges per tile (partial sums kept per range)
+constexpr int kOBlock = 256;     // output columns per expand CTA (one per thread)
+constexpr int kGroupRows = 16;   // y rows per arrival barrier in the expand
+constexpr int kMaxGroups = kTileRows / kGroupRows;
+constexpr int kShrinkCtasPerSm = 3;
+static_assert(kMaxGroups * 8 <= 128, "expand barriers live in the first 128 bytes");
+
+// Up to kTileRows consecutive rows [row0, row0 + n) of one lane and its adapter.
+struct alignas(16) Tile {
+  int32_t row0, n, adapter, pad;
+};
+
+template <int R>
+struct __align__(1024) ShrinkSmem {
+  uint8_t a[kStages][R * 128];           // A_a chunk: R rows x 64 columns (bf16)
+  uint8_t x[kStages][kTileRows * 128];   // x chunk: up to 128 rows x 64 columns
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t done;
+  uint32_t tmem_base;
+};
+// The M=128 operand read from the last A stage stays inside the structure.
+static_assert(sizeof(ShrinkSmem<8>) >= (kStages - 1) * 8 * 128 + 128 * 128, "A operand overrun");
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* f) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(r[i]);
+}
+
+// 1-D bulk copy shared -> global in the calling thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+}  // namespace ad
+
+// t_part[split][row][k] = sum over the split's d_in range of A_a[k][i] x[row][i]
+template <int R>
+__global__ void __launch_bounds__(128) adapter_shrink_kernel(
+    const ad::Tile* __restrict__ tiles, int chunks_per_split, int num_chunks, int num_rows,
+    float* __restrict__ t_part, uint32_t* status, const __grid_constant__ CUtensorMap xmap,
+    const __grid_constant__ CUtensorMap amap) {
+  using namespace ad;
+  using namespace tc;
+  extern __shared__ uint8_t raw[];
+  ShrinkSmem<R>& S = *reinterpret_cast<ShrinkSmem<R>*>(
+      (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  const Tile tile = tiles[blockIdx.x];
+  const int split = blockIdx.y;
+  const int c0 = split * chunks_per_split;
+  const int nc = min(num_chunks, c0 + chunks_per_split) - c0;  // >= 1 (host sizing)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = (tile.n + 15) & ~15;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&S.tmem_base)),
+                 "r"(kTileRows)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool bad = false;
+
+  if (warp == 0) {
+    // ---- producer: lane i < N/16 copies x rows [row0 + 16 i, +16), lane 31 A_a
+    const uint64_t pol_x = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    int issued = 0;
+    for (int i = 0; i < nc; ++i) {
+      const int st = i % kStages;
+      if (i >= kStages) {
+        int ok = lane == 0 ? int(mbar_wait(&S.empty[st], ((i / kStages) - 1) & 1)) : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          bad = true;
+          break;
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&S.full[st], uint32_t(R + N) * 128u);
+      __syncwarp();
+      const int cx = (c0 + i) * kChunk;
+      if (lane < N / 16)
+        tma_2d(S.x[st] + lane * 2048, &xmap, cx, tile.row0 + lane * 16, &S.full[st], pol_x);
+      if (lane == 31) tma_2d(S.a[st], &amap, cx, tile.adapter * R, &S.full[st], pol_a);
+      issued = i + 1;
+    }
+    // copies still in flight must land before the CTA may exit
+    if (lane == 0)
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        if (!mbar_wait(&S.full[i % kStages], (i / kStages) & 1)) bad = true;
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer: D[k][j] += A_a[k][c] x[j][c] over the chunk, 4 x K=16
+    if (lane == 0) {
+      const uint32_t id = idesc(128, N, false);
+      for (int i = 0; i < nc; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(&S.full[st], (i / kStages) & 1)) {
+          bad = true;
+          break;
+        }
+        fence_after();
+        const uint64_t da = sdesc(S.a[st], 16, 1024), dx = sdesc(S.x[st], 16, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem, da + 2 * k, dx + 2 * k, id, (i > 0 || k > 0) ? 1u : 0u);
+        commit(&S.empty[st]);
+      }
+      commit(&S.done);  // arrives when every MMA issued above has completed
+    }
+    __syncwarp();
+  }
+
+  // ---- epilogue: TMEM lane k holds t[row0 + j][k] at column j
+  if (warp < (R + 31) / 32) {
+    int ok = lane == 0 ? int(mbar_wait(&S.done, 0)) : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      bad = true;
+    } else {
+      fence_after();
+      const int k = warp * 32 + lane;
+      float* dst = t_part + (int64_t(split) * num_rows + tile.row0) * R + k;
+      for (int cb = 0; cb < N; cb += 16) {
+        float v[16];
+        tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(cb), v);
+        if (k < R) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (cb + jj < tile.n) dst[int64_t(cb + jj) * R] = v[jj];
+        }
+      }
+    }
+  }
+  if (bad) set_status(status, PIE_STATUS_TIMEOUT);
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTileRows)
+                 : "memory");
+  }
+}
+
+// y[row][o] = (y[row][o] + c_a sum_k B_a[o][k] t[row][k]) * s_a[o] for the
+// tile's rows and 256 columns
+template <int R>
+__global__ void __launch_bounds__(ad::kOBlock) adapter_expand_kernel(
+    const ad::Tile* __restrict__ tiles, int splits, int num_rows, const float* __restrict__ t_part,
+    const __nv_bfloat16* __restrict__ lora_b, const float* __restrict__ scale,
+    const __nv_bfloat16* __restrict__ ia3, __nv_bfloat16* __restrict__ y, int d_out,
+    int max_rows, uint32_t* status) {
+  using namespace ad;
+  extern __shared__ __align__(128) uint8_t raw[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(raw);
+  float* ts = reinterpret_cast<float*>(raw + 128);  // [max_rows][R]
+  __nv_bfloat16* ys =
+      reinterpret_cast<__nv_bfloat16*>(raw + 128 + size_t(max_rows) * R * 4);  // [max_rows][256]
+  const Tile tile = tiles[blockIdx.x];
+  const int o0 = blockIdx.y * kOBlock;
+  const int n = tile.n, a = tile.adapter;
+  const int ngroups = (n + kGroupRows - 1) / kGroupRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int g = 0; g < ngroups; ++g) mbar_init(&bar[g], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  __nv_bfloat16* yt = y + int64_t(tile.row0) * d_out + o0;
+  if (warp == 0) {
+    if (lane < ngroups)
+      mbar_arrive_expect_tx(&bar[lane],
+                            uint32_t(min(kGroupRows, n - lane * kGroupRows)) * kOBlock * 2u);
+    __syncwarp();
+    for (int j = lane; j < n; j += 32)
+      bulk_g2s(ys + j * kOBlock, yt + int64_t(j) * d_out, kOBlock * 2, &bar[j / kGroupRows]);
+  }
+
+  const int o = o0 + tid;
+  float b[R > 0 ? R : 1];
+  if constexpr (R > 0) {
+    const float c = scale[a];
+    for (int e = tid; e < n * R; e += kOBlock) {
+      const float* src = t_part + int64_t(tile.row0) * R + e;
+      float acc = 0.f;
+      for (int s = 0; s < splits; ++s) acc += src[int64_t(s) * num_rows * R];
+      ts[e] = acc * c;
+    }
+    const uint4* bp = reinterpret_cast<const uint4*>(lora_b + (int64_t(a) * d_out + o) * R);
+#pragma unroll
+    for (int q = 0; q < R / 8; ++q) unpack16<__nv_bfloat16>(__ldg(bp + q), b + 8 * q);
+  }
+  const float s_o = ia3 ? __bfloat162float(ia3[int64_t(a) * d_out + o]) : 1.f;
+  __syncthreads();
+
+  bool bad = false;
+  for (int g = 0; g < ngroups; ++g) {
+    const bool ok = mbar_wait(&bar[g], 0);
+    if (__syncthreads_or(!ok)) {
+      bad = true;
+      break;
+    }
+    const int j0 = g * kGroupRows, j1 = min(n, j0 + kGroupRows);
+    for (int j = j0; j < j1; ++j) {
+      float acc0 = 0.f, acc1 = 0.f;
+      if constexpr (R > 0) {
+        const float4* tj = reinterpret_cast<const float4*>(ts + j * R);
+#pragma unroll
+        for (int q = 0; q < R / 4; ++q) {
+          const float4 t4 = tj[q];
+          ffma2(acc0, acc1, b[4 * q], b[4 * q + 1], t4.x, t4.y, acc0, acc1);
+          ffma2(acc0, acc1, b[4 * q + 2], b[4 * q + 3], t4.z, t4.w, acc0, acc1);
+        }
+      }
+      __nv_bfloat16& yv = ys[j * kOBlock + tid];
+      yv = __float2bfloat16_rn((__bfloat162float(yv) + (acc0 + acc1)) * s_o);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0 && lane < j1 - j0) {
+      const int j = j0 + lane;
+      bulk_s2g(yt + int64_t(j) * d_out, ys + j * kOBlock, kOBlock * 2);
+      bulk_commit();
+    }
+  }
+  if (warp == 0) bulk_wait_read_all();  // shared memory must outlive the stores' reads
+  if (bad && tid == 0) {
+    set_status(status, PIE_STATUS_TIMEOUT);
+    for (int g = 0; g < ngroups; ++g) mbar_wait(&bar[g], 0);  // copies still in flight land first
+  }
+}
+
+}  // namespace pie
+
+// ---------------------------------------------------------------------------
+// host side: plan and launches
+// ---------------------------------------------------------------------------
+struct pie_fwd_adapter_plan {
+  int32_t num_lanes, num_rows, num_adapters, max_rank;
+  int32_t num_tiles, max_tile_rows;
+  pie::ad::Tile* tiles;  // device, in the workspace
+  float* t_part;         // device scratch: [kMaxSplits][num_rows][max_rank]
+  pie::PinnedBlock* staging;
+};
+
+namespace {
+
+using pie::set_last_error;
+
+int check_lanes(int32_t num_lanes, const int32_t* row_indptr, int64_t* num_tiles) {
+  if (num_lanes < 0) return set_last_error(PIE_EINVAL, "num_lanes < 0");
+  if (!row_indptr) return set_last_error(PIE_EINVAL, "row_indptr is NULL");
+  if (row_indptr[0] != 0) return set_last_error(PIE_EINVAL, "row_indptr[0] != 0");
+  int64_t t = 0;
+  for (int l = 0; l < num_lanes; ++l) {
+    if (row_indptr[l + 1] < row_indptr[l])
+      return set_last_error(PIE_EINVAL, "row_indptr is not monotone");
+    t += (int64_t(row_indptr[l + 1]) - row_indptr[l] + pie::ad::kTileRows - 1) /
+         pie::ad::kTileRows;
+  }
+  *num_tiles = t;
+  return PIE_OK;
+}
+
+bool rank_built(int r) { return r == 0 || r == 8 || r == 16 || r == 32 || r == 64; }
+
+struct WsLayout {
+  size_t tiles = 0, t_part = 0, total = 0;
+};
+
+WsLayout ws_layout(int64_t num_tiles, int64_t num_rows, int max_rank) {
+  auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
+  WsLayout Y;
+  Y.tiles = 0;
+  Y.t_part = up(size_t(num_tiles) * sizeof(pie::ad::Tile));
+  Y.total = Y.t_part + up(size_t(pie::ad::kMaxSplits) * size_t(num_rows) * size_t(max_rank) * 4);
+  return Y;
+}
+
+template <int R>
+cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out, const void* x,
+                           void* y, const void* lora_a, const void* lora_b, const float* scale,
+                           const void* ia3, uint32_t* status, cudaStream_t s) {
+  using namespace pie;
+  int splits = 1;
+  if constexpr (R > 0) {
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int num_chunks = d_in / ad::kChunk;
+    const int64_t want = (int64_t(ad::kShrinkCtasPerSm) * sms + p.num_tiles - 1) / p.num_tiles;
+    splits = int(std::max<int64_t>(1, std::min<int64_t>(want, std::min(ad::kMaxSplits, num_chunks))));
+    const int cps = (num_chunks + splits - 1) / splits;
+    splits = (num_chunks + cps - 1) / cps;
+
+    CUtensorMap xmap, amap;
+    {
+      const cuuint64_t dims[2] = {cuuint64_t(d_in), cuuint64_t(p.num_rows)};
+      const cuuint64_t str[1] = {cuuint64_t(d_in) * 2};
+      const cuuint32_t box[2] = {ad::kChunk, 16};
+      if (!tc::make_map(&xmap, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+      const cuuint64_t dims[2] = {cuuint64_t(d_in), cuuint64_t(p.num_adapters) * R};
+      const cuuint64_t str[1] = {cuuint64_t(d_in) * 2};
+      const cuuint32_t box[2] = {ad::kChunk, cuuint32_t(R)};
+      if (!tc::make_map(&amap, lora_a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    const size_t smem = sizeof(ad::ShrinkSmem<R>) + 1024;
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(adapter_shrink_kernel<R>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    adapter_shrink_kernel<R><<<dim3(p.num_tiles, splits), 128, smem, s>>>(
+        p.tiles, cps, num_chunks, p.num_rows, p.t_part, status, xmap, amap);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = 128 + size_t(p.max_tile_rows) * (R * 4 + ad::kOBlock * 2);
+  static bool configured_e = false;
+  if (!configured_e) {
+    cudaError_t e = cudaFuncSetAttribute(adapter_expand_kernel<R>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(128 + ad::kTileRows * (R * 4 + ad::kOBlock * 2)));
+    if (e != cudaSuccess) return e;
+    configured_e = true;
+  }
+  adapter_expand_kernel<R><<<dim3(p.num_tiles, d_out / ad::kOBlock), ad::kOBlock, smem, s>>>(
+      p.tiles, splits, p.num_rows, p.t_part, static_cast<const __nv_bfloat16*>(lora_b), scale,
+      static_cast<const __nv_bfloat16*>(ia3), static_cast<__nv_bfloat16*>(y), d_out,
+      p.max_tile_rows, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+int pie_fwd_adapter_workspace_bytes(int32_t num_lanes, const int32_t* row_indptr,
+                                    int32_t max_rank, size_t* bytes) {
+  if (!bytes) return set_last_error(PIE_EINVAL, "bytes is NULL");
+  if (!rank_built(max_rank)) return set_last_error(PIE_EUNSUPPORTED, "max_rank not in {0, 8, 16, 32, 64}");
+  int64_t nt = 0;
+  int rc = check_lanes(num_lanes, row_indptr, &nt);
+  if (rc != PIE_OK) return rc;
+  *bytes = ws_layout(nt, row_indptr[num_lanes], max_rank).total;
+  return PIE_OK;
+}
+
+int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
+                         const int32_t* adapter_of_lane, int32_t num_adapters, int32_t max_rank,
+                         void* dev_workspace, size_t ws_bytes, void* stream,
+                         pie_fwd_adapter_plan_t** out) {
+  using namespace pie;
+  if (!out) return set_last_error(PIE_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!rank_built(max_rank)) return set_last_error(PIE_EUNSUPPORTED, "max_rank not in {0, 8, 16, 32, 64}");
+  if (num_adapters < 0) return set_last_error(PIE_EINVAL, "num_adapters < 0");
+  int64_t nt_all = 0;
+  int rc = check_lanes(num_lanes, row_indptr, &nt_all);
+  if (rc != PIE_OK) return rc;
+  if (num_lanes > 0 && !adapter_of_lane) return set_last_error(PIE_EINVAL, "adapter_of_lane is NULL");
+  std::vector<ad::Tile> tiles;
+  for (int l = 0; l < num_lanes; ++l) {
+    const int a = adapter_of_lane[l];
+    if (a < -1 || a >= num_adapters)
+      return set_last_error(PIE_ERANGE, "adapter id outside [-1, num_adapters)");
+    if (a < 0) continue;
+    for (int r0 = row_indptr[l]; r0 < row_indptr[l + 1]; r0 += ad::kTileRows)
+      tiles.push_back({r0, std::min(ad::kTileRows, row_indptr[l + 1] - r0), a, 0});
+  }
+  if (tiles.size() > size_t(INT32_MAX)) return set_last_error(PIE_ERANGE, "too many tiles");
+  // largest tiles first (the grid's tail is made of the short ones); tiles of
+  // one adapter next to each other so that its A and B are read while in L2
+  std::stable_sort(tiles.begin(), tiles.end(), [](const ad::Tile& u, const ad::Tile& v) {
+    return u.n != v.n ? u.n > v.n : u.adapter < v.adapter;
+  });
+  const int N = row_indptr[num_lanes];
+  const WsLayout Y = ws_layout(nt_all, N, max_rank);
+  if (ws_bytes < Y.total || (Y.total > 0 && !dev_workspace))
+    return set_last_error(PIE_ENOSPACE, "workspace smaller than pie_fwd_adapter_workspace_bytes()");
+  if (reinterpret_cast<uintptr_t>(dev_workspace) % 256 != 0)
+    return set_last_error(PIE_EINVAL, "workspace must be 256-byte aligned");
+
+  const size_t copy = tiles.size() * sizeof(ad::Tile);
+  int err = PIE_OK;
+  PinnedBlock* blk = pinned_acquire(std::max<size_t>(copy, 1), &err);
+  if (!blk) return err;
+  if (copy) std::memcpy(blk->ptr, tiles.data(), copy);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (copy && cudaMemcpyAsync(static_cast<char*>(dev_workspace) + Y.tiles, blk->ptr, copy,
+                              cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    pinned_release(blk);
+    return set_last_error(PIE_ECUDA, std::string("adapter plan upload failed: ") +
+                                         cudaGetErrorString(cudaGetLastError()));
+  }
+  if (cudaEventRecord(blk->ev, s) != cudaSuccess)
+    return set_last_error(PIE_ECUDA, "cudaEventRecord failed after the adapter plan upload");
+
+  pie_fwd_adapter_plan_t* p = new pie_fwd_adapter_plan_t;
+  p->num_lanes = num_lanes;
+  p->num_rows = N;
+  p->num_adapters = num_adapters;
+  p->max_rank = max_rank;
+  p->num_tiles = int32_t(tiles.size());
+  p->max_tile_rows = 0;
+  for (const ad::Tile& t : tiles) p->max_tile_rows = std::max(p->max_tile_rows, t.n);
+  p->tiles = reinterpret_cast<ad::Tile*>(static_cast<char*>(dev_workspace) + Y.tiles);
+  p->t_part = reinterpret_cast<float*>(static_cast<char*>(dev_workspace) + Y.t_part);
+  p->staging = blk;
+  *out = p;
+  return PIE_OK;
+}
+
+int32_t pie_fwd_adapter_plan_num_tiles(const pie_fwd_adapter_plan_t* plan) {
+  return plan ? plan->num_tiles : -1;
+}
+
+int pie_fwd_adapter_apply(const pie_fwd_adapter_plan_t* plan, int32_t dtype, int32_t d_in,
+                          int32_t d_out, int32_t rank, const void* x, void* y, const void* lora_a,
+                          const void* lora_b, const float* scale, const void* ia3,
+                          uint32_t* status, void* stream) {
+  using namespace pie;
+  if (!plan) return set_last_error(PIE_EINVAL, "plan is NULL");
+  if (dtype != PIE_BF16) return set_last_error(PIE_EUNSUPPORTED, "adapters are built for bf16");
+  if (!rank_built(rank)) return set_last_error(PIE_EUNSUPPORTED, "rank not in {0, 8, 16, 32, 64}");
+  if (rank > plan->max_rank) return set_last_error(PIE_ERANGE, "rank above the plan's max_rank");
+  if (d_in <= 0 || d_in % ad::kChunk != 0)
+    return set_last_error(PIE_EUNSUPPORTED, "d_in must be a positive multiple of 64");
+  if (d_out <= 0 || d_out % ad::kOBlock != 0)
+    return set_last_error(PIE_EUNSUPPORTED, "d_out must be a positive multiple of 256");
+  if (plan->num_tiles == 0 || (rank == 0 && !ia3)) return PIE_OK;
+  if (!y) return set_last_error(PIE_EINVAL, "y is NULL");
+  if (rank > 0 && (!x || !lora_a || !lora_b || !scale))
+    return set_last_error(PIE_EINVAL, "x, lora_a, lora_b and scale are required when rank > 0");
+  auto misaligned = [](const void* q) { return q && reinterpret_cast<uintptr_t>(q) % 16 != 0; };
+  if (misaligned(x) || misaligned(y) || misaligned(lora_a) || misaligned(lora_b))
+    return set_last_error(PIE_EINVAL, "x, y, lora_a and lora_b must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ia3) % 2 != 0)
+    return set_last_error(PIE_EINVAL, "ia3 must be 2-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (rank) {
+    case 0: e = launch_adapter<0>(*plan, d_in, d_out, x, y, lora_a, lora_b, scale, ia3, status, s); break;
+    case 8: e = launch_adapter<8>(*plan, d_in, d_out, x, y, lora_a, lora_b, scale, ia3, status, s); break;
+    case 16: e = launch_adapter<16>(*plan, d_in, d_out, x, y, lora_a, lora_b, scale, ia3, status, s); break;
+    case 32: e = launch_adapter<32>(*plan, d_in, d_out, x, y, lora_a, lora_b, scale, ia3, status, s); break;
+    default: e = launch_adapter<64>(*plan, d_in, d_out, x, y, lora_a, lora_b, scale, ia3, status, s); break;
+  }
+  if (e != cudaSuccess)
+    return set_last_error(PIE_ECUDA, std::string("adapter launch failed: ") + cudaGetErrorString(e));
+  return PIE_OK;
+}
+
+void pie_fwd_adapter_plan_destroy(pie_fwd_adapter_plan_t* plan) {
+  if (!plan) return;
+  pie::pinned_release(plan->staging);
+  delete plan;
+}
+
+}  // extern "C"

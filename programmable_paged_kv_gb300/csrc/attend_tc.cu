@@ -41,11 +41,8 @@
 // (max, sum, unnormalised output) for the combine step.  Every wait is
 // bounded in time.
 
-#include <cuda.h>
-
-#include <mutex>
-
 #include "common.cuh"
+#include "tc_util.cuh"
 #include "tmem128.cuh"
 
 namespace pie {
@@ -90,60 +87,6 @@ template <int BN>
 __device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(BN) * (2 * t + b); }
 __device__ __forceinline__ uint32_t o_col(int t) { return 256u + 128u * t; }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (start address, leading
-// and stride byte offsets in 16-byte units, descriptor version 1, layout
-// type 2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t sdesc(const void* p, uint32_t lbo, uint32_t sbo) {
-  const uint32_t a = smem_u32(p);
-  uint64_t d = uint64_t((a >> 4) & 0x3FFFu);
-  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-  d |= uint64_t(1) << 46;
-  d |= uint64_t(2) << 61;
-  return d;
-}
-
-// Instruction descriptor for kind::f16: bf16 A and B, fp32 accumulator,
-// A K-major, B K-major (false) or MN-major (true), N >> 3 and M >> 4.
-__host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D (TMEM) (+)= A (shared memory) * B (shared memory)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
-
-// D (TMEM) (+)= A (TMEM) * B (shared memory)
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* f) {
   uint32_t r[128];
   asm volatile(PIE_TMEM_LD128_ASM : PIE_TMEM_LD_OUTS : "r"(taddr) : "memory");
@@ -183,64 +126,6 @@ template <int BN>
 __device__ __forceinline__ void store_p(uint32_t taddr, const uint32_t* r) {
   if constexpr (BN == 128) tmem_st64(taddr, r);
   else tmem_st32(taddr, r);
-}
-
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                       uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                       int w, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Four 128-byte rows (one box of the map each, at rows y0..y3, column x) into
-// four consecutive 128-byte rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int y0,
-                                            int y1, int y2, int y3, uint64_t* bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-struct Out {
-  __nv_bfloat16* out_readout;
-  float* lse_readout;
-  __nv_bfloat16* out_all;
-  float* lse_all;
-};
-
-// Row output: bf16 o / l to out_all and to every readout position of the row.
-__device__ __forceinline__ void write_row(const DevMeta& m, const Out& out, int Hq, int row,
-                                          int head, const uint4* packed, float lse) {
-  constexpr int D = 128;
-  if (out.out_all) {
-    uint4* dst = reinterpret_cast<uint4*>(out.out_all + (int64_t(row) * Hq + head) * D);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) dst[c] = packed[c];
-  }
-  if (out.lse_all) out.lse_all[int64_t(row) * Hq + head] = lse;
-  for (int r = m.ro_indptr[row]; r < m.ro_indptr[row + 1]; ++r) {
-    const int jj = m.ro_idx[r];
-    if (out.out_readout) {
-      uint4* dst = reinterpret_cast<uint4*>(out.out_readout + (int64_t(jj) * Hq + head) * D);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) dst[c] = packed[c];
-    }
-    if (out.lse_readout) out.lse_readout[int64_t(jj) * Hq + head] = lse;
-  }
 }
 
 }  // namespace tc
@@ -660,35 +545,6 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
 // ---------------------------------------------------------------------------
 // host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-static bool make_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                     const cuuint64_t* strides, const cuuint32_t* box) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NT>
 static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words, tc::Out out,
                              uint32_t* status, const CUtensorMap& qm, const CUtensorMap& km,
@@ -720,14 +576,14 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
     const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(G), cuuint64_t(Hkv), cuuint64_t(p.N)};
     const cuuint64_t str[3] = {cuuint64_t(D) * 2, cuuint64_t(G) * D * 2, cuuint64_t(Hq) * D * 2};
     const cuuint32_t box[4] = {64, cuuint32_t(G), 1, cuuint32_t(kTcTileQueries / G)};
-    if (!make_map(&qm, q_rot, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&qm, q_rot, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(p.num_pool_pages) * Hkv * P};
     const cuuint64_t str[1] = {cuuint64_t(D) * 2};
     const cuuint32_t box[2] = {64, cuuint32_t(P)};
-    if (!make_map(&km, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&vm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&km, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&vm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   // one-row boxes for the slot-granular gathers of masked passes
   CUtensorMap kgm = km, vgm = vm;
@@ -735,8 +591,8 @@ cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const v
     const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(p.num_pool_pages) * Hkv * P};
     const cuuint64_t str[1] = {cuuint64_t(D) * 2};
     const cuuint32_t box[2] = {64, 1};
-    if (!make_map(&kgm, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&vgm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&kgm, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&vgm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   tc::Out out{static_cast<__nv_bfloat16*>(out_readout), lse_readout,
               static_cast<__nv_bfloat16*>(out_all), lse_all};

@@ -118,7 +118,17 @@ struct DevMeta {
   int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
 };
 
-struct PinnedBlock;
+// Pinned host staging block: metadata uploads copy from pinned memory so that
+// they are truly asynchronous.  A released block returns to a process-wide
+// pool and is handed out again only once the event recorded after its copy
+// has completed.
+struct PinnedBlock {
+  void* ptr = nullptr;
+  size_t cap = 0;
+  cudaEvent_t ev = nullptr;
+};
+PinnedBlock* pinned_acquire(size_t bytes, int* err);
+void pinned_release(PinnedBlock* b);
 
 }  // namespace pie
 

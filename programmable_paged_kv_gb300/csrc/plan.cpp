@@ -43,16 +43,10 @@ int set_last_error(int code, const std::string& msg) { return fail(code, msg); }
 // that the copy is truly asynchronous; a block returns to the pool when its
 // plan is destroyed and is reused only after its copy event has completed.
 // ---------------------------------------------------------------------------
-struct PinnedBlock {
-  void* ptr = nullptr;
-  size_t cap = 0;
-  cudaEvent_t ev = nullptr;
-};
-
 static std::mutex g_pool_mu;
 static std::vector<PinnedBlock*> g_pool_free;
 
-static PinnedBlock* pinned_acquire(size_t bytes, int* err) {
+PinnedBlock* pinned_acquire(size_t bytes, int* err) {
   *err = PIE_OK;
   {
     std::lock_guard<std::mutex> lk(g_pool_mu);
@@ -70,20 +64,20 @@ static PinnedBlock* pinned_acquire(size_t bytes, int* err) {
   PinnedBlock* b = new PinnedBlock;
   if (cudaMallocHost(&b->ptr, cap) != cudaSuccess) {
     delete b;
-    *err = fail(PIE_ECUDA, "cudaMallocHost failed for plan staging");
+    *err = fail(PIE_ECUDA, "cudaMallocHost failed for metadata staging");
     return nullptr;
   }
   if (cudaEventCreateWithFlags(&b->ev, cudaEventDisableTiming) != cudaSuccess) {
     cudaFreeHost(b->ptr);
     delete b;
-    *err = fail(PIE_ECUDA, "cudaEventCreate failed for plan staging");
+    *err = fail(PIE_ECUDA, "cudaEventCreate failed for metadata staging");
     return nullptr;
   }
   b->cap = cap;
   return b;
 }
 
-static void pinned_release(PinnedBlock* b) {
+void pinned_release(PinnedBlock* b) {
   if (!b) return;
   std::lock_guard<std::mutex> lk(g_pool_mu);
   g_pool_free.push_back(b);
@@ -463,7 +457,7 @@ extern "C" {
 
 const char* pie_fwd_last_error(void) { return g_last_error.c_str(); }
 
-int pie_fwd_abi_version(void) { return 101; }
+int pie_fwd_abi_version(void) { return 102; }
 
 static thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 

@@ -34,7 +34,7 @@ def test_build_can_be_called_again(lib):
 
 
 def test_abi_version(lib):
-    assert lib.pie_fwd_abi_version() == 101
+    assert lib.pie_fwd_abi_version() == 102
 
 
 def test_timing_events_need_both_or_neither(lib):
@@ -150,3 +150,34 @@ def test_readout_refuses_bad_calls_before_any_launch(lib):
                                     None) == abi.PIE_EINVAL
     assert lib.pie_fwd_readout_topk(p, abi.PIE_F32, 2, 1000, 1000, 8, p, p, None, None, p, 16,
                                     None) == abi.PIE_ENOSPACE
+
+
+def test_adapter_plan_refuses_bad_lanes_before_any_cuda_call(lib):
+    i32 = lambda a: np.ascontiguousarray(a, dtype=np.int32)
+    n = C.c_size_t(0)
+    ws = lib.pie_fwd_adapter_workspace_bytes
+    ri = i32([0, 1, 130, 130, 131])
+    assert ws(4, ri.ctypes.data, 16, C.byref(n)) == abi.PIE_OK
+    # tiles: 1 + 2 + 0 + 1 rows-of-128 blocks, 16 bytes each (256-aligned),
+    # then 8 ranges x 131 rows x 16 fp32 partial sums
+    assert n.value == 256 + ((8 * 131 * 16 * 4 + 255) // 256) * 256
+    assert ws(4, ri.ctypes.data, 12, C.byref(n)) == abi.PIE_EUNSUPPORTED   # rank not built
+    assert ws(2, i32([0, 3, 2]).ctypes.data, 16, C.byref(n)) == abi.PIE_EINVAL   # not monotone
+    assert ws(1, i32([1, 3]).ctypes.data, 16, C.byref(n)) == abi.PIE_EINVAL      # indptr[0] != 0
+    h = C.c_void_p()
+    plan = lib.pie_fwd_adapter_plan
+    ad = i32([0, 1, -1, 2])
+    buf = C.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
+    assert plan(4, ri.ctypes.data, i32([0, 3, -1, 2]).ctypes.data, 3, 16, buf, 1 << 30, None,
+                C.byref(h)) == abi.PIE_ERANGE                                   # adapter 3 of 3
+    assert plan(4, ri.ctypes.data, i32([0, -2, -1, 2]).ctypes.data, 3, 16, buf, 1 << 30, None,
+                C.byref(h)) == abi.PIE_ERANGE                                   # adapter -2
+    assert plan(4, ri.ctypes.data, ad.ctypes.data, 3, 16, buf, 16, None,
+                C.byref(h)) == abi.PIE_ENOSPACE
+    assert plan(4, ri.ctypes.data, ad.ctypes.data, 3, 16, C.c_void_p((1 << 20) + 16), 1 << 30,
+                None, C.byref(h)) == abi.PIE_EINVAL                             # alignment
+    assert plan(4, ri.ctypes.data, None, 3, 16, buf, 1 << 30, None, C.byref(h)) == abi.PIE_EINVAL
+    assert h.value is None
+    apply = lib.pie_fwd_adapter_apply
+    assert apply(None, abi.PIE_BF16, 64, 256, 16, buf, buf, buf, buf, buf, None, None,
+                 None) == abi.PIE_EINVAL

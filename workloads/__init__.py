@@ -486,6 +486,58 @@ def readout_logits(seed: int, rows: int, vocab: int, spikes: int = 8,
     return x
 
 
+@dataclasses.dataclass
+class AdapterSite:
+    """Inputs of the adapters at one projection site: the lanes' rows and
+    adapter ids, x [N, d_in] and y [N, d_out] (bf16 bit patterns), the
+    adapters' A [n_ad, r, d_in], B [n_ad, d_out, r] (bf16 bits), scale
+    float32 [n_ad] and IA3 vectors [n_ad, d_out] (bf16 bits) or None."""
+    row_indptr: np.ndarray
+    adapter_of_lane: np.ndarray
+    x: np.ndarray
+    y: np.ndarray
+    lora_a: Optional[np.ndarray]
+    lora_b: Optional[np.ndarray]
+    scale: np.ndarray
+    ia3: Optional[np.ndarray]
+    rank: int
+    recipe: str
+
+
+def adapter_site(seed: int, rows_per_lane, n_adapters: int = 16, d_in: int = 4096,
+                 d_out: int = 4096, rank: int = 16, ia3: bool = True,
+                 none_every: int = 8) -> AdapterSite:
+    """Synthetic per-lane adapters (no trained weights): every lane draws an
+    adapter uniformly from n_adapters, except every `none_every`-th lane,
+    which has none (-1); x, y ~ N(0, 1); A ~ N(0, 1/d_in) and B ~ N(0, 1/r)
+    so that B (A x) is of the order of y; scale = 2 (LoRA alpha = 2 r);
+    IA3 entries ~ U[0.5, 1.5].  rank 0 gives an IA3-only site."""
+    rows = np.asarray(rows_per_lane, dtype=np.int64).reshape(-1)
+    L = rows.size
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 11]))
+    row_indptr = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    N = int(row_indptr[-1])
+    ad = rng.integers(0, max(n_adapters, 1), size=L).astype(np.int32)
+    if none_every > 0:
+        ad[none_every - 1::none_every] = -1
+    if n_adapters == 0:
+        ad[:] = -1
+    f32 = np.float32
+    x = f32_to_bf16_bits(rng.standard_normal((N, d_in), dtype=f32))
+    y = f32_to_bf16_bits(rng.standard_normal((N, d_out), dtype=f32))
+    a = b = None
+    if rank > 0:
+        a = f32_to_bf16_bits(rng.standard_normal((n_adapters, rank, d_in), dtype=f32) / f32(np.sqrt(d_in)))
+        b = f32_to_bf16_bits(rng.standard_normal((n_adapters, d_out, rank), dtype=f32) / f32(np.sqrt(rank)))
+    scale = np.full(n_adapters, 2.0, dtype=f32)
+    s = f32_to_bf16_bits(rng.uniform(0.5, 1.5, size=(n_adapters, d_out)).astype(f32)) if ia3 else None
+    recipe = (f"{L} lanes, {N} rows, adapter per lane ~ U{{0..{n_adapters - 1}}} (every "
+              f"{none_every}th lane none), d_in {d_in}, d_out {d_out}, rank {rank}, "
+              f"x, y ~ N(0,1), A ~ N(0,1/d_in), B ~ N(0,1/r), scale 2, "
+              f"IA3 {'~ U[0.5,1.5]' if ia3 else 'off'}, bf16")
+    return AdapterSite(row_indptr, ad, x, y, a, b, scale, s, rank, recipe)
+
+
 FULL = {
     "tiny": lambda seed=0: tiny(seed),
     "decode_batch": lambda seed=0: decode_batch(seed),
