@@ -43,9 +43,10 @@ namespace ad {
 
 constexpr int kTileRows = 128;   // rows per tile (the MMA's largest N used here)
 constexpr int kChunk = 64;       // d_in columns per ring stage: one 128-byte swizzle row
-constexpr int kStages = 4;       // shrink ring depth
+constexpr int kStages = 6;       // shrink ring depth
 constexpr int kMaxSplits = 8;    // d_in ranges per tile (partial sums kept per range)
-constexpr int kOBlock = 256;     // output columns per expand CTA (one per thread)
+constexpr int kOBlock = 256;     // output columns per expand CTA
+constexpr int kExpandThreads = 256;  // one output column (TMEM lane) per thread
 constexpr int kGroupRows = 16;   // y rows per arrival barrier in the expand
 constexpr int kMaxGroups = kTileRows / kGroupRows;
 constexpr int kShrinkCtasPerSm = 3;
@@ -56,17 +57,25 @@ struct alignas(16) Tile {
   int32_t row0, n, adapter, pad;
 };
 
-template <int R>
-struct __align__(1024) ShrinkSmem {
-  uint8_t a[kStages][R * 128];           // A_a chunk: R rows x 64 columns (bf16)
-  uint8_t x[kStages][kTileRows * 128];   // x chunk: up to 128 rows x 64 columns
+// Shrink shared memory, laid out for the plan's largest tile (nmax rows):
+// a 1 KB header, then kStages A_a chunks (R rows x 64 columns, bf16), then
+// kStages x chunks (nmax rows x 64 columns), then a guard so that the M=128
+// operand read from the last A stage (128 rows) stays inside the allocation.
+struct ShrinkHdr {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t done;
   uint32_t tmem_base;
+  int last;  // this CTA is the tile's last d_in range to finish
 };
-// The M=128 operand read from the last A stage stays inside the structure.
-static_assert(sizeof(ShrinkSmem<8>) >= (kStages - 1) * 8 * 128 + 128 * 128, "A operand overrun");
+static_assert(sizeof(ShrinkHdr) <= 1024, "shrink header");
+
+__host__ __device__ constexpr size_t shrink_smem_bytes(int R, int nmax) {
+  return 1024 + size_t(kStages) * R * 128 + size_t(kStages) * nmax * 128 +
+         (size_t(kStages) * nmax * 128 + size_t(R) * 128 < 128 * 128
+              ? 128 * 128 - size_t(kStages) * nmax * 128 - size_t(R) * 128
+              : 0);
+}
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
@@ -95,6 +104,15 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
                "r"(smem_u32(src)), "r"(bytes)
                : "memory");
 }
+// 2-D tensor store shared -> global (the map's box at {x, y}) in the calling
+// thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
+                                             const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+      "r"(x), "r"(y), "r"(smem_u32(src))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -104,17 +122,25 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 }  // namespace ad
 
-// t_part[split][row][k] = sum over the split's d_in range of A_a[k][i] x[row][i]
+// t[row][k] = c_a sum_i A_a[k][i] x[row][i] for the tile's rows.  With d_in cut
+// into `splits` ranges, each CTA stores its range's sums to t_part[split] and
+// the last CTA of the tile to finish adds them up in range order (the result
+// does not depend on which CTA finishes last) and resets the tile's counter.
 template <int R>
 __global__ void __launch_bounds__(128) adapter_shrink_kernel(
-    const ad::Tile* __restrict__ tiles, int chunks_per_split, int num_chunks, int num_rows,
-    float* __restrict__ t_part, uint32_t* status, const __grid_constant__ CUtensorMap xmap,
+    const ad::Tile* __restrict__ tiles, int splits, int chunks_per_split, int num_chunks,
+    int num_rows, const float* __restrict__ scale, float* __restrict__ t_part,
+    float* __restrict__ t_final, int* __restrict__ counters, uint32_t* status,
+    int nmax, uint32_t tmem_cols, const __grid_constant__ CUtensorMap xmap,
     const __grid_constant__ CUtensorMap amap) {
   using namespace ad;
   using namespace tc;
-  extern __shared__ uint8_t raw[];
-  ShrinkSmem<R>& S = *reinterpret_cast<ShrinkSmem<R>*>(
-      (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ uint8_t raw_[];
+  uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw_) + 1023) &
+                                            ~uintptr_t(1023));
+  ShrinkHdr& S = *reinterpret_cast<ShrinkHdr*>(raw);
+  uint8_t* a_st = raw + 1024;                       // stage st at a_st + st * R * 128
+  uint8_t* x_st = a_st + size_t(kStages) * R * 128;  // stage st at x_st + st * nmax * 128
   const Tile tile = tiles[blockIdx.x];
   const int split = blockIdx.y;
   const int c0 = split * chunks_per_split;
@@ -133,7 +159,7 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&S.tmem_base)),
-                 "r"(kTileRows)
+                 "r"(tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -162,8 +188,9 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
       __syncwarp();
       const int cx = (c0 + i) * kChunk;
       if (lane < N / 16)
-        tma_2d(S.x[st] + lane * 2048, &xmap, cx, tile.row0 + lane * 16, &S.full[st], pol_x);
-      if (lane == 31) tma_2d(S.a[st], &amap, cx, tile.adapter * R, &S.full[st], pol_a);
+        tma_2d(x_st + size_t(st) * nmax * 128 + lane * 2048, &xmap, cx, tile.row0 + lane * 16,
+               &S.full[st], pol_x);
+      if (lane == 31) tma_2d(a_st + st * R * 128, &amap, cx, tile.adapter * R, &S.full[st], pol_a);
       issued = i + 1;
     }
     // copies still in flight must land before the CTA may exit
@@ -182,7 +209,8 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
           break;
         }
         fence_after();
-        const uint64_t da = sdesc(S.a[st], 16, 1024), dx = sdesc(S.x[st], 16, 1024);
+        const uint64_t da = sdesc(a_st + st * R * 128, 16, 1024);
+        const uint64_t dx = sdesc(x_st + size_t(st) * nmax * 128, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tmem, da + 2 * k, dx + 2 * k, id, (i > 0 || k > 0) ? 1u : 0u);
@@ -202,16 +230,50 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
     } else {
       fence_after();
       const int k = warp * 32 + lane;
-      float* dst = t_part + (int64_t(split) * num_rows + tile.row0) * R + k;
+      const float c = splits == 1 ? scale[tile.adapter] : 1.f;
+      float* dst = (splits == 1 ? t_final + int64_t(tile.row0) * R
+                                : t_part + (int64_t(split) * num_rows + tile.row0) * R) + k;
       for (int cb = 0; cb < N; cb += 16) {
         float v[16];
         tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(cb), v);
         if (k < R) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
-            if (cb + jj < tile.n) dst[int64_t(cb + jj) * R] = v[jj];
+            if (cb + jj < tile.n) dst[int64_t(cb + jj) * R] = v[jj] * c;
         }
       }
+      __threadfence();  // this range's sums are visible before the counter moves
+    }
+  }
+  if (splits > 1) {
+    __syncthreads();
+    if (threadIdx.x == 0) S.last = atomicAdd(&counters[blockIdx.x], 1) == splits - 1;
+    __syncthreads();
+    if (S.last) {
+      __threadfence();
+      const float c = scale[tile.adapter];
+      const int cnt = tile.n * R;
+      const float* src0 = t_part + int64_t(tile.row0) * R;
+      constexpr int kBatch = 4;  // elements per thread whose loads are in flight together
+      for (int e0 = threadIdx.x; e0 < cnt; e0 += 128 * kBatch) {
+        float p[kBatch][kMaxSplits];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + 128 * b;
+#pragma unroll
+          for (int q = 0; q < kMaxSplits; ++q)
+            p[b][q] = (q < splits && e < cnt) ? __ldcg(src0 + int64_t(q) * num_rows * R + e) : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + 128 * b;
+          float acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxSplits; ++q) acc += p[b][q];
+          if (e < cnt) t_final[int64_t(tile.row0) * R + e] = acc * c;
+        }
+      }
+      if (threadIdx.x == 0) counters[blockIdx.x] = 0;  // ready for the next apply
     }
   }
   if (bad) set_status(status, PIE_STATUS_TIMEOUT);
@@ -220,88 +282,207 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTileRows)
+                 "r"(tmem_cols)
                  : "memory");
   }
 }
 
-// y[row][o] = (y[row][o] + c_a sum_k B_a[o][k] t[row][k]) * s_a[o] for the
-// tile's rows and 256 columns
+namespace ad {
+
+// Expand operand geometry for rank R: t is split into bf16 parts hi + lo (t
+// to about 16 bits); the MMA's K runs over [hi | lo], each part padded to a
+// multiple of 16, in 128-byte swizzled K halves (one half up to rank 32).
 template <int R>
-__global__ void __launch_bounds__(ad::kOBlock) adapter_expand_kernel(
-    const ad::Tile* __restrict__ tiles, int splits, int num_rows, const float* __restrict__ t_part,
-    const __nv_bfloat16* __restrict__ lora_b, const float* __restrict__ scale,
-    const __nv_bfloat16* __restrict__ ia3, __nv_bfloat16* __restrict__ y, int d_out,
-    int max_rows, uint32_t* status) {
+struct ExpandCfg {
+  static constexpr int KP = R < 16 ? 16 : R;   // one part, padded to a K step
+  static constexpr int H = (2 * KP + 63) / 64;  // 128-byte K halves
+  static constexpr int KSTEPS = 2 * KP / 16;    // K=16 MMAs per 128 output columns
+};
+
+// Byte offset of element (row, k) in a K-major operand of `rows` rows laid out
+// as H halves of 64 K columns, 128-byte swizzle (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int k) {
+  const int half = k >> 6, c = (k & 63) >> 3;
+  return uint32_t(half * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                  ((c ^ (row & 7)) << 4) + ((k & 7) << 1));
+}
+
+}  // namespace ad
+
+// y[row][o] = (y[row][o] + sum_k B_a[o][k] t[row][k]) * s_a[o] for the tile's
+// rows and 256 output columns (t already scaled by c_a).  B_a t runs on the
+// tensor cores: two M=128 tiles of output columns, N = the tile's rows rounded
+// up to 16, K over [t_hi | t_lo]; each thread then owns one output column of
+// one M tile (its TMEM lane) and streams the tile's y rows through shared
+// memory, 16 rows (one tcgen05.ld) at a time.
+template <int R>
+__global__ void __launch_bounds__(ad::kExpandThreads) adapter_expand_kernel(
+    const ad::Tile* __restrict__ tiles, const float* __restrict__ t_final,
+    const __nv_bfloat16* __restrict__ lora_b, const __nv_bfloat16* __restrict__ ia3,
+    __nv_bfloat16* __restrict__ y, int d_out, int max_rows, uint32_t tmem_cols,
+    uint32_t* status, const __grid_constant__ CUtensorMap ymap) {
   using namespace ad;
-  extern __shared__ __align__(128) uint8_t raw[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(raw);
-  float* ts = reinterpret_cast<float*>(raw + 128);  // [max_rows][R]
-  __nv_bfloat16* ys =
-      reinterpret_cast<__nv_bfloat16*>(raw + 128 + size_t(max_rows) * R * 4);  // [max_rows][256]
+  using namespace tc;
+  using C = ExpandCfg<R>;
+  extern __shared__ uint8_t raw_[];
+  uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw_) + 1023) &
+                                            ~uintptr_t(1023));
+  const int nmax = (max_rows + 15) & ~15;
+  const size_t ys_bytes = (size_t(max_rows) * kOBlock * 2 + 1023) & ~size_t(1023);
+  const size_t a_bytes = R > 0 ? size_t(2) * C::H * 128 * 128 : 0;
+  const size_t b_bytes = R > 0 ? size_t(C::H) * nmax * 128 : 0;
+  __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(raw);  // [max_rows][256]
+  uint8_t* a_op = raw + ys_bytes;                              // [2][H][128 rows][128 B]
+  uint8_t* b_op = a_op + a_bytes;                              // [H][nmax rows][128 B]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_op + b_bytes); // [kMaxGroups] y groups
+  uint64_t* mma_done = bar + kMaxGroups;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
   const Tile tile = tiles[blockIdx.x];
   const int o0 = blockIdx.y * kOBlock;
   const int n = tile.n, a = tile.adapter;
+  const int N = (n + 15) & ~15;
   const int ngroups = (n + kGroupRows - 1) / kGroupRows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int g = 0; g < ngroups; ++g) mbar_init(&bar[g], 1);
+    mbar_init(mma_done, 1);
     fence_barrier_init();
   }
+  if constexpr (R > 0) {
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(tmem_cols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+  }
+  fence_before();
   __syncthreads();
+  fence_after();
+
+  // full groups of 16 rows move as one 2-D box each way; the rows of a last,
+  // partial group one by one (a box would also cover the next lane's rows)
   __nv_bfloat16* yt = y + int64_t(tile.row0) * d_out + o0;
+  const int nfull = n / kGroupRows;
   if (warp == 0) {
     if (lane < ngroups)
       mbar_arrive_expect_tx(&bar[lane],
                             uint32_t(min(kGroupRows, n - lane * kGroupRows)) * kOBlock * 2u);
     __syncwarp();
-    for (int j = lane; j < n; j += 32)
+    if (lane < nfull)
+      tma_2d(ys + lane * kGroupRows * kOBlock, &ymap, o0, tile.row0 + lane * kGroupRows,
+             &bar[lane], policy_evict_first());
+    for (int j = nfull * kGroupRows + lane; j < n; j += 32)
       bulk_g2s(ys + j * kOBlock, yt + int64_t(j) * d_out, kOBlock * 2, &bar[j / kGroupRows]);
   }
 
-  const int o = o0 + tid;
-  float b[R > 0 ? R : 1];
-  if constexpr (R > 0) {
-    const float c = scale[a];
-    for (int e = tid; e < n * R; e += kOBlock) {
-      const float* src = t_part + int64_t(tile.row0) * R + e;
-      float acc = 0.f;
-      for (int s = 0; s < splits; ++s) acc += src[int64_t(s) * num_rows * R];
-      ts[e] = acc * c;
-    }
-    const uint4* bp = reinterpret_cast<const uint4*>(lora_b + (int64_t(a) * d_out + o) * R);
-#pragma unroll
-    for (int q = 0; q < R / 8; ++q) unpack16<__nv_bfloat16>(__ldg(bp + q), b + 8 * q);
-  }
-  const float s_o = ia3 ? __bfloat162float(ia3[int64_t(a) * d_out + o]) : 1.f;
-  __syncthreads();
-
+  // this thread's output column: M tile m = warp / 4, TMEM lane quarter q
+  const int m = warp >> 2, q = warp & 3;
+  const int ol = m * 128 + q * 32 + lane;
+  const float s_o = ia3 ? __bfloat162float(ia3[int64_t(a) * d_out + o0 + ol]) : 1.f;
+  uint32_t tmem = 0;
   bool bad = false;
-  for (int g = 0; g < ngroups; ++g) {
+
+  if constexpr (R > 0) {
+    // operands: A = B_a rows [o0, o0 + 256) as [hi copy | lo copy] of K, B = [t_hi | t_lo]
+    constexpr int CH = R / 8;  // 16-byte chunks of one row of B_a or of t
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < kOBlock * CH; i += kExpandThreads) {
+      const int row = i / CH, c = i % CH;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                                lora_b + (int64_t(a) * d_out + o0 + row) * R) + c);
+      uint8_t* base = a_op + (row >> 7) * (C::H * 128 * 128);
+      const int r = row & 127;
+      *reinterpret_cast<uint4*>(base + sw128_offset(128, r, 8 * c)) = v;
+      *reinterpret_cast<uint4*>(base + sw128_offset(128, r, C::KP + 8 * c)) = v;
+      if (R < C::KP) {  // zero K padding of both parts
+        *reinterpret_cast<uint4*>(base + sw128_offset(128, r, R + 8 * c)) = zero;
+        *reinterpret_cast<uint4*>(base + sw128_offset(128, r, C::KP + R + 8 * c)) = zero;
+      }
+    }
+    const float* tsrc = t_final + int64_t(tile.row0) * R;
+    for (int i = tid; i < n * CH; i += kExpandThreads) {
+      const int j = i / CH, c = i % CH;
+      const float4 f0 = __ldcg(reinterpret_cast<const float4*>(tsrc + j * R + 8 * c));
+      const float4 f1 = __ldcg(reinterpret_cast<const float4*>(tsrc + j * R + 8 * c + 4));
+      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(f[2 * e] - __low2float(h),
+                                                       f[2 * e + 1] - __high2float(h));
+        hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+      }
+      *reinterpret_cast<uint4*>(b_op + sw128_offset(nmax, j, 8 * c)) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(b_op + sw128_offset(nmax, j, C::KP + 8 * c)) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if (R < C::KP) {
+        *reinterpret_cast<uint4*>(b_op + sw128_offset(nmax, j, R + 8 * c)) = zero;
+        *reinterpret_cast<uint4*>(b_op + sw128_offset(nmax, j, C::KP + R + 8 * c)) = zero;
+      }
+    }
+    fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
+    fence_before();
+    __syncthreads();
+    fence_after();
+    tmem = *tmem_slot;
+    if (tid == 0) {
+      const uint32_t id = idesc(128, N, false);
+      const uint64_t db = sdesc(b_op, 16, 1024);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint64_t da = sdesc(a_op + mt * (C::H * 128 * 128), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < C::KSTEPS; ++ks) {
+          const uint64_t offa = uint64_t((ks >> 2) * ((128 * 128) >> 4) + (ks & 3) * 2);
+          const uint64_t offb = uint64_t((ks >> 2) * ((nmax * 128) >> 4) + (ks & 3) * 2);
+          mma_ss(tmem + uint32_t(mt * nmax), da + offa, db + offb, id, ks > 0 ? 1u : 0u);
+        }
+      }
+      commit(mma_done);
+    }
+    const bool ok = mbar_wait(mma_done, 0);
+    if (__syncthreads_or(!ok)) bad = true;
+    fence_after();
+  } else {
+    __syncthreads();
+  }
+
+  for (int g = 0; g < ngroups && !bad; ++g) {
     const bool ok = mbar_wait(&bar[g], 0);
     if (__syncthreads_or(!ok)) {
       bad = true;
       break;
     }
     const int j0 = g * kGroupRows, j1 = min(n, j0 + kGroupRows);
-    for (int j = j0; j < j1; ++j) {
-      float acc0 = 0.f, acc1 = 0.f;
-      if constexpr (R > 0) {
-        const float4* tj = reinterpret_cast<const float4*>(ts + j * R);
+    float d[16];
+    if constexpr (R > 0) {
+      tmem_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(m * nmax + j0), d);
+    } else {
 #pragma unroll
-        for (int q = 0; q < R / 4; ++q) {
-          const float4 t4 = tj[q];
-          ffma2(acc0, acc1, b[4 * q], b[4 * q + 1], t4.x, t4.y, acc0, acc1);
-          ffma2(acc0, acc1, b[4 * q + 2], b[4 * q + 3], t4.z, t4.w, acc0, acc1);
-        }
+      for (int jj = 0; jj < 16; ++jj) d[jj] = 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      if (j0 + jj < j1) {
+        __nv_bfloat16& yv = ys[(j0 + jj) * kOBlock + ol];
+        yv = __float2bfloat16_rn((__bfloat162float(yv) + d[jj]) * s_o);
       }
-      __nv_bfloat16& yv = ys[j * kOBlock + tid];
-      yv = __float2bfloat16_rn((__bfloat162float(yv) + (acc0 + acc1)) * s_o);
     }
     fence_proxy_async_smem();
     __syncthreads();
-    if (warp == 0 && lane < j1 - j0) {
+    if (g < nfull) {
+      if (tid == 0) {
+        tma_store_2d(&ymap, o0, tile.row0 + j0, ys + j0 * kOBlock);
+        bulk_commit();
+      }
+    } else if (warp == 0 && lane < j1 - j0) {
       const int j = j0 + lane;
       bulk_s2g(yt + int64_t(j) * d_out, ys + j * kOBlock, kOBlock * 2);
       bulk_commit();
@@ -311,6 +492,16 @@ __global__ void __launch_bounds__(ad::kOBlock) adapter_expand_kernel(
   if (bad && tid == 0) {
     set_status(status, PIE_STATUS_TIMEOUT);
     for (int g = 0; g < ngroups; ++g) mbar_wait(&bar[g], 0);  // copies still in flight land first
+  }
+  if constexpr (R > 0) {
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(tmem_cols)
+                   : "memory");
+    }
   }
 }
 
@@ -323,7 +514,9 @@ struct pie_fwd_adapter_plan {
   int32_t num_lanes, num_rows, num_adapters, max_rank;
   int32_t num_tiles, max_tile_rows;
   pie::ad::Tile* tiles;  // device, in the workspace
-  float* t_part;         // device scratch: [kMaxSplits][num_rows][max_rank]
+  int* counters;         // device: finished d_in ranges per tile (zero between applies)
+  float* t_part;         // device scratch: [kMaxSplits][num_rows][rank] partial sums
+  float* t_final;        // device scratch: [num_rows][rank], c_a A_a x
   pie::PinnedBlock* staging;
 };
 
@@ -348,16 +541,20 @@ int check_lanes(int32_t num_lanes, const int32_t* row_indptr, int64_t* num_tiles
 
 bool rank_built(int r) { return r == 0 || r == 8 || r == 16 || r == 32 || r == 64; }
 
+// workspace: tiles | counters (both uploaded, counters as zeros) | t_part | t_final
 struct WsLayout {
-  size_t tiles = 0, t_part = 0, total = 0;
+  size_t tiles = 0, counters = 0, t_part = 0, t_final = 0, total = 0;
 };
 
 WsLayout ws_layout(int64_t num_tiles, int64_t num_rows, int max_rank) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   WsLayout Y;
   Y.tiles = 0;
-  Y.t_part = up(size_t(num_tiles) * sizeof(pie::ad::Tile));
-  Y.total = Y.t_part + up(size_t(pie::ad::kMaxSplits) * size_t(num_rows) * size_t(max_rank) * 4);
+  Y.counters = up(size_t(num_tiles) * sizeof(pie::ad::Tile));
+  Y.t_part = Y.counters + up(size_t(num_tiles) * 4);
+  Y.t_final =
+      Y.t_part + up(size_t(pie::ad::kMaxSplits) * size_t(num_rows) * size_t(max_rank) * 4);
+  Y.total = Y.t_final + up(size_t(num_rows) * size_t(max_rank) * 4);
   return Y;
 }
 
@@ -390,32 +587,59 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
       const cuuint32_t box[2] = {ad::kChunk, cuuint32_t(R)};
       if (!tc::make_map(&amap, lora_a, 2, dims, str, box)) return cudaErrorInvalidValue;
     }
-    const size_t smem = sizeof(ad::ShrinkSmem<R>) + 1024;
+    const int nmax = (p.max_tile_rows + 15) & ~15;
+    const size_t smem = 1024 + ad::shrink_smem_bytes(R, nmax);  // + alignment slack
     static bool configured = false;
     if (!configured) {
       cudaError_t e = cudaFuncSetAttribute(adapter_shrink_kernel<R>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(1024 + ad::shrink_smem_bytes(R, ad::kTileRows)));
       if (e != cudaSuccess) return e;
       configured = true;
     }
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < uint32_t(nmax)) tmem_cols <<= 1;
     adapter_shrink_kernel<R><<<dim3(p.num_tiles, splits), 128, smem, s>>>(
-        p.tiles, cps, num_chunks, p.num_rows, p.t_part, status, xmap, amap);
+        p.tiles, splits, cps, num_chunks, p.num_rows, scale, p.t_part, p.t_final, p.counters,
+        status, nmax, tmem_cols, xmap, amap);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const size_t smem = 128 + size_t(p.max_tile_rows) * (R * 4 + ad::kOBlock * 2);
+  // shared memory: 1 KB alignment slack, y rows, the two MMA operands, barriers
+  using EC = ad::ExpandCfg<R>;
+  auto expand_smem = [](int rows) {
+    const size_t nmax = size_t((rows + 15) & ~15);
+    const size_t ys = (size_t(rows) * ad::kOBlock * 2 + 1023) & ~size_t(1023);
+    const size_t ops = R > 0 ? size_t(2) * EC::H * 128 * 128 + size_t(EC::H) * nmax * 128 : 0;
+    return 1024 + ys + ops + 256;
+  };
+  const size_t smem = expand_smem(p.max_tile_rows);
   static bool configured_e = false;
   if (!configured_e) {
     cudaError_t e = cudaFuncSetAttribute(adapter_expand_kernel<R>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(128 + ad::kTileRows * (R * 4 + ad::kOBlock * 2)));
+                                         int(expand_smem(ad::kTileRows)));
     if (e != cudaSuccess) return e;
     configured_e = true;
   }
-  adapter_expand_kernel<R><<<dim3(p.num_tiles, d_out / ad::kOBlock), ad::kOBlock, smem, s>>>(
-      p.tiles, splits, p.num_rows, p.t_part, static_cast<const __nv_bfloat16*>(lora_b), scale,
+  // TMEM: two M tiles of up to nmax columns, a power of two of at least 32
+  uint32_t tmem_cols = 0;
+  if (R > 0) {
+    tmem_cols = 32;
+    while (tmem_cols < uint32_t(2 * ((p.max_tile_rows + 15) & ~15))) tmem_cols <<= 1;
+  }
+  CUtensorMap ymap;
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(d_out), cuuint64_t(p.num_rows)};
+    const cuuint64_t str[1] = {cuuint64_t(d_out) * 2};
+    const cuuint32_t box[2] = {ad::kOBlock, ad::kGroupRows};
+    if (!tc::make_map(&ymap, y, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  adapter_expand_kernel<R><<<dim3(p.num_tiles, d_out / ad::kOBlock), ad::kExpandThreads, smem, s>>>(
+      p.tiles, p.t_final, static_cast<const __nv_bfloat16*>(lora_b),
       static_cast<const __nv_bfloat16*>(ia3), static_cast<__nv_bfloat16*>(y), d_out,
-      p.max_tile_rows, status);
+      p.max_tile_rows, tmem_cols, status, ymap);
   return cudaGetLastError();
 }
 
@@ -469,11 +693,15 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
   if (reinterpret_cast<uintptr_t>(dev_workspace) % 256 != 0)
     return set_last_error(PIE_EINVAL, "workspace must be 256-byte aligned");
 
-  const size_t copy = tiles.size() * sizeof(ad::Tile);
+  // one copy: the tiles, then zeroed per-tile counters
+  const size_t copy = tiles.empty() ? 0 : Y.counters + tiles.size() * 4;
   int err = PIE_OK;
   PinnedBlock* blk = pinned_acquire(std::max<size_t>(copy, 1), &err);
   if (!blk) return err;
-  if (copy) std::memcpy(blk->ptr, tiles.data(), copy);
+  if (copy) {
+    std::memset(blk->ptr, 0, copy);
+    std::memcpy(blk->ptr, tiles.data(), tiles.size() * sizeof(ad::Tile));
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (copy && cudaMemcpyAsync(static_cast<char*>(dev_workspace) + Y.tiles, blk->ptr, copy,
                               cudaMemcpyHostToDevice, s) != cudaSuccess) {
@@ -493,7 +721,9 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
   p->max_tile_rows = 0;
   for (const ad::Tile& t : tiles) p->max_tile_rows = std::max(p->max_tile_rows, t.n);
   p->tiles = reinterpret_cast<ad::Tile*>(static_cast<char*>(dev_workspace) + Y.tiles);
+  p->counters = reinterpret_cast<int*>(static_cast<char*>(dev_workspace) + Y.counters);
   p->t_part = reinterpret_cast<float*>(static_cast<char*>(dev_workspace) + Y.t_part);
+  p->t_final = reinterpret_cast<float*>(static_cast<char*>(dev_workspace) + Y.t_final);
   p->staging = blk;
   *out = p;
   return PIE_OK;
