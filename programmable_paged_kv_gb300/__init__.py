@@ -287,3 +287,69 @@ class AdapterPlan:
             self.close()
         except Exception:
             pass
+
+
+class Batcher:
+    """Work-conserving dispatch of GPU-bound calls (pie_batcher_*): queues with
+    priorities, calls with dependencies and read/write sets, one batch per
+    dispatch() on a GPU-idle notification, complete() when it has run."""
+
+    def __init__(self, ordered, max_calls: int, max_rows: int):
+        self.lib = abi.load()
+        flags = (C.c_uint8 * len(ordered))(*[1 if o else 0 for o in ordered])
+        h = C.c_void_p()
+        abi.check(self.lib.pie_batcher_create(len(ordered), flags, max_calls, max_rows,
+                                              C.byref(h)), "pie_batcher_create")
+        self.handle = h
+        self.max_calls = max_calls
+        self._calls = (C.c_int64 * max_calls)()
+        self._lanes = (C.c_int32 * max_calls)()
+
+    def add_queue(self, priority: int = 0) -> int:
+        q = C.c_int32()
+        abi.check(self.lib.pie_batcher_add_queue(self.handle, priority, C.byref(q)),
+                  "pie_batcher_add_queue")
+        return q.value
+
+    def submit(self, queue: int, handler: int, rows: int, key: int = -1, deps=(), reads=(),
+               writes=()) -> int:
+        arr = lambda xs: (C.c_int64 * max(len(xs), 1))(*xs)
+        deps, reads, writes = list(deps), list(reads), list(writes)
+        cid = C.c_int64()
+        abi.check(self.lib.pie_batcher_submit(
+            self.handle, queue, handler, rows, key, arr(deps), len(deps), arr(reads), len(reads),
+            arr(writes), len(writes), C.byref(cid)), "pie_batcher_submit")
+        return cid.value
+
+    def dispatch(self):
+        """(handler, call ids, lanes) of the next batch, or None."""
+        n, h = C.c_int32(), C.c_int32()
+        abi.check(self.lib.pie_batcher_dispatch(self.handle, self._calls, self._lanes,
+                                                self.max_calls, C.byref(n), C.byref(h)),
+                  "pie_batcher_dispatch")
+        if n.value == 0:
+            return None
+        return h.value, list(self._calls[:n.value]), list(self._lanes[:n.value])
+
+    def complete(self, ids):
+        ids = list(ids)
+        arr = (C.c_int64 * max(len(ids), 1))(*ids)
+        abi.check(self.lib.pie_batcher_complete(self.handle, arr, len(ids)),
+                  "pie_batcher_complete")
+
+    def counts(self):
+        a, b = C.c_int64(), C.c_int64()
+        abi.check(self.lib.pie_batcher_counts(self.handle, C.byref(a), C.byref(b)),
+                  "pie_batcher_counts")
+        return a.value, b.value
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.pie_batcher_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

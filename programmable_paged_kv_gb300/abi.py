@@ -1,4 +1,4 @@
-"""ctypes declarations of the C ABI in include/pie_fwd.h.
+"""ctypes declarations of the C ABI in include/pie_fwd.h and include/pie_batcher.h.
 
 Argument marshalling only: every step of the ForwardPass hot path runs in
 libpie_fwd.so.  Loading fails loudly when the library has not been built;
@@ -13,6 +13,7 @@ import re
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpie_fwd.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "pie_fwd.h")
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "pie_batcher.h")]
 
 PIE_OK = 0
 PIE_EINVAL = -1
@@ -89,14 +90,26 @@ SIGNATURES = {
     "pie_fwd_adapter_apply": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
                                         _P, _P, _P, _P, _P, _P]),
     "pie_fwd_adapter_plan_destroy": (None, [_P]),
+    "pie_batcher_create": (C.c_int, [C.c_int32, _P, C.c_int32, C.c_int64, C.POINTER(C.c_void_p)]),
+    "pie_batcher_destroy": (None, [_P]),
+    "pie_batcher_add_queue": (C.c_int, [_P, C.c_int32, C.POINTER(C.c_int32)]),
+    "pie_batcher_submit": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int64, C.c_int64, _P,
+                                     C.c_int32, _P, C.c_int32, _P, C.c_int32,
+                                     C.POINTER(C.c_int64)]),
+    "pie_batcher_dispatch": (C.c_int, [_P, _P, _P, C.c_int32, C.POINTER(C.c_int32),
+                                       C.POINTER(C.c_int32)]),
+    "pie_batcher_complete": (C.c_int, [_P, _P, C.c_int32]),
+    "pie_batcher_counts": (C.c_int, [_P, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
 }
 
 
 def header_functions() -> list:
-    """Names of the functions include/pie_fwd.h declares."""
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(pie_fwd_[a-z0-9_]+)\s*\(", src)))
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pie_(?:fwd|batcher)_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 _lib = None

@@ -1,0 +1,300 @@
+// Work-conserving dispatch of GPU-bound API calls (the Pie review, section 5:
+// Algorithm 2, Eq. (4), horizontal and vertical batching).  The policy, call by
+// call, is stated in include/pie_batcher.h; this file holds the bookkeeping.
+//
+// Per call: queue, handler type, rows, working-set key, state (queued, in
+// flight, done), dependencies and sorted, de-duplicated read/write sets.  Per
+// queue: its priority and its queued calls in arrival order.  A dispatch walks
+// the queues that hold calls (a list kept in insertion order, compacted as
+// queues empty), builds each ready queue's group, buckets the groups by
+// handler type, and for each type takes groups in priority order under Eq. (4)
+// against the union of the read and write sets already taken (which is the
+// same test as Eq. (4) against every taken group in turn), then truncates.
+
+#include <algorithm>
+#include <cstring>
+#include <deque>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "internal.h"
+#include "pie_batcher.h"
+
+namespace {
+
+using pie::set_last_error;
+
+enum State : uint8_t { kQueued = 0, kInFlight = 1, kDone = 2 };
+
+struct CallRec {
+  int32_t queue, handler;
+  int64_t rows, key;
+  std::vector<int64_t> deps, reads, writes;  // reads/writes sorted, unique
+};
+
+struct Queue {
+  int32_t priority;
+  std::deque<int64_t> ids;  // queued calls, arrival order
+  bool listed = false;      // present in Batcher::active
+};
+
+struct Group {
+  int32_t queue;
+  std::vector<int64_t> ids;
+};
+
+bool any_common(const std::vector<int64_t>& sorted, const std::unordered_set<int64_t>& set) {
+  for (int64_t v : sorted)
+    if (set.count(v)) return true;
+  return false;
+}
+
+}  // namespace
+
+struct pie_batcher {
+  std::vector<uint8_t> ordered;
+  int32_t max_calls;
+  int64_t max_rows;
+  std::vector<CallRec> calls;
+  std::vector<uint8_t> state;
+  std::vector<Queue> queues;
+  std::vector<int32_t> active;  // queues that may hold calls
+  int64_t queued = 0, in_flight = 0;
+
+  bool ready(int64_t id) const {
+    for (int64_t d : calls[size_t(id)].deps)
+      if (state[size_t(d)] != kDone) return false;
+    return true;
+  }
+
+  // lines 06 and 08: the queue's ready head and its vertical group
+  void group_of(int32_t q, Group* g) const {
+    g->queue = q;
+    g->ids.clear();
+    const Queue& Q = queues[size_t(q)];
+    if (Q.ids.empty() || !ready(Q.ids.front())) return;
+    const int64_t head = Q.ids.front();
+    g->ids.push_back(head);
+    const int32_t h = calls[size_t(head)].handler;
+    if (!ordered[size_t(h)]) return;
+    for (size_t i = 1; i < Q.ids.size(); ++i) {
+      const CallRec& c = calls[size_t(Q.ids[i])];
+      if (c.handler != h) break;
+      bool ok = true;
+      for (int64_t d : c.deps)
+        if (state[size_t(d)] != kDone &&
+            std::find(g->ids.begin(), g->ids.end(), d) == g->ids.end()) {
+          ok = false;
+          break;
+        }
+      if (!ok) break;
+      g->ids.push_back(Q.ids[i]);
+    }
+  }
+};
+
+extern "C" {
+
+int pie_batcher_create(int32_t num_handlers, const uint8_t* ordered, int32_t max_calls,
+                       int64_t max_rows, pie_batcher_t** out) {
+  if (!out) return set_last_error(PIE_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (num_handlers < 1) return set_last_error(PIE_EINVAL, "num_handlers < 1");
+  if (max_calls < 1 || max_rows < 1) return set_last_error(PIE_EINVAL, "batch limits must be >= 1");
+  pie_batcher_t* b = new pie_batcher_t;
+  b->ordered.assign(size_t(num_handlers), 0);
+  if (ordered)
+    for (int h = 0; h < num_handlers; ++h) b->ordered[size_t(h)] = ordered[h] ? 1 : 0;
+  b->max_calls = max_calls;
+  b->max_rows = max_rows;
+  *out = b;
+  return PIE_OK;
+}
+
+void pie_batcher_destroy(pie_batcher_t* b) { delete b; }
+
+int pie_batcher_add_queue(pie_batcher_t* b, int32_t priority, int32_t* queue_id) {
+  if (!b || !queue_id) return set_last_error(PIE_EINVAL, "NULL argument");
+  if (b->queues.size() >= size_t(INT32_MAX)) return set_last_error(PIE_ERANGE, "too many queues");
+  Queue q;
+  q.priority = priority;
+  b->queues.push_back(std::move(q));
+  *queue_id = int32_t(b->queues.size() - 1);
+  return PIE_OK;
+}
+
+int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t rows,
+                       int64_t key, const int64_t* deps, int32_t num_deps,
+                       const int64_t* reads, int32_t num_reads, const int64_t* writes,
+                       int32_t num_writes, int64_t* call_id) {
+  if (!b || !call_id) return set_last_error(PIE_EINVAL, "NULL argument");
+  if (queue < 0 || size_t(queue) >= b->queues.size()) return set_last_error(PIE_EINVAL, "unknown queue");
+  if (handler < 0 || size_t(handler) >= b->ordered.size())
+    return set_last_error(PIE_EINVAL, "unknown handler type");
+  if (rows < 1) return set_last_error(PIE_EINVAL, "rows < 1");
+  if (num_deps < 0 || num_reads < 0 || num_writes < 0) return set_last_error(PIE_EINVAL, "negative count");
+  if ((num_deps && !deps) || (num_reads && !reads) || (num_writes && !writes))
+    return set_last_error(PIE_EINVAL, "NULL array with a positive count");
+  const int64_t id = int64_t(b->calls.size());
+  for (int i = 0; i < num_deps; ++i)
+    if (deps[i] < 0 || deps[i] >= id)
+      return set_last_error(PIE_EINVAL, "a dependency is not an earlier call");
+  CallRec c;
+  c.queue = queue;
+  c.handler = handler;
+  c.rows = rows;
+  c.key = key < 0 ? -1 : key;
+  c.deps.assign(deps, deps + num_deps);
+  c.reads.assign(reads, reads + num_reads);
+  c.writes.assign(writes, writes + num_writes);
+  for (auto* v : {&c.reads, &c.writes}) {
+    std::sort(v->begin(), v->end());
+    v->erase(std::unique(v->begin(), v->end()), v->end());
+  }
+  b->calls.push_back(std::move(c));
+  b->state.push_back(kQueued);
+  Queue& Q = b->queues[size_t(queue)];
+  Q.ids.push_back(id);
+  if (!Q.listed) {
+    Q.listed = true;
+    b->active.push_back(queue);
+  }
+  ++b->queued;
+  *call_id = id;
+  return PIE_OK;
+}
+
+int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32_t capacity,
+                         int32_t* num_calls, int32_t* handler) {
+  if (!b || !calls || !lanes || !num_calls || !handler)
+    return set_last_error(PIE_EINVAL, "NULL argument");
+  if (capacity < b->max_calls) return set_last_error(PIE_ENOSPACE, "capacity < max_calls");
+  *num_calls = 0;
+  *handler = -1;
+
+  // lines 06 and 08: ready groups, bucketed by handler type; drop empty queues
+  std::vector<std::vector<Group>> by_type(b->ordered.size());
+  size_t keep = 0;
+  for (size_t i = 0; i < b->active.size(); ++i) {
+    const int32_t q = b->active[i];
+    Queue& Q = b->queues[size_t(q)];
+    if (Q.ids.empty()) {
+      Q.listed = false;
+      continue;
+    }
+    b->active[keep++] = q;
+    Group g;
+    b->group_of(q, &g);
+    if (!g.ids.empty()) by_type[size_t(b->calls[size_t(g.ids[0])].handler)].push_back(std::move(g));
+  }
+  b->active.resize(keep);
+
+  // lines 07, 09, 10 per handler type; line 11 across types
+  std::vector<std::pair<int32_t, std::vector<int64_t>>> best_batch;  // (group index, kept ids)
+  int64_t best_oldest = -1;
+  int32_t best_type = -1;
+  std::vector<const Group*> order;
+  std::unordered_set<int64_t> taken_r, taken_w;
+  for (size_t h = 0; h < by_type.size(); ++h) {
+    std::vector<Group>& groups = by_type[h];
+    if (groups.empty()) continue;
+    order.clear();
+    for (const Group& g : groups) order.push_back(&g);
+    std::sort(order.begin(), order.end(), [&](const Group* u, const Group* v) {
+      const int32_t pu = b->queues[size_t(u->queue)].priority;
+      const int32_t pv = b->queues[size_t(v->queue)].priority;
+      return pu != pv ? pu > pv : u->ids[0] < v->ids[0];
+    });
+    taken_r.clear();
+    taken_w.clear();
+    std::vector<std::pair<int32_t, std::vector<int64_t>>> cand;
+    int64_t n_calls = 0, n_rows = 0, oldest = INT64_MAX;
+    bool stop = false;
+    std::vector<int64_t> gr, gw;
+    for (size_t gi = 0; gi < order.size() && !stop; ++gi) {
+      const Group& g = *order[gi];
+      gr.clear();
+      gw.clear();
+      for (int64_t id : g.ids) {
+        const CallRec& c = b->calls[size_t(id)];
+        gr.insert(gr.end(), c.reads.begin(), c.reads.end());
+        gw.insert(gw.end(), c.writes.begin(), c.writes.end());
+      }
+      // Eq. (4) against every group taken so far
+      if (any_common(gw, taken_r) || any_common(gw, taken_w) || any_common(gr, taken_w)) continue;
+      taken_r.insert(gr.begin(), gr.end());
+      taken_w.insert(gw.begin(), gw.end());
+      std::vector<int64_t> kept;
+      for (int64_t id : g.ids) {
+        const int64_t rows = b->calls[size_t(id)].rows;
+        if (n_calls > 0 && (n_calls + 1 > b->max_calls || n_rows + rows > b->max_rows)) {
+          stop = true;
+          break;
+        }
+        kept.push_back(id);
+        ++n_calls;
+        n_rows += rows;
+        oldest = std::min(oldest, id);
+      }
+      if (!kept.empty()) cand.emplace_back(int32_t(gi), std::move(kept));
+    }
+    if (!cand.empty() && (best_type < 0 || oldest < best_oldest)) {
+      best_oldest = oldest;
+      best_type = int32_t(h);
+      best_batch = std::move(cand);
+    }
+  }
+  if (best_type < 0) return PIE_OK;
+
+  // lanes, and the calls leave their queues (each group is its queue's prefix)
+  int32_t n = 0, lane = -1;
+  for (auto& kv : best_batch) {
+    const std::vector<int64_t>& kept = kv.second;
+    int64_t prev_key = -1;
+    for (size_t i = 0; i < kept.size(); ++i) {
+      const CallRec& c = b->calls[size_t(kept[i])];
+      if (i == 0 || c.key < 0 || c.key != prev_key) ++lane;
+      prev_key = c.key;
+      calls[n] = kept[i];
+      lanes[n] = lane;
+      ++n;
+    }
+    Queue& Q = b->queues[size_t(b->calls[size_t(kept[0])].queue)];
+    for (size_t i = 0; i < kept.size(); ++i) {
+      Q.ids.pop_front();
+      b->state[size_t(kept[i])] = kInFlight;
+    }
+  }
+  b->queued -= n;
+  b->in_flight += n;
+  *num_calls = n;
+  *handler = best_type;
+  return PIE_OK;
+}
+
+int pie_batcher_complete(pie_batcher_t* b, const int64_t* calls, int32_t n) {
+  if (!b || (n > 0 && !calls) || n < 0) return set_last_error(PIE_EINVAL, "bad arguments");
+  for (int i = 0; i < n; ++i)
+    if (calls[i] < 0 || size_t(calls[i]) >= b->state.size() || b->state[size_t(calls[i])] != kInFlight)
+      return set_last_error(PIE_EINVAL, "a completed call was not in flight");
+  for (int i = 0; i < n; ++i) {
+    if (b->state[size_t(calls[i])] == kInFlight) {  // duplicates in the list count once
+      b->state[size_t(calls[i])] = kDone;
+      --b->in_flight;
+      CallRec& c = b->calls[size_t(calls[i])];
+      std::vector<int64_t>().swap(c.reads);  // no longer needed
+      std::vector<int64_t>().swap(c.writes);
+    }
+  }
+  return PIE_OK;
+}
+
+int pie_batcher_counts(const pie_batcher_t* b, int64_t* queued, int64_t* in_flight) {
+  if (!b) return set_last_error(PIE_EINVAL, "batcher is NULL");
+  if (queued) *queued = b->queued;
+  if (in_flight) *in_flight = b->in_flight;
+  return PIE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+"""The native batcher (pie_batcher_*) against the Algorithm 2 oracle on the
+same operation sequences: every dispatch must return the same handler type,
+the same call ids in the same order and the same lanes (integer work:
+compared exactly).  Plus the calls it refuses.  Host code only: no GPU."""
+import ctypes as C
+import random
+
+import pytest
+
+import oracle.batcher as OB
+from programmable_paged_kv_gb300 import Batcher, abi, build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+
+
+def _drive(seed, n_calls=120, steps=600):
+    rng = random.Random(seed)
+    n_types = rng.randrange(1, 4)
+    ordered = [rng.random() < 0.6 for _ in range(n_types)]
+    nq = rng.randrange(1, 9)
+    prios = [rng.randrange(4) for _ in range(nq)]
+    max_calls, max_rows = rng.randrange(1, 9), rng.randrange(3, 40)
+    nat = Batcher(ordered, max_calls, max_rows)
+    for p in prios:
+        nat.add_queue(p)
+    orc = OB.Batcher({q: p for q, p in enumerate(prios)}, dict(enumerate(ordered)), max_calls,
+                     max_rows)
+    n_pages = rng.randrange(2, 30)
+    submitted, in_flight = 0, []
+    for _ in range(steps):
+        act = rng.random()
+        if act < 0.4 and submitted < n_calls:
+            q, h = rng.randrange(nq), rng.randrange(n_types)
+            rows = rng.randrange(1, 12)
+            deps = sorted({rng.randrange(submitted) for _ in range(rng.randrange(3))}) if submitted else []
+            reads = [rng.randrange(n_pages) for _ in range(rng.randrange(4))]
+            writes = [rng.randrange(n_pages) for _ in range(rng.randrange(3))]
+            key = rng.randrange(-1, 4)
+            cid = nat.submit(q, h, rows, key, deps, reads, writes)
+            assert cid == submitted
+            orc.submit(OB.Call(cid, q, h, rows, tuple(deps), frozenset(reads), frozenset(writes),
+                               key))
+            submitted += 1
+        elif act < 0.6 and in_flight:
+            done = in_flight.pop(rng.randrange(len(in_flight)))
+            nat.complete(done)
+            orc.complete(done)
+        else:
+            a = nat.dispatch()
+            b = orc.dispatch()
+            assert (a is None) == (b is None), (seed, a, b)
+            if a is not None:
+                assert a == (b.handler, b.calls, b.lane_of_call), (seed, a, b)
+                in_flight.append(a[1])
+    queued, flying = nat.counts()
+    assert flying == sum(len(x) for x in in_flight)
+    assert queued == sum(len(v) for v in orc.pending.values())
+    nat.close()
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_native_batcher_matches_the_oracle(seed):
+    _drive(seed)
+
+
+def test_native_batcher_large_trace():
+    # many queues and calls: the same decisions at scale
+    _drive(1234, n_calls=3000, steps=12000)
+
+
+def test_batcher_refusals():
+    lib = abi.load()
+    h = C.c_void_p()
+    assert lib.pie_batcher_create(0, None, 4, 16, C.byref(h)) == abi.PIE_EINVAL
+    assert lib.pie_batcher_create(2, None, 0, 16, C.byref(h)) == abi.PIE_EINVAL
+    assert lib.pie_batcher_create(2, None, 4, 0, C.byref(h)) == abi.PIE_EINVAL
+    b = Batcher([True, False], 4, 16)
+    q = b.add_queue(1)
+    cid = C.c_int64()
+    sub = lambda *a: lib.pie_batcher_submit(b.handle, *a, C.byref(cid))
+    assert sub(5, 0, 1, -1, None, 0, None, 0, None, 0) == abi.PIE_EINVAL     # unknown queue
+    assert sub(q, 2, 1, -1, None, 0, None, 0, None, 0) == abi.PIE_EINVAL     # unknown handler
+    assert sub(q, 0, 0, -1, None, 0, None, 0, None, 0) == abi.PIE_EINVAL     # rows < 1
+    dep = (C.c_int64 * 1)(0)
+    assert sub(q, 0, 1, -1, dep, 1, None, 0, None, 0) == abi.PIE_EINVAL      # not an earlier call
+    assert sub(q, 0, 1, -1, None, 1, None, 0, None, 0) == abi.PIE_EINVAL     # NULL with a count
+    assert b.submit(q, 0, 1) == 0
+    n, hh = C.c_int32(), C.c_int32()
+    small = (C.c_int64 * 2)()
+    lanes = (C.c_int32 * 2)()
+    assert lib.pie_batcher_dispatch(b.handle, small, lanes, 2, C.byref(n), C.byref(hh)) == abi.PIE_ENOSPACE
+    assert b.counts() == (1, 0)
+    assert lib.pie_batcher_complete(b.handle, (C.c_int64 * 1)(0), 1) == abi.PIE_EINVAL  # still queued
+    assert b.dispatch() == (0, [0], [0])
+    assert b.counts() == (0, 1)
+    b.complete([0])
+    assert b.counts() == (0, 0)
+    assert lib.pie_batcher_complete(b.handle, (C.c_int64 * 1)(0), 1) == abi.PIE_EINVAL  # twice
+    assert b.dispatch() is None
+    b.close()
