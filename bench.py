@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
                              "masked_tova", "decode_pass", "readout_topk", "decode_loop",
-                             "adapters_decode", "adapters_prefill"],
+                             "adapters_decode", "adapters_prefill", "batcher"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
     ap.add_argument("--pool-pages", type=int, default=65536,
@@ -811,6 +811,176 @@ def run_adapters(args, local):
     plan.close()
 
 
+def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
+    """Closed loop of the work-conserving batcher over the ForwardPass: every
+    agent (command queue) submits its next decode call only when its previous
+    one has completed (an inferlet awaiting its result); on each GPU-idle
+    instant one batch is dispatched as one multi-lane pass.  Returns (seconds,
+    calls, batches, attended tokens, host dispatch seconds)."""
+    import torch
+    from programmable_paged_kv_gb300 import (Batcher, ForwardPlan, make_desc, make_meta, runner,
+                                             set_timing_events)
+    from programmable_paged_kv_gb300.batching import forward_batch_pass
+    d = trace.pool.desc
+    desc = make_desc(d)
+    P, Hq, Hkv, D = d.page_size, d.num_q_heads, d.num_kv_heads, d.head_dim
+    tdt = torch.bfloat16
+    pools = runner.DevicePools(trace.pool)
+    b = Batcher([True], max_calls, max_rows)
+    Q = len(trace.queue_pages)
+    qids = [b.add_queue(0) for _ in range(Q)]
+    frozen = [int(c) for c in trace.cached]
+    cursor = list(frozen)
+    left = [steps] * Q
+    call_set, call_rows = {}, {}
+    rng = np.random.default_rng(5)
+    q_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hq, D), dtype=np.float32)).view(np.int16)).pin_memory()
+    kv_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hkv, D), dtype=np.float32)).view(np.int16)).pin_memory()
+
+    pages64 = [np.asarray(pg, np.int64) for pg in trace.queue_pages]
+
+    def submit(q):
+        pages = pages64[q]
+        c = cursor[q]
+        cid = b.submit(qids[q], 0, 1, key=q, reads=pages[:c // P + 1], writes=pages[c // P:c // P + 1])
+        cursor[q] += 1
+        left[q] -= 1
+        call_set[cid], call_rows[cid] = q, 1
+    for q in range(Q):
+        submit(q)
+    ev = [] if kernel_ms is not None else None
+    calls = batches = tokens = 0
+    host = 0.0    # native dispatch calls
+    marshal = 0.0  # completion events and the next calls' submission
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    while True:
+        h0 = time.perf_counter()
+        r = b.dispatch()
+        host += time.perf_counter() - h0
+        if r is None:
+            break
+        _, ids, lanes = r
+        p, lane_set, first = forward_batch_pass(ids, lanes, call_set, call_rows, trace.queue_pages,
+                                                frozen)
+        N = int(p.row_indptr[-1])
+        sel = torch.tensor(lane_set, dtype=torch.long)
+        qd = q_in.index_select(0, sel).cuda(non_blocking=True).view(tdt)
+        kd = kv_in.index_select(0, sel).cuda(non_blocking=True).view(tdt)
+        plan = ForwardPlan(desc, make_meta(p, trace.pool.num_pool_pages))
+        fr = torch.tensor([frozen[w] for w in lane_set], dtype=torch.int32).cuda(non_blocking=True)
+        q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+        plan.append_kv(qd, kd, kd, q_rot, pools.k, pools.v, fr)
+        out = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+        if ev is not None:
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            set_timing_events(*e)
+            ev.append(e)
+        plan.attend(q_rot, pools.k, pools.v, None, out)
+        if ev is not None:
+            set_timing_events()
+        plan.fold(fr)
+        out_h = out.cpu()  # the agents' results (a completion event each)
+        plan.close()
+        for w, n in zip(lane_set, np.diff(p.row_indptr)):
+            frozen[w] += int(n)
+        tokens += int(p.kv_len.sum())
+        calls += len(ids)
+        batches += 1
+        h0 = time.perf_counter()
+        b.complete(ids)
+        for c in ids:
+            if left[call_set[c]] > 0:
+                submit(call_set[c])
+        marshal += time.perf_counter() - h0
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    if ev is not None:
+        kernel_ms.extend(a.elapsed_time(c) for a, c in ev)
+    del out_h
+    b.close()
+    return secs, calls, batches, tokens, host, marshal
+
+
+def run_batcher(args, local):
+    """The work-conserving batcher in a closed loop (see batcher_closed_loop)
+    on the decode batch's shape: 64 agents with C ~ U[512, 4096] cached slots,
+    `--steps` decode calls each; batches of up to 64 calls against one call
+    per pass."""
+    import torch
+    import oracle.batcher as OB
+    from programmable_paged_kv_gb300 import build
+    torch.cuda.set_device(local)
+    build()
+    steps = min(max(args.steps, 4), 64)  # each agent's pages hold 64 slots past its context
+    trace = W.forward_calls(args.seed, queues=64, calls_per_queue=1, prefix=512, private_hi=3584,
+                            prefill_lo=64, prefill_hi=64, num_pool_pages=args.pool_pages)
+    # warm-up (libraries, allocator, first plans)
+    batcher_closed_loop(trace, 2, 64, 4096)
+    batcher_closed_loop(trace, 2, 1, 4096)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    kms = []
+    secs, calls, batches, tokens, host, marshal = batcher_closed_loop(trace, steps, 64, 4096, kms)
+    s1, c1, b1, t1, h1, m1 = batcher_closed_loop(trace, steps, 1, 4096)
+    clk = clocks.stop()
+    # the oracle batcher on the same closed loop's decisions (dispatch + complete)
+    ob = OB.Batcher({q: 0 for q in range(64)}, {0: True}, 64, 4096)
+    nxt, t_orc, left = 0, 0.0, [steps] * 64
+    for q in range(64):
+        ob.submit(OB.Call(nxt, q, 0, 1, key=q)); nxt += 1
+    while True:
+        h0 = time.perf_counter()
+        r = ob.dispatch()
+        if r is None:
+            break
+        ob.complete(r.calls)
+        t_orc += time.perf_counter() - h0
+        for c in r.calls:
+            q = ob.calls[c].queue
+            left[q] -= 1
+            if left[q] > 0:
+                ob.submit(OB.Call(nxt, q, 0, 1, key=q)); nxt += 1
+    hbm, kind = peaks()
+    D, Hkv = 128, 8
+    kbytes = tokens * Hkv * 2 * D * 2
+    kern = sum(kms) / 1e3
+    line = {"workload": "batcher",
+            "metric": "forward calls/s, closed loop of 64 decode agents through the "
+                      "work-conserving batcher",
+            "unit": "calls/s", "value": calls / secs, "ms_per_step": secs / batches * 1e3,
+            "steps": steps, "warmup": 2, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "one_call_per_pass": {"calls_per_s": c1 / s1, "passes": b1},
+            "speedup_vs_one_call_per_pass": (calls / secs) / (c1 / s1),
+            "batches": batches, "mean_batch_calls": calls / batches,
+            "attended_tokens_per_s": tokens / secs,
+            "dispatch_us_per_batch_native": host / batches * 1e6,
+            "complete_and_submit_us_per_batch": marshal / batches * 1e6,
+            "attention_kernel_ms_per_batch": sum(kms) / len(kms) if kms else None,
+            "e2e": {"value": calls / secs, "unit": "calls/s",
+                    "h2d_bytes_per_step": 64 * (32 + 8) * 128 * 2,
+                    "d2h_bytes_per_step": 64 * 32 * 128 * 2},
+            "gpu_launches": batches * 5,
+            "roofline": {"bound": "hbm", "achieved": kbytes / kern / 1e9 if kern else None,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": kbytes / kern / 1e9 / hbm if kern else None, "traffic": None,
+                         "kernel": "attention kernels of the batched passes"},
+            "config": {"workload": "batcher", "agents": 64, "decode_calls_each": steps,
+                       "max_calls": 64, "max_rows": 4096, "q_heads": 32, "kv_heads": 8,
+                       "head_dim": 128, "page_size": 16, "cached": "512 shared by pairs + U[0, 3584]",
+                       "l2": "KV pages of 64 agents (~300 MB) larger than L2"},
+            "cpu_baseline": {"value": batches / t_orc, "unit": "dispatches/s (+complete)",
+                             "cores": 1, "kind": "oracle",
+                             "sample": f"the oracle batcher on the same closed loop ({batches} "
+                                       f"dispatches); the native one took "
+                                       f"{host / batches * 1e6:.1f} us per dispatch"}}
+    if clk:
+        line["clocks"] = clk
+    print(json.dumps(line))
+
+
 def run_decode_loop(args, local):
     """Time the decode loop that runs ahead of the host: the decode batch (64
     lanes, C ~ U[512, 4096]) for K single-token steps in one
@@ -911,6 +1081,8 @@ def main():
         run_decode_loop(args, local)
     elif args.workload in ADAPTER_SHAPES:
         run_adapters(args, local)
+    elif args.workload == "batcher":
+        run_batcher(args, local)
     elif args.workload != "decode_batch":
         run_workload(args, local)
     else:

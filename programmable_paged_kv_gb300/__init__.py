@@ -21,7 +21,8 @@ from .abi import (PIE_BF16, PIE_F32, PIE_FOLD_ALL, PIE_FOLD_CHANNEL, PIE_FOLD_CO
 
 __all__ = ["ForwardPlan", "PieError", "make_desc", "make_meta", "workspace_bytes", "build",
            "set_timing_events", "readout_topk", "readout_topk_workspace_bytes",
-           "decode_loop", "decode_loop_workspace_bytes",
+           "decode_loop", "decode_loop_workspace_bytes", "AdapterPlan", "adapter_workspace_bytes",
+           "Batcher",
            "PIE_F32", "PIE_BF16", "PIE_FOLD_NONE", "PIE_FOLD_ALL", "PIE_FOLD_COUNT",
            "PIE_FOLD_CHANNEL", "PIE_STATUS_FROZEN_WRITE", "PIE_STATUS_FOLD_CLAMP",
            "PIE_STATUS_FOLD_GAP", "PIE_STATUS_TIMEOUT"]
@@ -313,12 +314,13 @@ class Batcher:
 
     def submit(self, queue: int, handler: int, rows: int, key: int = -1, deps=(), reads=(),
                writes=()) -> int:
-        arr = lambda xs: (C.c_int64 * max(len(xs), 1))(*xs)
-        deps, reads, writes = list(deps), list(reads), list(writes)
+        deps, reads, writes = (np.ascontiguousarray(x, dtype=np.int64).reshape(-1)
+                               for x in (deps, reads, writes))
         cid = C.c_int64()
         abi.check(self.lib.pie_batcher_submit(
-            self.handle, queue, handler, rows, key, arr(deps), len(deps), arr(reads), len(reads),
-            arr(writes), len(writes), C.byref(cid)), "pie_batcher_submit")
+            self.handle, queue, handler, rows, key, deps.ctypes.data, deps.size,
+            reads.ctypes.data, reads.size, writes.ctypes.data, writes.size, C.byref(cid)),
+            "pie_batcher_submit")
         return cid.value
 
     def dispatch(self):
@@ -332,9 +334,8 @@ class Batcher:
         return h.value, list(self._calls[:n.value]), list(self._lanes[:n.value])
 
     def complete(self, ids):
-        ids = list(ids)
-        arr = (C.c_int64 * max(len(ids), 1))(*ids)
-        abi.check(self.lib.pie_batcher_complete(self.handle, arr, len(ids)),
+        ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+        abi.check(self.lib.pie_batcher_complete(self.handle, ids.ctypes.data, ids.size),
                   "pie_batcher_complete")
 
     def counts(self):

@@ -538,6 +538,71 @@ def adapter_site(seed: int, rows_per_lane, n_adapters: int = 16, d_in: int = 409
     return AdapterSite(row_indptr, ad, x, y, a, b, scale, s, rank, recipe)
 
 
+@dataclasses.dataclass
+class CallTrace:
+    """GPU-bound forward calls from several command queues, in arrival order,
+    for the work-conserving batcher: queue q owns one working set (its pages
+    in slot order, frozen for its first cached[q] slots); each call appends n
+    rows to its queue's working set (the folding() geometry: position = slot
+    = the next free slot, fold all).  `pool` holds the pages' initial
+    contents (passes is empty)."""
+    pool: Scenario
+    queue_pages: List[np.ndarray]
+    cached: np.ndarray               # int32 [Q]
+    priority: np.ndarray             # int32 [Q]
+    calls: list                      # [(queue, q [n,Hq,d], k [n,Hkv,d], v [n,Hkv,d])]
+    recipe: str = ""
+
+
+def forward_calls(seed: int = 0, queues: int = 16, calls_per_queue: int = 6, prefix: int = 256,
+                  private_hi: int = 100, prefill_lo: int = 8, prefill_hi: int = 64,
+                  desc: Optional[Desc] = None, num_pool_pages: int = 4096) -> CallTrace:
+    """Queues 2i and 2i+1 share a frozen prefix of `prefix` slots (whole
+    pages, read-only) and add U[0, private_hi] cached slots of their own; each
+    queue's first call is a prefill of U[prefill_lo, prefill_hi] rows, the
+    others decode steps (one row) or short continuations (U[2, 8] rows); the
+    calls of all queues arrive interleaved in a seeded random order, queue
+    priorities ~ U{0, 1, 2}; q/k/v ~ N(0, 1)."""
+    desc = desc or Desc(32, 8, 128, 16, BF16)
+    P = desc.page_size
+    assert prefix % P == 0
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 13]))
+    extra = rng.integers(0, private_hi + 1, size=queues)
+    rows = []
+    for q in range(queues):
+        r = [int(rng.integers(prefill_lo, prefill_hi + 1))]
+        for _ in range(calls_per_queue - 1):
+            r.append(1 if rng.random() < 0.6 else int(rng.integers(2, 9)))
+        rows.append(r)
+    npairs = (queues + 1) // 2
+    shared_pages = prefix // P
+    private_need = [_pages_for(int(extra[q]) + sum(rows[q]), P) + 1 for q in range(queues)]
+    chunks = _permuted_pool(rng, num_pool_pages, [shared_pages] * npairs + private_need)
+    queue_pages = []
+    for q in range(queues):
+        queue_pages.append(np.concatenate([chunks[q // 2], chunks[npairs + q]]).astype(np.int32))
+    cached = (prefix + extra).astype(np.int32)
+    pool_pages = np.unique(np.concatenate(queue_pages)).astype(np.int32)
+    k_init, v_init = _fill_pool_init(desc, pool_pages, queue_pages, cached, rng)
+    order = np.concatenate([np.full(calls_per_queue, q) for q in range(queues)])
+    rng.shuffle(order)
+    seen = np.zeros(queues, np.int64)
+    calls = []
+    Hq, Hkv, d = desc.num_q_heads, desc.num_kv_heads, desc.head_dim
+    for q in order:
+        n = rows[q][seen[q]]
+        seen[q] += 1
+        calls.append((int(q), _normal(rng, (n, Hq, d), desc.dtype),
+                      _normal(rng, (n, Hkv, d), desc.dtype), _normal(rng, (n, Hkv, d), desc.dtype)))
+    pool = Scenario("forward_calls", desc, num_pool_pages, pool_pages, k_init, v_init, cached, [],
+                    "")
+    recipe = (f"{queues} queues x {calls_per_queue} calls, pairs share a {prefix}-slot prefix, "
+              f"private cached U[0,{private_hi}], prefill U[{prefill_lo},{prefill_hi}] rows then "
+              f"decodes (60%) or 2-8-row continuations, random interleaving, priorities U{{0,1,2}}")
+    return CallTrace(pool, queue_pages, cached, rng.integers(0, 3, size=queues).astype(np.int32),
+                     calls, recipe)
+
+
 FULL = {
     "tiny": lambda seed=0: tiny(seed),
     "decode_batch": lambda seed=0: decode_batch(seed),
