@@ -52,10 +52,12 @@ int pie_batcher_add_queue(pie_batcher_t* b, int32_t priority, int32_t* queue_id)
 
 /* Enqueue a call (Algorithm 2, lines 01 and 03).  rows >= 1 counts against
  * max_rows; key >= 0 names its working set (-1: none); deps are ids of earlier
- * calls; reads / writes are resource ids (e.g. KV page ids), any order,
- * duplicates allowed.  Arrays may be NULL when their count is 0.  The call's
- * id goes to *call_id.  Errors: PIE_EINVAL (unknown queue or handler, rows < 1,
- * a dependency that is not an earlier call, negative counts). */
+ * calls; reads / writes are resource ids in [0, 2^26) (e.g. KV page ids; the
+ * batcher keeps a table indexed by resource id), any order, duplicates
+ * allowed.  Arrays may be NULL when their count is 0.  The call's id goes to
+ * *call_id.  Errors: PIE_EINVAL (unknown queue or handler, rows < 1, a
+ * dependency that is not an earlier call, negative counts), PIE_ERANGE (a
+ * resource id outside [0, 2^26)). */
 int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t rows,
                        int64_t key, const int64_t* deps, int32_t num_deps,
                        const int64_t* reads, int32_t num_reads, const int64_t* writes,

@@ -10,12 +10,14 @@
 // handler type, and for each type takes groups in priority order under Eq. (4)
 // against the union of the read and write sets already taken (which is the
 // same test as Eq. (4) against every taken group in turn), then truncates.
+// Resource ids are small non-negative integers (KV page ids), so the taken
+// sets are two arrays indexed by resource id holding the stamp of the last
+// candidate that marked the resource: marking and testing cost one access.
 
 #include <algorithm>
 #include <cstring>
 #include <deque>
 #include <string>
-#include <unordered_set>
 #include <vector>
 
 #include "internal.h"
@@ -44,11 +46,7 @@ struct Group {
   std::vector<int64_t> ids;
 };
 
-bool any_common(const std::vector<int64_t>& sorted, const std::unordered_set<int64_t>& set) {
-  for (int64_t v : sorted)
-    if (set.count(v)) return true;
-  return false;
-}
+constexpr int64_t kMaxResource = int64_t(1) << 26;  // resource ids: [0, 2^26)
 
 }  // namespace
 
@@ -61,6 +59,18 @@ struct pie_batcher {
   std::vector<Queue> queues;
   std::vector<int32_t> active;  // queues that may hold calls
   int64_t queued = 0, in_flight = 0;
+  std::vector<uint32_t> rstamp, wstamp;  // per resource: stamp of the candidate that read / wrote it
+  uint32_t stamp = 0;
+
+  // a new candidate: a fresh stamp (arrays cleared when the counter wraps)
+  uint32_t next_stamp() {
+    if (++stamp == 0) {
+      std::fill(rstamp.begin(), rstamp.end(), 0u);
+      std::fill(wstamp.begin(), wstamp.end(), 0u);
+      stamp = 1;
+    }
+    return stamp;
+  }
 
   bool ready(int64_t id) const {
     for (int64_t d : calls[size_t(id)].deps)
@@ -140,6 +150,19 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
   for (int i = 0; i < num_deps; ++i)
     if (deps[i] < 0 || deps[i] >= id)
       return set_last_error(PIE_EINVAL, "a dependency is not an earlier call");
+  int64_t top = -1;
+  for (int i = 0; i < num_reads; ++i) top = std::max(top, reads[i]);
+  for (int i = 0; i < num_writes; ++i) top = std::max(top, writes[i]);
+  for (int i = 0; i < num_reads; ++i)
+    if (reads[i] < 0) top = kMaxResource;
+  for (int i = 0; i < num_writes; ++i)
+    if (writes[i] < 0) top = kMaxResource;
+  if (top >= kMaxResource) return set_last_error(PIE_ERANGE, "resource id outside [0, 2^26)");
+  if (top >= int64_t(b->rstamp.size())) {
+    const size_t n = std::max<size_t>(size_t(top) + 1, 2 * b->rstamp.size());
+    b->rstamp.resize(n, 0u);
+    b->wstamp.resize(n, 0u);
+  }
   CallRec c;
   c.queue = queue;
   c.handler = handler;
@@ -195,7 +218,6 @@ int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32
   int64_t best_oldest = -1;
   int32_t best_type = -1;
   std::vector<const Group*> order;
-  std::unordered_set<int64_t> taken_r, taken_w;
   for (size_t h = 0; h < by_type.size(); ++h) {
     std::vector<Group>& groups = by_type[h];
     if (groups.empty()) continue;
@@ -206,25 +228,30 @@ int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32
       const int32_t pv = b->queues[size_t(v->queue)].priority;
       return pu != pv ? pu > pv : u->ids[0] < v->ids[0];
     });
-    taken_r.clear();
-    taken_w.clear();
+    const uint32_t st = b->next_stamp();
+    uint32_t* rs = b->rstamp.data();
+    uint32_t* ws = b->wstamp.data();
     std::vector<std::pair<int32_t, std::vector<int64_t>>> cand;
     int64_t n_calls = 0, n_rows = 0, oldest = INT64_MAX;
     bool stop = false;
-    std::vector<int64_t> gr, gw;
     for (size_t gi = 0; gi < order.size() && !stop; ++gi) {
       const Group& g = *order[gi];
-      gr.clear();
-      gw.clear();
+      // Eq. (4) against every group taken so far: the group's writes meet no
+      // taken read or write, its reads no taken write
+      bool clash = false;
+      for (size_t i = 0; i < g.ids.size() && !clash; ++i) {
+        const CallRec& c = b->calls[size_t(g.ids[i])];
+        for (int64_t x : c.writes)
+          if (rs[x] == st || ws[x] == st) clash = true;
+        for (int64_t x : c.reads)
+          if (ws[x] == st) clash = true;
+      }
+      if (clash) continue;
       for (int64_t id : g.ids) {
         const CallRec& c = b->calls[size_t(id)];
-        gr.insert(gr.end(), c.reads.begin(), c.reads.end());
-        gw.insert(gw.end(), c.writes.begin(), c.writes.end());
+        for (int64_t x : c.reads) rs[x] = st;
+        for (int64_t x : c.writes) ws[x] = st;
       }
-      // Eq. (4) against every group taken so far
-      if (any_common(gw, taken_r) || any_common(gw, taken_w) || any_common(gr, taken_w)) continue;
-      taken_r.insert(gr.begin(), gr.end());
-      taken_w.insert(gw.begin(), gw.end());
       std::vector<int64_t> kept;
       for (int64_t id : g.ids) {
         const int64_t rows = b->calls[size_t(id)].rows;

@@ -87,6 +87,10 @@ def test_batcher_refusals():
     dep = (C.c_int64 * 1)(0)
     assert sub(q, 0, 1, -1, dep, 1, None, 0, None, 0) == abi.PIE_EINVAL      # not an earlier call
     assert sub(q, 0, 1, -1, None, 1, None, 0, None, 0) == abi.PIE_EINVAL     # NULL with a count
+    big = (C.c_int64 * 1)(1 << 26)
+    neg = (C.c_int64 * 1)(-1)
+    assert sub(q, 0, 1, -1, None, 0, big, 1, None, 0) == abi.PIE_ERANGE      # resource id too large
+    assert sub(q, 0, 1, -1, None, 0, None, 0, neg, 1) == abi.PIE_ERANGE      # negative resource id
     assert b.submit(q, 0, 1) == 0
     n, hh = C.c_int32(), C.c_int32()
     small = (C.c_int64 * 2)()
