@@ -309,8 +309,13 @@ def run_ours(args, ws, rank, local, pg):
             for p in passes]
     from programmable_paged_kv_gb300 import workspace_bytes
     ws_bytes = max(workspace_bytes(cdesc, metas[t]) for t in (0, total_steps - 1))
-    workspace = torch.empty(ws_bytes + 4096, dtype=torch.uint8, device=dev)
+    # two plan workspaces: step t's metadata upload (on a copy stream) overlaps
+    # step t-1's kernels; a workspace is rewritten only after the step that
+    # used it two steps earlier has finished on the compute stream
+    workspaces = [torch.empty(ws_bytes + 4096, dtype=torch.uint8, device=dev) for _ in range(2)]
     stream = torch.cuda.current_stream(dev)
+    copy_stream = torch.cuda.Stream(dev)
+    ws_free = [torch.cuda.Event(), torch.cuda.Event()]
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     # the attention kernel alone (recorded by the library around its launch)
@@ -319,7 +324,12 @@ def run_ours(args, ws, rank, local, pg):
     live = []
 
     def step(t, q, k, v, timed_ev=None, kernel_ev=None):
-        plan = ForwardPlan(cdesc, metas[t], workspace=workspace)
+        i = t % 2
+        copy_stream.wait_event(ws_free[i])
+        plan = ForwardPlan(cdesc, metas[t], workspace=workspaces[i], stream=copy_stream)
+        uploaded = torch.cuda.Event()
+        uploaded.record(copy_stream)
+        stream.wait_event(uploaded)
         plan.append_kv(q, k, v, q_rot, k_pool, v_pool, frozen, status)
         if timed_ev is not None:
             timed_ev[0].record(stream)
@@ -331,6 +341,7 @@ def run_ours(args, ws, rank, local, pg):
         if timed_ev is not None:
             timed_ev[1].record(stream)
         plan.fold(frozen, None, status)
+        ws_free[i].record(stream)
         live.append(plan)
         if len(live) > 4:
             live.pop(0).close()

@@ -2,11 +2,13 @@
 // carries an explicit position ID for RoPE and a slot of its lane's working
 // set where its K/V state is written).
 //
-// One CTA per row.  The row's D/2 rotation angles positions[r] * base^(-2i/d)
-// are evaluated once into shared memory (fp32 angle, CUDA's accurate
-// sincosf) and reused by every q and k head of the row.  Work is split into
-// 16-byte units so that every global load and store is one coalesced vector
-// access:
+// One CTA per row, or gridDim.y CTAs per row for passes of few rows (a decode
+// step's 64 rows would otherwise leave most SMs idle and each CTA several
+// dependent load rounds).  Each CTA evaluates the row's D/2 rotation angles
+// positions[r] * base^(-2i/d) once into shared memory (fp32 angle, CUDA's
+// accurate sincosf) and reuses them for its share of the row's q and k heads.
+// Work is split into 16-byte units so that every global load and store is one
+// coalesced vector access:
 //   * a rotation unit covers VEC elements of the low half [i, i+VEC) and the
 //     matching VEC elements of the high half [i+d/2, ...) of one head;
 //   * a copy unit moves VEC elements of one v head into the pool.
@@ -54,7 +56,9 @@ __global__ void __launch_bounds__(128) rope_scatter_kernel(
   const int k_units = write_kv ? Hkv * HALF_UNITS : 0;
   const int v_units = write_kv ? Hkv * FULL_UNITS : 0;
   const int total = q_units + k_units + v_units;
-  for (int u = threadIdx.x; u < total; u += blockDim.x) {
+  // this CTA's units: every gridDim.y-th run of blockDim.x units
+  const int stride = blockDim.x * gridDim.y;
+  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < total; u += stride) {
     if (u < q_units + k_units) {
       const bool is_q = u < q_units;
       const int uu = is_q ? u : u - q_units;
@@ -89,7 +93,9 @@ template <typename T, int D>
 static cudaError_t launch_rs(const pie_fwd_plan_t& p, const void* q, const void* k, const void* v,
                              void* q_rot, void* k_pool, void* v_pool, const int32_t* frozen,
                              uint32_t* status, cudaStream_t s) {
-  rope_scatter_kernel<T, D><<<p.N, 128, 0, s>>>(
+  // few rows (decode): split each row's units over 4 CTAs
+  const dim3 grid(p.N, p.N < 256 ? 4 : 1);
+  rope_scatter_kernel<T, D><<<grid, 128, 0, s>>>(
       p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
       static_cast<T*>(q_rot), static_cast<T*>(k_pool), static_cast<T*>(v_pool), frozen, status);
