@@ -35,21 +35,59 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
   const int nch = ce.mblock < 0 ? ce.nchunks
                                 : masked_chunks((m.list_len[ce.mblock] + tc_bn - 1) / tc_bn,
                                                 ce.nchunks, *m.mask_tiles, Hkv);
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
   float o[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-  float Ls = 0.f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nch; ++c) {
-      const int idx = ce.part_base + c * ce.stride + qi;
-      const float2 ml = m.part_ml[idx];
-      const float f = ex2(ml.x - M);
-      Ls = fmaf(f, ml.y, Ls);
-      const float* po = m.part_o + int64_t(idx) * D + lane * DPL;
+  float M = -INFINITY, Ls = 0.f;
+  if (nch <= 32) {
+    // lane c holds chunk c's (max, sum): the merged max and sum by warp
+    // reductions, then the chunks' outputs four at a time, their loads in flight
+    // together, each weighted by its lane's factor
+    const float2 ml = lane < nch ? m.part_ml[ce.part_base + lane * ce.stride + qi]
+                                 : make_float2(-INFINITY, 0.f);
+    M = ml.x;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[e] = fmaf(f, po[e], o[e]);
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float f = M == -INFINITY || ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+    float lp = f * ml.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(0xffffffffu, lp, off);
+    Ls = lp;
+    if (M != -INFINITY) {
+      for (int c0 = 0; c0 < nch; c0 += 4) {
+        float po[4][DPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u;
+          if (c < nch) {
+            const float* src = m.part_o + int64_t(ce.part_base + c * ce.stride + qi) * D + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) po[u][e] = src[e];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u;
+          const float fc = __shfl_sync(0xffffffffu, f, c & 31);
+          if (c < nch) {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[e] = fmaf(fc, po[u][e], o[e]);
+          }
+        }
+      }
+    }
+  } else {
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, m.part_ml[ce.part_base + c * ce.stride + qi].x);
+    if (M != -INFINITY) {
+      for (int c = 0; c < nch; ++c) {
+        const int idx = ce.part_base + c * ce.stride + qi;
+        const float2 ml = m.part_ml[idx];
+        const float f = ex2(ml.x - M);
+        Ls = fmaf(f, ml.y, Ls);
+        const float* po = m.part_o + int64_t(idx) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = fmaf(f, po[e], o[e]);
+      }
     }
   }
   const bool empty = !(Ls > 0.f);
