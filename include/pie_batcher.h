@@ -25,7 +25,10 @@
  *
  * Every function returns PIE_OK (0) or a negative PIE_E* code of pie_fwd.h
  * and changes nothing on error.  A batcher is not thread-safe: one control
- * thread owns it.  No CUDA call is made.
+ * thread owns it.  No CUDA call is made.  Ids are never reused: a completed
+ * call keeps a record of about 100 bytes (its dependency and resource lists
+ * are freed), so a long-lived control layer starts a new batcher when the
+ * record count matters.
  */
 #ifndef PIE_BATCHER_H_
 #define PIE_BATCHER_H_

@@ -310,7 +310,8 @@ int pie_batcher_complete(pie_batcher_t* b, const int64_t* calls, int32_t n) {
       b->state[size_t(calls[i])] = kDone;
       --b->in_flight;
       CallRec& c = b->calls[size_t(calls[i])];
-      std::vector<int64_t>().swap(c.reads);  // no longer needed
+      std::vector<int64_t>().swap(c.deps);  // no longer needed: only its state is read
+      std::vector<int64_t>().swap(c.reads);
       std::vector<int64_t>().swap(c.writes);
     }
   }
