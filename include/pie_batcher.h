@@ -53,7 +53,7 @@ void pie_batcher_destroy(pie_batcher_t* b);
  * its id is written to *queue_id (0, 1, 2, ...). */
 int pie_batcher_add_queue(pie_batcher_t* b, int32_t priority, int32_t* queue_id);
 
-/* Enqueue a call (Algorithm 2, lines 01 and 03).  rows >= 1 counts against
+/* Enqueue a call (Algorithm 2's arrival step).  rows >= 1 counts against
  * max_rows; key >= 0 names its working set (-1: none); deps are ids of earlier
  * calls; reads / writes are resource ids in [0, 2^26) (e.g. KV page ids; the
  * batcher keeps a table indexed by resource id), any order, duplicates
@@ -66,7 +66,7 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
                        const int64_t* reads, int32_t num_reads, const int64_t* writes,
                        int32_t num_writes, int64_t* call_id);
 
-/* Form and dispatch one batch (lines 05-11): its call ids in order go to
+/* Form and dispatch one batch (Algorithm 2's GPU-idle step): its call ids in order go to
  * calls[0..n), the lane of each call to lanes[0..n) (0, 1, ...), its handler
  * type to *handler, n to *num_calls (0 and handler -1 when no call is
  * eligible).  The calls count as in flight until completed.  capacity is the
@@ -74,7 +74,7 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
 int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32_t capacity,
                          int32_t* num_calls, int32_t* handler);
 
-/* Completion events (line 12): the calls have finished on the GPU, so calls
+/* Completion events (Algorithm 2's completion step): the calls have finished on the GPU, so calls
  * that depend on them become eligible.  Errors: PIE_EINVAL if a call is not in
  * flight (unknown, still queued or already completed); nothing is changed. */
 int pie_batcher_complete(pie_batcher_t* b, const int64_t* calls, int32_t n);

@@ -82,7 +82,7 @@ class Batcher:
         self.pending: Dict[int, List[int]] = {q: [] for q in priorities}  # queue -> ids, in order
         self.done: set = set()
 
-    # line 01/03: identify the queue and dependencies, enqueue in order
+    # arrival (Algorithm 2): identify the queue and dependencies, enqueue in order
     def submit(self, call: Call):
         assert call.id not in self.calls
         for d in call.deps:
@@ -90,7 +90,7 @@ class Batcher:
         self.calls[call.id] = call
         self.pending[call.queue].append(call.id)
 
-    # line 12: completions make dependents eligible
+    # completion (Algorithm 2): completions make dependents eligible
     def complete(self, ids):
         self.done.update(ids)
 
@@ -145,7 +145,7 @@ class Batcher:
                 break
         return out
 
-    # lines 05-11: one dispatch on a GPU-idle notification
+    # GPU idle (Algorithm 2): one dispatch
     def dispatch(self) -> Optional[Batch]:
         by_handler: Dict[int, List[List[int]]] = {}
         for q in self.pending:

@@ -78,7 +78,7 @@ struct pie_batcher {
     return true;
   }
 
-  // lines 06 and 08: the queue's ready head and its vertical group
+  // the queue's ready head and its vertical group (Algorithm 2)
   void group_of(int32_t q, Group* g) const {
     g->queue = q;
     g->ids.clear();
@@ -196,7 +196,7 @@ int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32
   *num_calls = 0;
   *handler = -1;
 
-  // lines 06 and 08: ready groups, bucketed by handler type; drop empty queues
+  // ready groups, bucketed by handler type; drop empty queues
   std::vector<std::vector<Group>> by_type(b->ordered.size());
   size_t keep = 0;
   for (size_t i = 0; i < b->active.size(); ++i) {
@@ -213,7 +213,8 @@ int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32
   }
   b->active.resize(keep);
 
-  // lines 07, 09, 10 per handler type; line 11 across types
+  // per handler type: priority order, Eq. (4) and the limits; then the oldest
+  // call decides between handler types
   std::vector<std::pair<int32_t, std::vector<int64_t>>> best_batch;  // (group index, kept ids)
   int64_t best_oldest = -1;
   int32_t best_type = -1;
