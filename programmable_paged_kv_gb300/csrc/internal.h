@@ -176,5 +176,8 @@ cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* ls
 // Records `msg` as the calling thread's last error (pie_fwd_last_error) and
 // returns `code`.
 int set_last_error(int code, const std::string& msg);
+// The calling thread's timing events of pie_fwd_set_timing_events (both NULL
+// when the hook is off).
+void timing_events(cudaEvent_t* start, cudaEvent_t* stop);
 
 }  // namespace pie

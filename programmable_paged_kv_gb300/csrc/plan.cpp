@@ -469,6 +469,15 @@ int pie_fwd_set_timing_events(void* start_event, void* stop_event) {
   return PIE_OK;
 }
 
+}  // extern "C"
+
+void pie::timing_events(cudaEvent_t* start, cudaEvent_t* stop) {
+  *start = g_ev_start;
+  *stop = g_ev_stop;
+}
+
+extern "C" {
+
 // One host plan per calling thread, reused so that its vectors keep their
 // capacity from one pass to the next (build_host_plan resets every field).
 static HostPlan& thread_host_plan() {
