@@ -644,7 +644,7 @@ def run_readout(args, local):
     vocabulary (fp32 synthetic logits), p, Z and lse.  Eight distinct logits
     buffers (262 MB, more than L2) are cycled so every step reads from HBM.
     Eager calls give the call time and, through the timing hook, the time of
-    the pass over the logits (the filter kernel); the eight calls captured in
+    the pass over the logits (the stream kernel); the eight calls captured in
     one CUDA graph and replayed give the device time per call without host
     launch costs (`value`)."""
     import torch
@@ -711,17 +711,17 @@ def run_readout(args, local):
     kmed = kms[len(kms) // 2] / 1e3
     dev_s = t2.elapsed_time(t3) / 1e3 / (reps * NB)
     byts = R * V * 4 + R * K * 8 + R * 8
-    fbytes = R * V * 4          # the filter kernel reads the logits once
+    fbytes = R * V * 4          # the stream kernel reads the logits once
     hbm, kind = peaks()
     line = {"workload": "readout_topk", "metric": "readout rows/s (top-256 of a 128,256-token "
             "distribution, p, Z, lse)", "unit": "rows/s", "value": R / dev_s,
             "ms_per_step": dev_s * 1e3, "steps": Kst, "warmup": Wm,
             "device_ms_per_call": dev_s * 1e3, "eager_call_ms_median": med * 1e3,
             "eager_ms_per_step": t0.elapsed_time(t1) / Kst, "eager_rows_per_s": R / med,
-            "filter_kernel_ms_median": kmed * 1e3, "alg_bytes": byts,
+            "stream_kernel_ms_median": kmed * 1e3, "alg_bytes": byts,
             "hbm_gbs": byts / dev_s / 1e9, "hbm_frac": byts / dev_s / 1e9 / hbm,
             "gpu_launches": 3 * (Kst + reps * NB),
-            "roofline": {"bound": "hbm", "kernel": "filter_kernel",
+            "roofline": {"bound": "hbm", "kernel": "stream_kernel",
                          "achieved": fbytes / kmed / 1e9, "peak": hbm, "unit": "GB/s",
                          "frac": fbytes / kmed / 1e9 / hbm, "traffic": None, "peak_kind": kind},
             "config": {"rows": R, "vocab": V, "k": K, "dtype": "f32",

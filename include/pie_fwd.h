@@ -310,8 +310,8 @@ void pie_fwd_adapter_plan_destroy(pie_fwd_adapter_plan_t* plan);
  * `start` on its stream right before its attention kernels (split-KV and/or
  * tensor-core) and `stop` right after them; the mask pre-pass and the
  * combine step fall outside.  Every pie_fwd_readout_topk call records them
- * around its pass over the logits (the filter kernel); the slice and merge
- * steps fall outside.  The events stay caller-owned; (NULL, NULL)
+ * around its pass over the logits (the stream kernel); the sample, slice and
+ * merge steps fall outside.  The events stay caller-owned; (NULL, NULL)
  * turns the hook off.  Returns PIE_EINVAL when exactly one is NULL. */
 int pie_fwd_set_timing_events(void* start_event, void* stop_event);
 

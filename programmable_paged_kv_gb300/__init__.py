@@ -83,7 +83,7 @@ def workspace_bytes(desc: abi.pie_fwd_desc, meta: _HostMeta) -> int:
 def set_timing_events(start=None, stop=None) -> None:
     """Have later attend calls on this thread record two timing-enabled
     torch.cuda.Event objects right around their attention kernels, and later
-    readout_topk calls around their filter kernel (pie_fwd_set_timing_events);
+    readout_topk calls around their stream kernel (pie_fwd_set_timing_events);
     no arguments turns it off."""
     for e in (start, stop):
         if e is not None and not e.cuda_event:

@@ -150,6 +150,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Programmatic dependent launch.  grid_dep_wait: wait until the grids this
+// one was launched behind have completed and their writes are visible (at
+// once when it was launched without the programmatic-serialization
+// attribute).  grid_dep_launch: let the grid launched behind this one begin
+// launching (it still waits in grid_dep_wait for this grid to complete).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 1-D bulk copy global -> shared through the TMA engine, completing on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

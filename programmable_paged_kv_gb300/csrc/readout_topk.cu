@@ -8,35 +8,42 @@
 // p = softmax(logits row); the k tokens of largest p, ties by smaller token
 // id; their p (not renormalised), Z = the sum of those p, and the natural-log
 // normaliser lse.  The pass is bound by HBM (the logits are read once, ~0.5 MB
-// per row at 128K fp32 tokens), so a row is cut into parts read by many CTAs:
-//   1. filter kernel, grid (rows, parts), 512 threads: a 16,384-token part
-//      into registers (32 tokens per thread, coalesced 16-byte loads), the
-//      part's max and sum of exp(x - max), and a short unsorted list of
-//      (key, token) candidates: every token at or above a lower bound on the
-//      part's k-th largest logit.  The bound is the k-th largest of the 512
-//      thread maxima (k distinct tokens reach it), found to within 1/4,096 of
-//      their range by one shared-memory histogram whose bins span exactly
-//      [min, max] of those maxima; about 2 % of a part is listed.  A part
-//      whose list would pass 512 entries (ties, flat rows) sets a flag;
-//   2. slice kernel, grid (rows, slices), 512 threads, only for flagged rows:
-//      a 8,192-token slice into shared memory as order-preserving 32-bit keys,
-//      its max and sum, then its exact k largest (a 4,096-bin histogram of the
-//      top 12 key bits finds the bucket of the k-th key; the keys in it or
-//      above are listed in token order and an exact radix select over the
-//      list, or over the whole slice when ties crowd the bucket, yields k
-//      (key, token) candidates);
-//   3. merge kernel, one CTA per row: over the row's candidates (the parts'
-//      lists, or the slices' k each), an exact radix select of the k-th
-//      largest key (12-, 10- and 10-bit passes) and, when that key has more
-//      copies than places, of the smallest tokens among them (two 10-bit
-//      passes); a bitonic sort of the k as 64-bit (key, ~token) words; the
-//      (max, sum) pairs merge into lse, and p = exp(x - lse) and Z follow.
-// Every token the row can return is a candidate: each part lists all of its
-// tokens at or above a bound that is at most the row's k-th largest logit,
-// and the row's top k lie in the union of its slices' top k.
+// per row at 128K fp32 tokens); four kernels, each after the first launched
+// to start while the one before drains:
+//   1. sample kernel, one CTA per row: a bound T on the row's candidates, the
+//      ceil(k / 4)-th largest (at least the 16th) of the logits of every 16th
+//      chunk of 128 tokens, to within 1/4,096 of the sample's range (one
+//      shared-memory histogram whose bins span [min, max] of the sample).
+//      About 16 s tokens reach T for the s-th sampled one (1,024 at k = 256);
+//   2. stream kernel, one CTA of 256 threads per 4,096 tokens of a row, no
+//      block barrier but one: every logit read once (16-byte loads, 16 per
+//      thread in registers); each warp's max and sum of exp(x - max); the
+//      tokens at or above T appended to the row's list at places taken by
+//      one atomic add per CTA;
+//   3. slice kernel, 512 threads, over the (row, slice) units of the rows
+//      whose list missed k tokens or passed its 4,096 places (ties, flat or
+//      masked rows, an unlucky sample): a 8,192-token slice into shared
+//      memory as order-preserving 32-bit keys, its max and sum, then its
+//      exact k largest (a 4,096-bin histogram of the top 12 key bits finds
+//      the bucket of the k-th key; the keys in it or above are listed in
+//      token order and an exact radix select over the list, or over the whole
+//      slice when ties crowd the bucket, yields k (key, token) candidates);
+//   4. merge kernel, one CTA per row: over the row's candidates (its list, or
+//      the slices' k each), a histogram whose 4,096 bins span the
+//      candidates' keys places each candidate of the bins down to the one of
+//      the k-th largest at its bin's first place plus its rank inside the bin
+//      (64-bit (key, ~token) words, so ties go to the smaller token); when
+//      those bins hold too many candidates, an exact radix select and a
+//      bitonic sort take over.  The (max, sum) pairs merge into lse, and
+//      p = exp(x - lse) and Z follow.
+// Every token the row can return is a candidate: a list holds every token at
+// or above T, and when at least k tokens reach T the row's top k all do; the
+// row's top k lie in the union of its slices' top k.
 
+#include <algorithm>
 #include <cmath>
 #include <string>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -51,13 +58,17 @@ constexpr int kMaxK = 256;
 constexpr int kMaxSlices = 32;           // vocab <= 262,144: the merge takes <= 8,192 candidates
 constexpr int kMergeThreads = 1024;
 constexpr int kListCap = 1024;           // keys the slice kernel's exact selection takes from a list
-constexpr int kPart = 16384;             // tokens per part of the filter kernel
-constexpr int kFThreads = 512;
-constexpr int kFPer = kPart / kFThreads; // tokens per thread, in registers
-constexpr int kFCap = 512;               // candidates a part may list (more: the row takes the slices)
-constexpr int kMaxParts = 16;            // vocab <= 262,144
-constexpr int kWin = 4096;               // bins of the thread-maxima histogram
-static_assert(kMaxParts * kFCap == kMaxSlices * kMaxK, "the merge holds either candidate set");
+constexpr int kChunk = 128;              // tokens per chunk of the sample
+constexpr int kSampleEvery = 16;         // one chunk in 16 is sampled
+constexpr int kSampleThreads = 1024;
+constexpr int kSamplePer = 16;           // sampled tokens per thread: vocab <= 262,144
+constexpr int kPart = 4096;              // tokens per CTA of the stream kernel
+constexpr int kStreamThreads = 256;
+constexpr int kStreamPer = kPart / kStreamThreads;  // tokens per thread, in registers
+constexpr int kRowCap = 4096;            // candidates a row may list (more: the row takes the slices)
+constexpr int kCntStride = 32;           // a row's count on a 128-byte line of its own
+static_assert(kRowCap <= kMaxSlices * kMaxK, "the merge holds either candidate set");
+static_assert(kSampleThreads * kSamplePer * kSampleEvery >= kMaxSlices * kSlice, "sample covers vocab");
 
 // Shared-memory position of slice token i: one pad word every 32 words, so
 // that thread t reading token t * 32 + c (its run) hits bank (t + c) % 32.
@@ -307,277 +318,329 @@ __device__ void gather_list(const uint32_t (&key)[E], Tok tok, uint32_t cb, Sele
   __syncthreads();
 }
 
+// Sample kernel, one CTA per row, 1,024 threads: the bound T of the row's
+// candidates and a zeroed candidate count.  The sample is every 16th chunk of
+// 128 tokens (chunks 0, 16, 32, ...); T is the smallest key of the bin that
+// holds the s-th largest sampled key, s = max(16, ceil(k / 4)), in a 4,096-bin
+// histogram whose bins span [min, max] of the sampled keys (0, every token,
+// when fewer than s tokens are sampled).  About 16 s tokens of the row reach
+// T (1,024 at k = 256), and at least s do: the sampled ones.  Any T is
+// correct once at least k tokens reach it, since the row's top k then all do;
+// a row with fewer, or with more than kRowCap, takes the slices.
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads, 1) sample_kernel(
+    const T* __restrict__ logits, int64_t ld, int vocab, int k, uint32_t* __restrict__ thr,
+    int* __restrict__ cnt) {
+  __shared__ int hist[4096];
+  __shared__ int warp_sums[32];
+  __shared__ int s_total;
+  __shared__ uint32_t s_kmax[32], s_kmin[32];
+  __shared__ uint32_t s_thr;
+  const int r = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const T* row = logits + int64_t(r) * ld;
+  grid_dep_launch();  // the stream kernel may start loading the logits now
+  for (int i = t; i < 4096; i += kSampleThreads) hist[i] = 0;
+  // sampled token i: chunk (i / 128) * 16, offset i % 128 (key 0: none)
+  uint32_t key[kSamplePer];
+  int have = 0;
+  uint32_t kx = 0u, kn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int e = 0; e < kSamplePer; ++e) {
+    const int i = e * kSampleThreads + t;
+    const int tok = (i / kChunk) * (kChunk * kSampleEvery) + i % kChunk;
+    key[e] = tok < vocab ? max(key_of(Elem<T>::to_f(row[tok])), 1u) : 0u;
+    if (key[e]) {
+      ++have;
+      kx = max(kx, key[e]);
+      kn = min(kn, key[e]);
+    }
+  }
+  kx = __reduce_max_sync(0xffffffffu, kx);
+  kn = __reduce_min_sync(0xffffffffu, kn);
+  have = __reduce_add_sync(0xffffffffu, have);
+  if (lane == 0) {
+    s_kmax[warp] = kx;
+    s_kmin[warp] = kn;
+    warp_sums[warp] = have;
+  }
+  __syncthreads();
+  const uint32_t KM = __reduce_max_sync(0xffffffffu, s_kmax[lane]);
+  const uint32_t Km = __reduce_min_sync(0xffffffffu, s_kmin[lane]);
+  const int nsamp = __reduce_add_sync(0xffffffffu, warp_sums[lane]);
+  const int sk = max(16, (k + 3) / 4);
+  uint32_t bound = 0u;
+  if (nsamp >= sk) {  // uniform
+    const uint32_t span = KM - Km;
+    const int sh = span < 4096u ? 0 : 20 - __clz(span);  // span >> sh < 4,096
+#pragma unroll
+    for (int e = 0; e < kSamplePer; ++e)
+      if (key[e]) atomicAdd(&hist[(KM - key[e]) >> sh], 1);
+    __syncthreads();
+    constexpr int per = 4096 / kSampleThreads;
+    int c[per], tot = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      c[q] = hist[t * per + q];
+      tot += c[q];
+    }
+    int acc = block_scan<kSampleThreads>(tot, warp_sums, &s_total);
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      if (acc < sk && sk <= acc + c[q]) {
+        const int64_t lo = int64_t(KM) - ((int64_t(t * per + q) + 1) << sh) + 1;
+        s_thr = lo < 0 ? 0u : uint32_t(lo);
+      }
+      acc += c[q];
+    }
+    __syncthreads();
+    bound = s_thr;
+  }
+  if (t == 0) {
+    thr[r] = bound;
+    cnt[r * kCntStride] = 0;
+  }
+}
+
+// Stream kernel, one CTA per 4,096-token part of a row, 256 threads: thread
+// t holds tokens (j * 256 + t) * W + e (j < 16 / W, e < W; W tokens per
+// 16-byte load).  Each warp writes its (max, sum of exp(x - max)) for the
+// row's normaliser, and the CTA lists its tokens at or above the row's bound
+// (compared as floats: the value of key T, -inf when T admits every token)
+// at places taken by one atomic add per CTA on the row's count (the warps'
+// shares by a scan of their totals); places past kRowCap are not written (the
+// count still grows, and the row takes the slices).
+// One part of the stream kernel; kFull: a whole 4,096-token part (no token
+// index checks), else the row's ragged last part (padding -inf, never listed).
+template <bool kFull, typename T>
+__device__ __forceinline__ void stream_part(const T* __restrict__ row, int n, int base, int r,
+                                            int slot, const uint32_t* __restrict__ thr,
+                                            int* __restrict__ cnt, uint2* __restrict__ cand,
+                                            float2* __restrict__ wstats, int* s_wt, int* s_base) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  constexpr int W = 16 / sizeof(T);
+  constexpr int J = kStreamPer / W;
+  constexpr float kL2e = 1.4426950408889634f;
+  auto live = [&](int j, int e) { return kFull || (j * kStreamThreads + t) * W + e < n; };
+  float v[kStreamPer];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int i0 = (j * kStreamThreads + t) * W;
+    if (kFull || i0 + W <= n) {
+      unpack16<T>(__ldg(reinterpret_cast<const uint4*>(row + i0)), v + j * W);
+    } else {
+#pragma unroll
+      for (int e = 0; e < W; ++e) v[j * W + e] = i0 + e < n ? Elem<T>::to_f(row[i0 + e]) : -INFINITY;
+    }
+  }
+  // the logits were written before the sample kernel started; the bound and
+  // the zeroed count are the sample kernel's
+  grid_dep_wait();
+  const uint32_t tk = thr[r];
+  const float thr_f = tk <= key_of(-INFINITY) ? -INFINITY : value_of(tk);
+  // ---- the warp's (max, sum): each thread's sum rescaled once to the warp max
+  static_assert(kStreamPer == 16, "the max tree and the four partial sums take 16 tokens");
+  const float m = max3(max3(max3(v[0], v[1], v[2]), max3(v[3], v[4], v[5]), max3(v[6], v[7], v[8])),
+                       max3(v[9], v[10], v[11]), max3(max3(v[12], v[13], v[14]), v[15], v[15]));
+  float sum = 0.f;
+  if (m != -INFINITY) {  // four independent partial sums
+    const float mb = m * kL2e;
+    float p4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kStreamPer; ++i) p4[i & 3] += ex2(fmaf(v[i], kL2e, -mb));
+    sum = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+  }
+  const uint32_t kw = __reduce_max_sync(0xffffffffu, m == -INFINITY ? 0u : key_of(m));
+  const float mw = kw == 0u ? -INFINITY : value_of(kw);
+  sum = m == -INFINITY ? 0.f : sum * ex2((m - mw) * kL2e);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane == 0) wstats[int64_t(slot) * (kStreamThreads / 32) + warp] = make_float2(mw, sum);
+  // ---- the tokens at or above the bound
+  int mine = 0;
+  if (m >= thr_f) {
+    int c4[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int e = 0; e < W; ++e) c4[(j * W + e) & 3] += (v[j * W + e] >= thr_f && live(j, e)) ? 1 : 0;
+    mine = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+  }
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_wt[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;  // the earlier warps' hits, the CTA's
+#pragma unroll
+  for (int w = 0; w < kStreamThreads / 32; ++w) {
+    const int c = s_wt[w];
+    before += w < warp ? c : 0;
+    total += c;
+  }
+  if (t == 0) *s_base = total ? atomicAdd(&cnt[r * kCntStride], total) : 0;
+  __syncthreads();
+  int pos = *s_base + before + incl - mine;
+  if (mine) {
+    uint2* out = cand + int64_t(r) * kRowCap;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int e = 0; e < W; ++e)
+        if (v[j * W + e] >= thr_f && live(j, e)) {
+          if (pos < kRowCap)
+            out[pos] = make_uint2(key_of(v[j * W + e]), uint32_t(base + (j * kStreamThreads + t) * W + e));
+          ++pos;
+        }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads) stream_kernel(
+    const T* __restrict__ logits, int64_t ld, int vocab, int nparts,
+    const uint32_t* __restrict__ thr, int* __restrict__ cnt, uint2* __restrict__ cand,
+    float2* __restrict__ wstats) {
+  __shared__ int s_wt[kStreamThreads / 32], s_base;
+  const int u = blockIdx.x, r = u / nparts, part = u % nparts;
+  const int base = part * kPart;
+  const int n = min(kPart, vocab - base);
+  const T* row = logits + int64_t(r) * ld + base;
+  if (n == kPart)
+    stream_part<true, T>(row, n, base, r, u, thr, cnt, cand, wstats, s_wt, &s_base);
+  else
+    stream_part<false, T>(row, n, base, r, u, thr, cnt, cand, wstats, s_wt, &s_base);
+  grid_dep_launch();
+}
+
+// A row takes the slices when its list missed the k or overflowed.
+__device__ __forceinline__ bool row_flagged(const int* cnt, int r, int kk) {
+  const int c = cnt[r * kCntStride];
+  return c < kk || c > kRowCap;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) slice_kernel(const T* __restrict__ logits, int64_t ld,
                                                           int vocab, int k, int nslices,
                                                           uint2* __restrict__ cand,
                                                           float2* __restrict__ stats,
-                                                          const int* __restrict__ ovf, int nparts) {
+                                                          const int* __restrict__ cnt, int units) {
   extern __shared__ uint32_t keys[];  // spos(kSlice) words
   __shared__ SelectSmem sel;
   __shared__ float2 red2[kThreads / 32];
   __shared__ __align__(16) uint32_t lkey[kListCap];
   __shared__ uint32_t ltok[kListCap];
-  const int r = blockIdx.x, s = blockIdx.y;
+  __shared__ int s_list[kThreads];
+  __shared__ int s_nlist;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  // only rows whose parts overflowed their lists come here
-  bool any = false;
-  for (int p = 0; p < nparts; ++p) any = any || ovf[int64_t(r) * nparts + p] != 0;
-  if (!any) return;
-  const int base = s * kSlice;
-  const int n = min(kSlice, vocab - base);
-  const int kk = min(k, n);
-  const T* row = logits + int64_t(r) * ld + base;
-
-  // ---- load: coalesced 16-byte vectors, keys into shared memory (to be
-  // re-read as each thread's contiguous run of tokens), the max and the sum
-  constexpr int W = 16 / sizeof(T);
+  grid_dep_wait();  // the counts are the stream kernel's
+  grid_dep_launch();
+  // the CTA's units (row, slice) = blockIdx.x + i * gridDim.x (i < kThreads),
+  // kept when a part of their row overflowed its list: one flag read each
+  if (t == 0) s_nlist = 0;
+  __syncthreads();
   {
-    float v[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer / W; ++j) {
-      const int i0 = (j * kThreads + t) * W;
-      float f[W];
-      if (i0 + W <= n) {
-        unpack16<T>(*reinterpret_cast<const uint4*>(row + i0), f);
-      } else {
-#pragma unroll
-        for (int e = 0; e < W; ++e) f[e] = i0 + e < n ? Elem<T>::to_f(row[i0 + e]) : -INFINITY;
-      }
-#pragma unroll
-      for (int e = 0; e < W; ++e) {
-        v[j * W + e] = f[e];
-        keys[spos(i0 + e)] = i0 + e < n ? key_of(f[e]) : 0u;  // padding below every token
-      }
-    }
-    // (max, sum of exp(x - max)) of the thread's values, then merged across
-    // the block in one reduction: (m1, s1) + (m2, s2) -> (m, s1 e^(m1-m) + s2 e^(m2-m))
-    constexpr float kL2e = 1.4426950408889634f;
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) m = fmaxf(m, v[i]);
-    float sum = 0.f;
-    if (m != -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) sum += ex2((v[i] - m) * kL2e);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-      const float so = __shfl_xor_sync(0xffffffffu, sum, off);
-      const float mm = fmaxf(m, mo);
-      sum = (m == -INFINITY ? 0.f : sum * ex2((m - mm) * kL2e)) +
-            (mo == -INFINITY ? 0.f : so * ex2((mo - mm) * kL2e));
-      m = mm;
-    }
-    if (lane == 0) red2[warp] = make_float2(m, sum);
-    __syncthreads();
-    if (t == 0) {
-      float M = -INFINITY, S = 0.f;
-      for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, red2[w].x);
-      for (int w = 0; w < kThreads / 32; ++w)
-        if (red2[w].x != -INFINITY) S += red2[w].y * ex2((red2[w].x - M) * kL2e);
-      stats[int64_t(r) * nslices + s] = make_float2(M, S);
-    }
+    const int u = blockIdx.x + t * gridDim.x;
+    if (u < units && row_flagged(cnt, u / nslices, min(k, vocab)))
+      s_list[atomicAdd(&s_nlist, 1)] = u;
   }
-  // ---- each thread's run of 32 consecutive tokens, in registers
-  uint32_t key[kPer];
+  __syncthreads();
+  const int nlist = s_nlist;
+  for (int li = 0; li < nlist; ++li) {
+    __syncthreads();  // shared memory of the previous unit
+    const int r = s_list[li] / nslices, s = s_list[li] % nslices;
+    const int base = s * kSlice;
+    const int n = min(kSlice, vocab - base);
+    const int kk = min(k, n);
+    const T* row = logits + int64_t(r) * ld + base;
+
+    // ---- load: coalesced 16-byte vectors, keys into shared memory (to be
+    // re-read as each thread's contiguous run of tokens), the max and the sum
+    constexpr int W = 16 / sizeof(T);
+    {
+      float v[kPer];
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) key[i] = keys[spos(t * kPer + i)];
-  uint2* out = cand + (int64_t(r) * nslices + s) * k;
-  // ---- one coarse pass finds the 4,096-bin bucket of the kk-th key; the keys
-  // in it or above (a few hundred for a peaked distribution) are copied, in
-  // token order, to a short list, and the exact selection runs on the list
-  int count_ge = 0;
-  const uint32_t cb = coarse_bin<kThreads, kPer>(key, kk, sel, count_ge);
-  if (count_ge <= kListCap) {
-    gather_list<kThreads, kPer>(key, TokRun{uint32_t(base + t * kPer)}, cb, sel, lkey, ltok);
-    constexpr int E2 = kListCap / kThreads;
-    uint32_t lk[E2], lt[E2];
+      for (int j = 0; j < kPer / W; ++j) {
+        const int i0 = (j * kThreads + t) * W;
+        float f[W];
+        if (i0 + W <= n) {
+          unpack16<T>(*reinterpret_cast<const uint4*>(row + i0), f);
+        } else {
 #pragma unroll
-    for (int e = 0; e < E2; ++e) {
-      const int i = t * E2 + e;
-      lk[e] = i < count_ge ? lkey[i] : 0u;
-      lt[e] = i < count_ge ? ltok[i] : 0u;
+          for (int e = 0; e < W; ++e) f[e] = i0 + e < n ? Elem<T>::to_f(row[i0 + e]) : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+          v[j * W + e] = f[e];
+          keys[spos(i0 + e)] = i0 + e < n ? key_of(f[e]) : 0u;  // padding below every token
+        }
+      }
+      // (max, sum of exp(x - max)) of the thread's values, then merged across
+      // the block in one reduction: (m1, s1) + (m2, s2) -> (m, s1 e^(m1-m) + s2 e^(m2-m))
+      constexpr float kL2e = 1.4426950408889634f;
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) m = fmaxf(m, v[i]);
+      float sum = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) sum += ex2((v[i] - m) * kL2e);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float so = __shfl_xor_sync(0xffffffffu, sum, off);
+        const float mm = fmaxf(m, mo);
+        sum = (m == -INFINITY ? 0.f : sum * ex2((m - mm) * kL2e)) +
+              (mo == -INFINITY ? 0.f : so * ex2((mo - mm) * kL2e));
+        m = mm;
+      }
+      if (lane == 0) red2[warp] = make_float2(m, sum);
+      __syncthreads();
+      if (t == 0) {
+        float M = -INFINITY, S = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, red2[w].x);
+        for (int w = 0; w < kThreads / 32; ++w)
+          if (red2[w].x != -INFINITY) S += red2[w].y * ex2((red2[w].x - M) * kL2e);
+        stats[int64_t(r) * nslices + s] = make_float2(M, S);
+      }
     }
-    int need_eq = 0;
-    const uint32_t thr = select_kth<kThreads, E2>(lk, kk, sel, need_eq);
-    emit_selected<kThreads, E2>(lk, TokList<E2>{lt}, thr, need_eq, sel, out);
-  } else {
-    // ties or a flat distribution crowd the bucket: select over all keys
-    int need_eq = 0;
-    const uint32_t thr = select_kth<kThreads, kPer>(key, kk, sel, need_eq);
-    emit_selected<kThreads, kPer>(key, TokRun{uint32_t(base + t * kPer)}, thr, need_eq, sel, out);
+    // ---- each thread's run of 32 consecutive tokens, in registers
+    uint32_t key[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) key[i] = keys[spos(t * kPer + i)];
+    uint2* out = cand + (int64_t(r) * nslices + s) * k;
+    // ---- one coarse pass finds the 4,096-bin bucket of the kk-th key; the keys
+    // in it or above (a few hundred for a peaked distribution) are copied, in
+    // token order, to a short list, and the exact selection runs on the list
+    int count_ge = 0;
+    const uint32_t cb = coarse_bin<kThreads, kPer>(key, kk, sel, count_ge);
+    if (count_ge <= kListCap) {
+      gather_list<kThreads, kPer>(key, TokRun{uint32_t(base + t * kPer)}, cb, sel, lkey, ltok);
+      constexpr int E2 = kListCap / kThreads;
+      uint32_t lk[E2], lt[E2];
+#pragma unroll
+      for (int e = 0; e < E2; ++e) {
+        const int i = t * E2 + e;
+        lk[e] = i < count_ge ? lkey[i] : 0u;
+        lt[e] = i < count_ge ? ltok[i] : 0u;
+      }
+      int need_eq = 0;
+      const uint32_t thr = select_kth<kThreads, E2>(lk, kk, sel, need_eq);
+      emit_selected<kThreads, E2>(lk, TokList<E2>{lt}, thr, need_eq, sel, out);
+    } else {
+      // ties or a flat distribution crowd the bucket: select over all keys
+      int need_eq = 0;
+      const uint32_t thr = select_kth<kThreads, kPer>(key, kk, sel, need_eq);
+      emit_selected<kThreads, kPer>(key, TokRun{uint32_t(base + t * kPer)}, thr, need_eq, sel, out);
+    }
   }
 }
 
 // 64-bit words compared as the sort order: key, then smaller token first.
 __device__ __forceinline__ unsigned long long sort_word(uint32_t key, uint32_t tok) {
   return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - tok);
-}
-
-// Filter kernel, grid (rows, parts), 512 threads: one 16,384-token part of a
-// row, 32 tokens per thread in registers, thread t holding tokens
-// (j * 512 + t) * W + e (j < 32 / W, e < W; W tokens per 16-byte load).
-//  - The thread's max and sum of exp(x - max), merged over the block: the
-//    part's (max, sum) for the row's normaliser.
-//  - The kk-th largest of the thread maxima (kk = min(k, part size)) is at
-//    most the part's kk-th largest logit, hence at most the row's k-th
-//    largest.  A 4,096-bin histogram of the maxima' keys, bins of width
-//    (range of the maxima) / 4,096 counted from the largest, gives the bin of
-//    that maximum; thr = the smallest key of the bin, a bound as good as the
-//    maximum itself to within one bin.
-//  - Every token with key >= thr is listed as (key, token) -- in thread order,
-//    not token order -- through one block scan of per-thread hit counts.  A
-//    list longer than kFCap sets the part's flag and the row takes the slices.
-template <typename T>
-__global__ void __launch_bounds__(kFThreads, 2) filter_kernel(
-    const T* __restrict__ logits, int64_t ld, int vocab, int k, int nparts,
-    uint2* __restrict__ cand, int* __restrict__ count, float2* __restrict__ stats,
-    int* __restrict__ ovf) {
-  __shared__ int hist[kWin];
-  __shared__ int warp_sums[32];
-  __shared__ int s_total;
-  __shared__ uint32_t s_kmax[kFThreads / 32], s_kmin[kFThreads / 32];
-  __shared__ float2 red2[kFThreads / 32];
-  __shared__ uint32_t s_thr;
-  const int r = blockIdx.x, part = blockIdx.y;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int base = part * kPart;
-  const int n = min(kPart, vocab - base);
-  const int kk = min(k, n);
-  const T* row = logits + int64_t(r) * ld + base;
-  constexpr int W = 16 / sizeof(T);
-  constexpr int J = kFPer / W;
-  constexpr float kL2e = 1.4426950408889634f;
-  const bool full = n == kPart;
-  float v[kFPer];
-  if (full) {
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-      unpack16<T>(__ldg(reinterpret_cast<const uint4*>(row + (j * kFThreads + t) * W)), v + j * W);
-  } else {
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int i0 = (j * kFThreads + t) * W;
-      if (i0 + W <= n) {
-        unpack16<T>(__ldg(reinterpret_cast<const uint4*>(row + i0)), v + j * W);
-      } else {
-#pragma unroll
-        for (int e = 0; e < W; ++e) v[j * W + e] = i0 + e < n ? Elem<T>::to_f(row[i0 + e]) : -INFINITY;
-      }
-    }
-  }
-  for (int i = t; i < kWin; i += kFThreads) hist[i] = 0;
-  // ---- the thread's (max, sum of exp(x - max)) and its max's key
-  float m = max3(v[0], v[1], v[2]);
-#pragma unroll
-  for (int i = 3; i + 1 < kFPer; i += 2) m = max3(m, v[i], v[i + 1]);
-  m = fmaxf(m, v[kFPer - 1]);
-  const bool tvalid = t * W < n;  // the thread holds at least one token
-  const uint32_t tk = tvalid ? key_of(m) : 0u;
-  float sum = 0.f;
-  if (m != -INFINITY) {
-    const float mb = m * kL2e;
-#pragma unroll
-    for (int i = 0; i < kFPer; ++i) sum += ex2(fmaf(v[i], kL2e, -mb));
-  }
-  uint32_t kmax = tk, kmin = tvalid ? tk : 0xFFFFFFFFu;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-    const float so = __shfl_xor_sync(0xffffffffu, sum, off);
-    const float mm = fmaxf(m, mo);
-    sum = (m == -INFINITY ? 0.f : sum * ex2((m - mm) * kL2e)) +
-          (mo == -INFINITY ? 0.f : so * ex2((mo - mm) * kL2e));
-    m = mm;
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
-  }
-  if (lane == 0) {
-    red2[warp] = make_float2(m, sum);
-    s_kmax[warp] = kmax;
-    s_kmin[warp] = kmin;
-  }
-  __syncthreads();
-  // ---- thr: the smallest key of the histogram bin that holds the kk-th
-  // largest thread maximum (0, every token, when fewer threads hold tokens)
-  uint32_t KM = 0u, Km = 0xFFFFFFFFu;
-#pragma unroll
-  for (int w = 0; w < kFThreads / 32; ++w) {
-    KM = max(KM, s_kmax[w]);
-    Km = min(Km, s_kmin[w]);
-  }
-  const int holders = min(kFThreads, (n + W - 1) / W);
-  uint32_t thr = 0u;
-  if (holders >= kk) {  // uniform over the block
-    const uint32_t span = KM - Km;
-    const int sh = span < uint32_t(kWin) ? 0 : 20 - __clz(span);  // span >> sh < 4,096
-    if (tvalid) atomicAdd(&hist[(KM - tk) >> sh], 1);
-    __syncthreads();
-    constexpr int per = kWin / kFThreads;
-    int c = 0;
-#pragma unroll
-    for (int q = 0; q < per; ++q) c += hist[t * per + q];
-    const int excl = block_scan<kFThreads>(c, warp_sums, &s_total);
-    if (excl < kk && kk <= excl + c) {
-      int acc = excl, b = t * per;
-      for (int q = 0; q < per; ++q) {
-        acc += hist[t * per + q];
-        if (acc >= kk) {
-          b = t * per + q;
-          break;
-        }
-      }
-      const int64_t lo = int64_t(KM) - ((int64_t(b) + 1) << sh) + 1;
-      s_thr = lo < 0 ? 0u : uint32_t(lo);
-    }
-    __syncthreads();
-    thr = s_thr;
-  }
-  // ---- the tokens at or above thr (compared as floats: thr_f is the value
-  // of key thr, -inf when thr admits every token), counted, placed by a block
-  // scan, then written; padding (tail part) never counts
-  const float thr_f = thr <= key_of(-INFINITY) ? -INFINITY : value_of(thr);
-  int mine = 0;
-  if (tvalid && tk >= thr) {
-    if (full) {
-#pragma unroll
-      for (int i = 0; i < kFPer; ++i) mine += v[i] >= thr_f;
-    } else {
-#pragma unroll
-      for (int j = 0; j < J; ++j)
-#pragma unroll
-        for (int e = 0; e < W; ++e) mine += (j * kFThreads + t) * W + e < n && v[j * W + e] >= thr_f;
-    }
-  }
-  int pos = block_scan<kFThreads>(mine, warp_sums, &s_total);
-  const int total = s_total;
-  const int64_t slot = int64_t(r) * nparts + part;
-  if (total > kFCap || total < kk) {  // uniform: the row takes the slices
-    if (t == 0) ovf[slot] = 1;
-    return;
-  }
-  if (mine) {
-    uint2* out = cand + slot * kFCap;
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-#pragma unroll
-      for (int e = 0; e < W; ++e) {
-        const int i = (j * kFThreads + t) * W + e;
-        if (v[j * W + e] >= thr_f && (full || i < n))
-          out[pos++] = make_uint2(key_of(v[j * W + e]), uint32_t(base + i));
-      }
-  }
-  if (t == 0) {
-    float M = -INFINITY, S = 0.f;
-    for (int w = 0; w < kFThreads / 32; ++w) M = fmaxf(M, red2[w].x);
-    for (int w = 0; w < kFThreads / 32; ++w)
-      if (red2[w].x != -INFINITY) S += red2[w].y * ex2((red2[w].x - M) * kL2e);
-    stats[slot] = make_float2(M, S);
-    count[slot] = total;
-    ovf[slot] = 0;
-  }
 }
 
 // Merge, one CTA per row, over the row's candidates: the parts' lists, or
@@ -600,8 +663,8 @@ constexpr int kMergeList = 2048;
 
 __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
     const uint2* __restrict__ cand8, const float2* __restrict__ stats8, int nslices,
-    const uint2* __restrict__ candf, const int* __restrict__ countf,
-    const float2* __restrict__ statsf, int nparts, const int* __restrict__ ovf, int vocab, int k,
+    const uint2* __restrict__ candr, const int* __restrict__ cnt,
+    const float2* __restrict__ wstats, int nparts, int vocab, int k,
     int32_t* __restrict__ ids, float* __restrict__ probs, float* __restrict__ z,
     float* __restrict__ lse_out) {
   constexpr int E = kMaxSlices * kMaxK / kMergeThreads;  // candidates per thread
@@ -610,23 +673,40 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
   __shared__ unsigned long long wl[kMergeList];
   __shared__ uint32_t s_kmax[NW], s_kmin[NW];
   __shared__ float red[NW];
+  static_assert(NW == 32, "one warp entry per lane");
   __shared__ float s_lse;
   __shared__ int s_b, s_above, s_m;
   const int r = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  bool slices = false;
-  for (int p = 0; p < nparts; ++p) slices = slices || ovf[int64_t(r) * nparts + p] != 0;
-  // ---- the row's normaliser from the (max, sum) pairs
-  if (warp == 0) {
-    const int nst = slices ? nslices : nparts;
-    const float2* st_row = slices ? stats8 + int64_t(r) * nslices : statsf + int64_t(r) * nparts;
-    const float2 st = lane < nst ? st_row[lane] : make_float2(-INFINITY, 0.f);
-    float M = st.x;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float S = st.x == -INFINITY ? 0.f : st.y * expf(st.x - M);
+  grid_dep_wait();  // the lists, counts and slices of the kernels before
+  const bool slices = row_flagged(cnt, r, min(k, vocab));
+  // ---- the row's normaliser from its (max, sum) pairs, one per thread
+  {
+    const int np = slices ? nslices : nparts * (kStreamThreads / 32);
+    const float2* st_row =
+        slices ? stats8 + int64_t(r) * nslices : wstats + int64_t(r) * nparts * (kStreamThreads / 32);
+    float M = -INFINITY, S = 0.f;
+    for (int i = t; i < np; i += kMergeThreads) {  // rows of 2,048 pairs and more: fold
+      const float2 st = st_row[i];
+      const float mm = fmaxf(M, st.x);
+      if (mm != -INFINITY) S = S * expf(M - mm) + st.y * expf(st.x - mm);
+      M = mm;
+    }
+    const uint32_t kb = __reduce_max_sync(0xffffffffu, M == -INFINITY ? 0u : key_of(M));
+    if (lane == 0) s_kmax[warp] = kb;
+    __syncthreads();
+    const uint32_t kr = __reduce_max_sync(0xffffffffu, s_kmax[lane]);
+    const float MR = kr == 0u ? -INFINITY : value_of(kr);
+    S = M == -INFINITY ? 0.f : S * expf(M - MR);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-    if (lane == 0) s_lse = M + logf(S);
+    if (lane == 0) red[warp] = S;
+    __syncthreads();
+    if (warp == 0) {
+      float SR = red[lane];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) SR += __shfl_xor_sync(0xffffffffu, SR, off);
+      if (lane == 0) s_lse = MR + logf(SR);
+    }
   }
   // ---- the candidates
   uint32_t key[E], tok[E];
@@ -643,15 +723,14 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
       }
     }
   } else {
-    const int p = (t * E) / kFCap;  // E divides kFCap: one part per thread
-    const int n_p = p < nparts ? countf[int64_t(r) * nparts + p] : 0;
-    const uint2* src = candf + (int64_t(r) * nparts + p) * kFCap;
+    const int n_r = cnt[r * kCntStride];  // at most kRowCap here
+    const uint2* src = candr + int64_t(r) * kRowCap;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int c = (t * E + e) % kFCap;
+      const int c = e * kMergeThreads + t;
       key[e] = 0u;
       tok[e] = 0u;
-      if (c < n_p) {
+      if (c < n_r) {
         const uint2 w = src[c];
         key[e] = w.x;
         tok[e] = w.y;
@@ -690,13 +769,13 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
     if (key[e] != 0u) atomicAdd(&sel.hist[(KM - key[e]) >> sh], 1);
   __syncthreads();
   constexpr int per = 4096 / kMergeThreads;
-  int c[per], cnt = 0;
+  int c[per], mine_bins = 0;
 #pragma unroll
   for (int q = 0; q < per; ++q) {
     c[q] = sel.hist[t * per + q];
-    cnt += c[q];
+    mine_bins += c[q];
   }
-  int acc = block_scan<kMergeThreads>(cnt, sel.warp_sums, &sel.total);
+  int acc = block_scan<kMergeThreads>(mine_bins, sel.warp_sums, &sel.total);
 #pragma unroll
   for (int q = 0; q < per; ++q) {  // first places in the order, in place
     if (acc < k && k <= acc + c[q]) {
@@ -790,14 +869,40 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
   }
 }
 
+// Launch behind the previous kernel of the stream; with pdl, programmatic
+// serialization: the kernel may start before that one completes and waits for
+// it in grid_dep_wait.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+static int num_sms() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
 static int nslices_of(int vocab) { return (vocab + kSlice - 1) / kSlice; }
 
 static int nparts_of(int vocab) { return (vocab + kPart - 1) / kPart; }
 
-// workspace: slice candidates and (max, sum); part lists, their lengths and
-// (max, sum); the parts' overflow flags
+// workspace: slice candidates and (max, sum); the rows' candidate lists,
+// counts and bounds; the warps' (max, sum) pairs
 struct RoLayout {
-  size_t cand8, stats8, candf, countf, statsf, ovf, total;
+  size_t cand8, stats8, candr, cnt, thr, wstats, total;
 };
 static RoLayout ro_layout(int rows, int vocab, int k) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -805,11 +910,11 @@ static RoLayout ro_layout(int rows, int vocab, int k) {
   RoLayout Y;
   Y.cand8 = 0;
   Y.stats8 = al(Y.cand8 + R * ns * k * sizeof(uint2));
-  Y.candf = al(Y.stats8 + R * ns * sizeof(float2));
-  Y.countf = al(Y.candf + R * np * kFCap * sizeof(uint2));
-  Y.statsf = al(Y.countf + R * np * sizeof(int));
-  Y.ovf = al(Y.statsf + R * np * sizeof(float2));
-  Y.total = al(Y.ovf + R * np * sizeof(int));
+  Y.candr = al(Y.stats8 + R * ns * sizeof(float2));
+  Y.cnt = al(Y.candr + R * kRowCap * sizeof(uint2));
+  Y.thr = al(Y.cnt + R * kCntStride * sizeof(int));
+  Y.wstats = al(Y.thr + R * sizeof(uint32_t));
+  Y.total = al(Y.wstats + R * np * (kStreamThreads / 32) * sizeof(float2));
   return Y;
 }
 static size_t ws_bytes_of(int rows, int vocab, int k) { return ro_layout(rows, vocab, k).total; }
@@ -861,10 +966,10 @@ extern "C" int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t r
   const ro::RoLayout Y = ro::ro_layout(rows, vocab, k);
   uint2* cand8 = reinterpret_cast<uint2*>(w + Y.cand8);
   float2* stats8 = reinterpret_cast<float2*>(w + Y.stats8);
-  uint2* candf = reinterpret_cast<uint2*>(w + Y.candf);
-  int* countf = reinterpret_cast<int*>(w + Y.countf);
-  float2* statsf = reinterpret_cast<float2*>(w + Y.statsf);
-  int* ovf = reinterpret_cast<int*>(w + Y.ovf);
+  uint2* candr = reinterpret_cast<uint2*>(w + Y.candr);
+  int* cnt = reinterpret_cast<int*>(w + Y.cnt);
+  uint32_t* thr = reinterpret_cast<uint32_t*>(w + Y.thr);
+  float2* wstats = reinterpret_cast<float2*>(w + Y.wstats);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t smem1 = sizeof(uint32_t) * (ro::kSlice + ro::kSlice / 32);
   static bool configured = false;
@@ -874,30 +979,35 @@ extern "C" int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t r
                          int(smem1));
     configured = true;
   }
-  // parts filter; rows whose parts overflowed go through the slices; merge
-  const dim3 g0(rows, np), g1(rows, ns);
+  // the rows' bounds from a sample; one pass over the logits lists the
+  // candidates; rows whose lists missed or overflowed go through the slices;
+  // the merge
+  const int units = rows * np;
+  const int units1 = rows * ns;
+  const int g1 = std::max(std::min(units1, 2 * ro::num_sms()), (units1 + ro::kThreads - 1) / ro::kThreads);
   cudaEvent_t ev0, ev1;
   timing_events(&ev0, &ev1);
-  if (ev0) cudaEventRecord(ev0, s);
-  if (dtype == PIE_BF16) {
-    ro::filter_kernel<__nv_bfloat16><<<g0, ro::kFThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(logits), ld, vocab, k, np, candf, countf, statsf, ovf);
+  // each kernel after the first starts while the one before drains (it waits
+  // for it before reading its results); with timing events between them, in
+  // plain stream order
+  const bool pdl = ev0 == nullptr;
+  auto run = [&](auto* x) -> cudaError_t {
+    using T = std::remove_const_t<std::remove_pointer_t<decltype(x)>>;
+    ro::sample_kernel<T><<<rows, ro::kSampleThreads, 0, s>>>(x, ld, vocab, k, thr, cnt);
+    if (ev0) cudaEventRecord(ev0, s);
+    cudaError_t e = ro::launch_dependent(ro::stream_kernel<T>, dim3(units), dim3(ro::kStreamThreads),
+                                         0, s, pdl, x, ld, vocab, np, thr, cnt, candr, wstats);
     if (ev1) cudaEventRecord(ev1, s);
-    ro::slice_kernel<__nv_bfloat16><<<g1, ro::kThreads, smem1, s>>>(
-        static_cast<const __nv_bfloat16*>(logits), ld, vocab, k, ns, cand8, stats8, ovf, np);
-  } else {
-    ro::filter_kernel<float><<<g0, ro::kFThreads, 0, s>>>(
-        static_cast<const float*>(logits), ld, vocab, k, np, candf, countf, statsf, ovf);
-    if (ev1) cudaEventRecord(ev1, s);
-    ro::slice_kernel<float><<<g1, ro::kThreads, smem1, s>>>(
-        static_cast<const float*>(logits), ld, vocab, k, ns, cand8, stats8, ovf, np);
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) {
-    ro::merge_kernel<<<rows, ro::kMergeThreads, 0, s>>>(cand8, stats8, ns, candf, countf, statsf, np,
-                                                        ovf, vocab, k, ids, probs, z, lse);
-    e = cudaGetLastError();
-  }
+    if (e == cudaSuccess)
+      e = ro::launch_dependent(ro::slice_kernel<T>, dim3(g1), dim3(ro::kThreads), smem1, s, pdl, x, ld,
+                               vocab, k, ns, cand8, stats8, cnt, units1);
+    if (e == cudaSuccess)
+      e = ro::launch_dependent(ro::merge_kernel, dim3(rows), dim3(ro::kMergeThreads), 0, s, pdl, cand8,
+                               stats8, ns, candr, cnt, wstats, np, vocab, k, ids, probs, z, lse);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+  };
+  const cudaError_t e = dtype == PIE_BF16 ? run(static_cast<const __nv_bfloat16*>(logits))
+                                          : run(static_cast<const float*>(logits));
   if (e != cudaSuccess) return set_last_error(PIE_ECUDA, std::string("readout launch: ") + cudaGetErrorString(e));
   return PIE_OK;
 }
