@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
     fence_barrier_init();
   }
   __syncthreads();
+  // set-up above overlaps the kernel before (RoPE and scatter of this pass's
+  // K/V and queries); everything below reads its results
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == C::WARPS) {
     // ---------------- producer warp: TMA bulk copies of K/V pages ----------
@@ -371,11 +375,11 @@ static cudaError_t launch_dec(const pie_fwd_plan_t& p, const void* q_rot, const 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attend_decode_kernel<T, D, NQ><<<p.num_dec_items, C::THREADS, C::SMEM, s>>>(
-      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.desc.page_size,
-      p.desc.sm_scale * kLog2e, static_cast<const T*>(q_rot), static_cast<const T*>(k_pool),
-      static_cast<const T*>(v_pool), mask_words, status);
-  return cudaGetLastError();
+  return launch_dependent(attend_decode_kernel<T, D, NQ>, dim3(p.num_dec_items), dim3(C::THREADS),
+                          C::SMEM, s, true, p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
+                          p.desc.page_size, p.desc.sm_scale * kLog2e, static_cast<const T*>(q_rot),
+                          static_cast<const T*>(k_pool), static_cast<const T*>(v_pool), mask_words,
+                          status);
 }
 
 template <typename T, int D>

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
                                                       T* out_readout, float* lse_readout,
                                                       T* out_all, float* lse_all) {
   constexpr int DPL = D / 32;
+  grid_dep_wait();  // the attention kernels' partial states
+  grid_dep_launch();
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int targets = R + (with_all ? N : 0);
@@ -110,11 +112,10 @@ static cudaError_t launch_comb(const pie_fwd_plan_t& p, void* out_readout, float
   const int with_all = (out_all || lse_all) ? 1 : 0;
   const int64_t warps = int64_t(p.R + (with_all ? p.N : 0)) * p.desc.num_q_heads;
   if (warps == 0) return cudaSuccess;
-  combine_kernel<T, D><<<int((warps + 3) / 4), 128, 0, s>>>(
-      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
-      tc_kv_tile(p.tc_nt), static_cast<T*>(out_readout), lse_readout, static_cast<T*>(out_all),
-      lse_all);
-  return cudaGetLastError();
+  return launch_dependent(combine_kernel<T, D>, dim3(int((warps + 3) / 4)), dim3(128), 0, s, true,
+                          p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
+                          tc_kv_tile(p.tc_nt), static_cast<T*>(out_readout), lse_readout,
+                          static_cast<T*>(out_all), lse_all);
 }
 
 cudaError_t launch_combine(const pie_fwd_plan_t& p, void* out_readout, float* lse_readout,

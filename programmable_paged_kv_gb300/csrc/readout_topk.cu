@@ -869,25 +869,6 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
   }
 }
 
-// Launch behind the previous kernel of the stream; with pdl, programmatic
-// serialization: the kernel may start before that one completes and waits for
-// it in grid_dep_wait.
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                    cudaStream_t s, bool pdl, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
 static int num_sms() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -995,14 +976,14 @@ extern "C" int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t r
     using T = std::remove_const_t<std::remove_pointer_t<decltype(x)>>;
     ro::sample_kernel<T><<<rows, ro::kSampleThreads, 0, s>>>(x, ld, vocab, k, thr, cnt);
     if (ev0) cudaEventRecord(ev0, s);
-    cudaError_t e = ro::launch_dependent(ro::stream_kernel<T>, dim3(units), dim3(ro::kStreamThreads),
+    cudaError_t e = launch_dependent(ro::stream_kernel<T>, dim3(units), dim3(ro::kStreamThreads),
                                          0, s, pdl, x, ld, vocab, np, thr, cnt, candr, wstats);
     if (ev1) cudaEventRecord(ev1, s);
     if (e == cudaSuccess)
-      e = ro::launch_dependent(ro::slice_kernel<T>, dim3(g1), dim3(ro::kThreads), smem1, s, pdl, x, ld,
+      e = launch_dependent(ro::slice_kernel<T>, dim3(g1), dim3(ro::kThreads), smem1, s, pdl, x, ld,
                                vocab, k, ns, cand8, stats8, cnt, units1);
     if (e == cudaSuccess)
-      e = ro::launch_dependent(ro::merge_kernel, dim3(rows), dim3(ro::kMergeThreads), 0, s, pdl, cand8,
+      e = launch_dependent(ro::merge_kernel, dim3(rows), dim3(ro::kMergeThreads), 0, s, pdl, cand8,
                                stats8, ns, candr, cnt, wstats, np, vocab, k, ids, probs, z, lse);
     return e == cudaSuccess ? cudaGetLastError() : e;
   };

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(128) rope_scatter_kernel(
   constexpr int FULL_UNITS = D / VEC;
   __shared__ float s_cos[D / 2], s_sin[D / 2];
 
+  grid_dep_launch();  // the attention kernel may start its set-up now
   const int r = blockIdx.x;
   const int pos = m.positions[r];
   const int lane = m.row_lane[r];
@@ -119,6 +120,7 @@ cudaError_t launch_rope_scatter(const pie_fwd_plan_t& p, const void* q, const vo
 // ---------------------------------------------------------------------------
 __global__ void fold_kernel(DevMeta m, int L, int32_t* __restrict__ frozen_len,
                             const int32_t* __restrict__ channel, uint32_t* status) {
+  grid_dep_wait();  // the kernels before it, channel included
   const int l = blockIdx.x * blockDim.x + threadIdx.x;
   if (l >= L) return;
   const int n = m.row_indptr[l + 1] - m.row_indptr[l];
@@ -139,8 +141,8 @@ __global__ void fold_kernel(DevMeta m, int L, int32_t* __restrict__ frozen_len,
 
 cudaError_t launch_fold(const pie_fwd_plan_t& p, int32_t* frozen_len, const int32_t* channel,
                         uint32_t* status, cudaStream_t s) {
-  fold_kernel<<<(p.L + 127) / 128, 128, 0, s>>>(p.dev, p.L, frozen_len, channel, status);
-  return cudaGetLastError();
+  return launch_dependent(fold_kernel, dim3((p.L + 127) / 128), dim3(128), 0, s, true, p.dev, p.L,
+                          frozen_len, channel, status);
 }
 
 }  // namespace pie
