@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = S.tmem_base;
+  // every CTA of this grid holds its TMEM now: the expand kernel may start its
+  // set-up (it waits for this grid before it reads A x)
+  grid_dep_launch();
   bool bad = false;
 
   if (warp == 0) {
@@ -403,6 +406,9 @@ __global__ void __launch_bounds__(ad::kExpandThreads) adapter_expand_kernel(
         *reinterpret_cast<uint4*>(base + sw128_offset(128, r, C::KP + R + 8 * c)) = zero;
       }
     }
+    // y, B_a and the IA3 scale above were written before the shrink kernel
+    // started; A x is the shrink kernel's
+    grid_dep_wait();
     const float* tsrc = t_final + int64_t(tile.row0) * R;
     for (int i = tid; i < n * CH; i += kExpandThreads) {
       const int j = i / CH, c = i % CH;
@@ -636,11 +642,13 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
     if (!tc::make_map(&ymap, y, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  adapter_expand_kernel<R><<<dim3(p.num_tiles, d_out / ad::kOBlock), ad::kExpandThreads, smem, s>>>(
-      p.tiles, p.t_final, static_cast<const __nv_bfloat16*>(lora_b),
-      static_cast<const __nv_bfloat16*>(ia3), static_cast<__nv_bfloat16*>(y), d_out,
-      p.max_tile_rows, tmem_cols, status, ymap);
-  return cudaGetLastError();
+  // behind the shrink kernel (rank > 0) it starts while that one drains; with
+  // no shrink kernel before it, in plain stream order
+  return launch_dependent(adapter_expand_kernel<R>, dim3(p.num_tiles, d_out / ad::kOBlock),
+                          dim3(ad::kExpandThreads), smem, s, R > 0, p.tiles, p.t_final,
+                          static_cast<const __nv_bfloat16*>(lora_b),
+                          static_cast<const __nv_bfloat16*>(ia3), static_cast<__nv_bfloat16*>(y),
+                          d_out, p.max_tile_rows, tmem_cols, status, ymap);
 }
 
 }  // namespace
