@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   SM& S = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const TcItem it = m.tc_items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the item is the plan's; everything below may be the kernels' before
+  // (mask lists and counts, the queries, K/V scattered this pass)
+  grid_dep_wait();
   // gather mode (masked passes): positions [kb, ke) of the row block's
   // compacted visible-slot list, this item's share of its tiles; otherwise
   // slots [kb, ke) of the lane
@@ -201,6 +204,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
   fence_after();
   const uint32_t tmem = S.tmem_base;
   bool bad = false;
+  grid_dep_launch();  // the combine kernel may start (it waits for this one)
 
   if (warp < Cfg<NT>::kIssuer0) {
     // ---------------- TMA producers: warp 0 loads K, warp 1 loads V ----------
@@ -558,10 +562,10 @@ static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attend_tc_kernel<NT><<<p.num_tc_items, tc::Cfg<NT>::kThreads, smem, s>>>(
-      p.dev, p.G, p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
-      p.desc.sm_scale * 1.4426950408889634f, mask_words, out, status, qm, km, vm, kgm, vgm);
-  return cudaGetLastError();
+  return launch_dependent(attend_tc_kernel<NT>, dim3(p.num_tc_items), dim3(tc::Cfg<NT>::kThreads),
+                          smem, s, true, p.dev, p.G, p.desc.num_q_heads, p.desc.num_kv_heads,
+                          p.desc.page_size, p.desc.sm_scale * 1.4426950408889634f, mask_words, out,
+                          status, qm, km, vm, kgm, vgm);
 }
 
 cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,

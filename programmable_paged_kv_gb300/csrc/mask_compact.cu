@@ -29,6 +29,7 @@ namespace pie {
 __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
                                                          const uint32_t* __restrict__ mask) {
   __shared__ uint32_t part[8][32];
+  grid_dep_launch();  // the list kernel may start (it waits for this one)
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *m.mask_tiles = 0;
   const MaskBlock B = m.mblocks[blockIdx.y];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,6 +91,8 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P, int B
   __shared__ int warp_tot[32];
   __shared__ int red[32];
   __shared__ int chunk_total;
+  grid_dep_wait();  // the union kernel's words
+  grid_dep_launch();
   const int b = blockIdx.x;
   const MaskBlock B = m.mblocks[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,6 +184,8 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P, int B
 __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
                                                          const uint32_t* __restrict__ mask,
                                                          int Hkv, int P) {
+  grid_dep_wait();  // the list kernel's lists
+  grid_dep_launch();
   const int b = blockIdx.y;
   const MaskBlock B = m.mblocks[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,13 +216,12 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
   mask_union_kernel<<<dim3((nw + 31) / 32, nb), 256, 0, s>>>(p.dev, mask_words);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mask_list_kernel<<<nb, 1024, 0, s>>>(p.dev, p.desc.page_size, tc_kv_tile(p.tc_nt));
-  e = cudaGetLastError();
+  e = launch_dependent(mask_list_kernel, dim3(nb), dim3(1024), 0, s, true, p.dev,
+                       p.desc.page_size, tc_kv_tile(p.tc_nt));
   if (e != cudaSuccess) return e;
   const int row_groups = (p.mblock_max_rows + 15) / 16;
-  mask_cmask_kernel<<<dim3((nw + 7) / 8, nb, row_groups), 256, 0, s>>>(
-      p.dev, mask_words, p.desc.num_kv_heads, p.desc.page_size);
-  return cudaGetLastError();
+  return launch_dependent(mask_cmask_kernel, dim3((nw + 7) / 8, nb, row_groups), dim3(256), 0, s,
+                          true, p.dev, mask_words, p.desc.num_kv_heads, p.desc.page_size);
 }
 
 }  // namespace pie
