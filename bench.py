@@ -385,7 +385,9 @@ def run_ours(args, ws, rank, local, pg):
     # K more steps, instrumented: events around the attend call and (from the
     # library) around the attention kernel.  Events between the kernels stop
     # each from starting while the one before drains, so the step throughput
-    # above is taken without them.
+    # above is taken without them.  A sleep kernel first lets the host queue
+    # all K steps, so the events time the GPU's work, not host gaps.
+    torch.cuda._sleep(int(K * 1e6))
     for i in range(K):
         bytes_attend += acct[t][2]
         step(t, q_d[t % NB], k_d[t % NB], v_d[t % NB], ev[i], kev[i])
@@ -616,7 +618,9 @@ def run_workload(args, local):
     torch.cuda.synchronize()
     # K more passes, instrumented (events between kernels stop each from
     # starting while the one before drains, so the throughput above is taken
-    # without them)
+    # without them); a sleep kernel first lets the host queue all K passes, so
+    # the events time the GPU's work, not host gaps
+    torch.cuda._sleep(int(K * 1e6))
     for i in range(K):
         step(ev[i], kev[i])
     torch.cuda.synchronize()
