@@ -167,8 +167,10 @@ __global__ void __launch_bounds__(128) adapter_shrink_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = S.tmem_base;
-  // every CTA of this grid holds its TMEM now: the expand kernel may start its
-  // set-up (it waits for this grid before it reads A x)
+  // after the kernels before it (x is read below); every CTA of this grid
+  // holds its TMEM now: the expand kernel may start its set-up (it waits for
+  // this grid before it reads A x)
+  grid_dep_wait();
   grid_dep_launch();
   bool bad = false;
 
@@ -605,10 +607,10 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
     }
     uint32_t tmem_cols = 32;
     while (tmem_cols < uint32_t(nmax)) tmem_cols <<= 1;
-    adapter_shrink_kernel<R><<<dim3(p.num_tiles, splits), 128, smem, s>>>(
-        p.tiles, splits, cps, num_chunks, p.num_rows, scale, p.t_part, p.t_final, p.counters,
-        status, nmax, tmem_cols, xmap, amap);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(adapter_shrink_kernel<R>, dim3(p.num_tiles, splits), dim3(128),
+                                     smem, s, true, p.tiles, splits, cps, num_chunks, p.num_rows,
+                                     scale, p.t_part, p.t_final, p.counters, status, nmax,
+                                     tmem_cols, xmap, amap);
     if (e != cudaSuccess) return e;
   }
   // shared memory: 1 KB alignment slack, y rows, the two MMA operands, barriers

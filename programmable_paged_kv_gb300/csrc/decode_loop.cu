@@ -89,6 +89,8 @@ __global__ void loop_init_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int 
 // empty items, whose partial state is (-inf, 0)).
 __global__ void loop_step_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int P,
                                  const int32_t* __restrict__ frozen_len, uint32_t* status) {
+  grid_dep_wait();  // the previous step's fold
+  grid_dep_launch();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < L * Hkv * MC) {
     const int c = i % MC, lg = i / MC, g = lg % Hkv, l = lg / Hkv;
@@ -210,9 +212,8 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
   const size_t kv_step = static_cast<size_t>(L) * Hkv * d * esz;
   const int items = L * Hkv * MC;
   for (int t = 0; t < steps && e == cudaSuccess; ++t) {
-    loop_step_kernel<<<(items + 255) / 256, 256, 0, s>>>(m, L, Hkv, MC, nq, D.page_size, frozen_len,
-                                                          status);
-    e = cudaGetLastError();
+    e = launch_dependent(loop_step_kernel, dim3((items + 255) / 256), dim3(256), 0, s, true, m, L,
+                         Hkv, MC, nq, D.page_size, frozen_len, status);
     if (e == cudaSuccess)
       e = launch_rope_scatter(p, static_cast<const char*>(q) + t * q_step,
                               static_cast<const char*>(k) + t * kv_step,

@@ -29,6 +29,7 @@ namespace pie {
 __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
                                                          const uint32_t* __restrict__ mask) {
   __shared__ uint32_t part[8][32];
+  grid_dep_wait();    // the kernels before it
   grid_dep_launch();  // the list kernel may start (it waits for this one)
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *m.mask_tiles = 0;
   const MaskBlock B = m.mblocks[blockIdx.y];
@@ -213,8 +214,8 @@ cudaError_t launch_mask_compact(const pie_fwd_plan_t& p, const uint32_t* mask_wo
                                 cudaStream_t s) {
   const int nb = p.num_mblocks, nw = p.mblock_max_nw;
   if (nb == 0 || nw == 0) return cudaSuccess;
-  mask_union_kernel<<<dim3((nw + 31) / 32, nb), 256, 0, s>>>(p.dev, mask_words);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(mask_union_kernel, dim3((nw + 31) / 32, nb), dim3(256), 0, s,
+                                   true, p.dev, mask_words);
   if (e != cudaSuccess) return e;
   e = launch_dependent(mask_list_kernel, dim3(nb), dim3(1024), 0, s, true, p.dev,
                        p.desc.page_size, tc_kv_tile(p.tc_nt));

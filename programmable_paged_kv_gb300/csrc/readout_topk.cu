@@ -338,7 +338,10 @@ __global__ void __launch_bounds__(kSampleThreads, 1) sample_kernel(
   __shared__ uint32_t s_thr;
   const int r = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const T* row = logits + int64_t(r) * ld;
-  grid_dep_launch();  // the stream kernel may start loading the logits now
+  // after the kernels before it: then the stream kernel may start loading the
+  // logits (they were written before this grid got past its wait)
+  grid_dep_wait();
+  grid_dep_launch();
   for (int i = t; i < 4096; i += kSampleThreads) hist[i] = 0;
   // sampled token i: chunk (i / 128) * 16, offset i % 128 (key 0: none)
   uint32_t key[kSamplePer];
@@ -974,17 +977,19 @@ extern "C" int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t r
   const bool pdl = ev0 == nullptr;
   auto run = [&](auto* x) -> cudaError_t {
     using T = std::remove_const_t<std::remove_pointer_t<decltype(x)>>;
-    ro::sample_kernel<T><<<rows, ro::kSampleThreads, 0, s>>>(x, ld, vocab, k, thr, cnt);
+    cudaError_t e = launch_dependent(ro::sample_kernel<T>, dim3(rows), dim3(ro::kSampleThreads), 0,
+                                     s, pdl, x, ld, vocab, k, thr, cnt);
     if (ev0) cudaEventRecord(ev0, s);
-    cudaError_t e = launch_dependent(ro::stream_kernel<T>, dim3(units), dim3(ro::kStreamThreads),
-                                         0, s, pdl, x, ld, vocab, np, thr, cnt, candr, wstats);
+    if (e == cudaSuccess)
+      e = launch_dependent(ro::stream_kernel<T>, dim3(units), dim3(ro::kStreamThreads), 0, s, pdl, x,
+                           ld, vocab, np, thr, cnt, candr, wstats);
     if (ev1) cudaEventRecord(ev1, s);
     if (e == cudaSuccess)
       e = launch_dependent(ro::slice_kernel<T>, dim3(g1), dim3(ro::kThreads), smem1, s, pdl, x, ld,
-                               vocab, k, ns, cand8, stats8, cnt, units1);
+                           vocab, k, ns, cand8, stats8, cnt, units1);
     if (e == cudaSuccess)
       e = launch_dependent(ro::merge_kernel, dim3(rows), dim3(ro::kMergeThreads), 0, s, pdl, cand8,
-                               stats8, ns, candr, cnt, wstats, np, vocab, k, ids, probs, z, lse);
+                           stats8, ns, candr, cnt, wstats, np, vocab, k, ids, probs, z, lse);
     return e == cudaSuccess ? cudaGetLastError() : e;
   };
   const cudaError_t e = dtype == PIE_BF16 ? run(static_cast<const __nv_bfloat16*>(logits))

@@ -29,7 +29,10 @@ __global__ void __launch_bounds__(128) rope_scatter_kernel(
   constexpr int FULL_UNITS = D / VEC;
   __shared__ float s_cos[D / 2], s_sin[D / 2];
 
-  grid_dep_launch();  // the attention kernel may start its set-up now
+  // after the kernels before it (in the decode loop, the one that writes this
+  // step's geometry); then the attention kernel may start its set-up
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = blockIdx.x;
   const int pos = m.positions[r];
   const int lane = m.row_lane[r];
@@ -96,11 +99,11 @@ static cudaError_t launch_rs(const pie_fwd_plan_t& p, const void* q, const void*
                              uint32_t* status, cudaStream_t s) {
   // few rows (decode): split each row's units over 4 CTAs
   const dim3 grid(p.N, p.N < 256 ? 4 : 1);
-  rope_scatter_kernel<T, D><<<grid, 128, 0, s>>>(
-      p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
-      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-      static_cast<T*>(q_rot), static_cast<T*>(k_pool), static_cast<T*>(v_pool), frozen, status);
-  return cudaGetLastError();
+  return launch_dependent(rope_scatter_kernel<T, D>, grid, dim3(128), 0, s, true, p.dev,
+                          p.desc.num_q_heads, p.desc.num_kv_heads, p.desc.page_size,
+                          static_cast<const T*>(q), static_cast<const T*>(k),
+                          static_cast<const T*>(v), static_cast<T*>(q_rot), static_cast<T*>(k_pool),
+                          static_cast<T*>(v_pool), frozen, status);
 }
 
 cudaError_t launch_rope_scatter(const pie_fwd_plan_t& p, const void* q, const void* k,
