@@ -435,12 +435,8 @@ __device__ __forceinline__ void stream_part(const T* __restrict__ row, int n, in
       for (int e = 0; e < W; ++e) v[j * W + e] = i0 + e < n ? Elem<T>::to_f(row[i0 + e]) : -INFINITY;
     }
   }
-  // the logits were written before the sample kernel started; the bound and
-  // the zeroed count are the sample kernel's
-  grid_dep_wait();
-  const uint32_t tk = thr[r];
-  const float thr_f = tk <= key_of(-INFINITY) ? -INFINITY : value_of(tk);
   // ---- the warp's (max, sum): each thread's sum rescaled once to the warp max
+  // (the logits were written before the sample kernel got past its wait)
   static_assert(kStreamPer == 16, "the max tree and the four partial sums take 16 tokens");
   const float m = max3(max3(max3(v[0], v[1], v[2]), max3(v[3], v[4], v[5]), max3(v[6], v[7], v[8])),
                        max3(v[9], v[10], v[11]), max3(max3(v[12], v[13], v[14]), v[15], v[15]));
@@ -458,6 +454,10 @@ __device__ __forceinline__ void stream_part(const T* __restrict__ row, int n, in
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (lane == 0) wstats[int64_t(slot) * (kStreamThreads / 32) + warp] = make_float2(mw, sum);
+  // the bound and the zeroed count are the sample kernel's
+  grid_dep_wait();
+  const uint32_t tk = thr[r];
+  const float thr_f = tk <= key_of(-INFINITY) ? -INFINITY : value_of(tk);
   // ---- the tokens at or above the bound
   int mine = 0;
   if (m >= thr_f) {
