@@ -42,6 +42,14 @@
  *     thread's last error.  No call synchronizes the host with the device.
  *   - Device-side findings are ORed into a caller-owned uint32 status word
  *     (PIE_STATUS_*); the caller reads it whenever convenient.
+ *   - Kernels are launched with programmatic stream serialization: each may
+ *     begin while the kernel queued before it on `stream` drains, and waits
+ *     for that kernel (griddepcontrol.wait) before it reads what that kernel
+ *     wrote.  The first kernel of every call waits at its start, and no
+ *     kernel lets the next one begin before its own wait has returned, so
+ *     anything written by work queued earlier on `stream` is complete before
+ *     any kernel of a call reads it: ordinary stream order is all a caller
+ *     needs, and the caller's own kernels keep their usual semantics.
  */
 #ifndef PIE_FWD_H_
 #define PIE_FWD_H_
@@ -208,8 +216,9 @@ const char* pie_fwd_last_error(void);
  *            pie_fwd_readout_topk_workspace_bytes() bytes, caller-owned.
  * Supported: 1 <= k <= 256, k <= vocab <= 262,144 (PIE_EUNSUPPORTED
  * beyond); PIE_EINVAL for a bad dtype, NULL logits/ids/probs, ld < vocab or
- * misaligned rows; PIE_ENOSPACE for a short workspace.  Two kernels on
- * `stream`; no host synchronization. */
+ * misaligned rows; PIE_ENOSPACE for a short workspace.  Four kernels on
+ * `stream` (a sampled bound, one pass over the logits, an exact fallback for
+ * rows the bound does not serve, the merge); no host synchronization. */
 int pie_fwd_readout_topk_workspace_bytes(int32_t dtype, int32_t rows, int32_t vocab, int32_t k,
                                          size_t* bytes);
 int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t rows, int32_t vocab,
