@@ -45,8 +45,10 @@
  *   - Kernels are launched with programmatic stream serialization: each may
  *     begin while the kernel queued before it on `stream` drains, and waits
  *     for that kernel (griddepcontrol.wait) before it reads what that kernel
- *     wrote.  The first kernel of every call waits at its start, and no
- *     kernel lets the next one begin before its own wait has returned, so
+ *     wrote.  The first kernel of every call waits at its start (the
+ *     attention kernels first read only their plan's work items, uploaded by
+ *     pie_fwd_plan before the pass's kernels), and no kernel lets the next
+ *     one begin before its own wait has returned, so
  *     anything written by work queued earlier on `stream` is complete before
  *     any kernel of a call reads it: ordinary stream order is all a caller
  *     needs, and the caller's own kernels keep their usual semantics.
