@@ -129,8 +129,8 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 template <int R>
 __global__ void __launch_bounds__(128) adapter_shrink_kernel(
     const ad::Tile* __restrict__ tiles, int splits, int chunks_per_split, int num_chunks,
-    int num_rows, const float* __restrict__ scale, float* __restrict__ t_part,
-    float* __restrict__ t_final, int* __restrict__ counters, uint32_t* status,
+    int num_rows, const float* scale, float* t_part, float* t_final, int* counters,
+    uint32_t* status,
     int nmax, uint32_t tmem_cols, const __grid_constant__ CUtensorMap xmap,
     const __grid_constant__ CUtensorMap amap) {
   using namespace ad;
@@ -322,9 +322,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int k) {
 // memory, 16 rows (one tcgen05.ld) at a time.
 template <int R>
 __global__ void __launch_bounds__(ad::kExpandThreads) adapter_expand_kernel(
-    const ad::Tile* __restrict__ tiles, const float* __restrict__ t_final,
+    const ad::Tile* __restrict__ tiles, const float* t_final,
     const __nv_bfloat16* __restrict__ lora_b, const __nv_bfloat16* __restrict__ ia3,
-    __nv_bfloat16* __restrict__ y, int d_out, int max_rows, uint32_t tmem_cols,
+    __nv_bfloat16* y, int d_out, int max_rows, uint32_t tmem_cols,
     uint32_t* status, const __grid_constant__ CUtensorMap ymap) {
   using namespace ad;
   using namespace tc;

@@ -134,9 +134,8 @@ __device__ __forceinline__ void load_probs(const float* p, float* f) {
 template <typename T, int D, int NQ>
 __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::MIN_BLOCKS)
     attend_decode_kernel(
-    DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const T* __restrict__ q_rot,
-    const T* __restrict__ k_pool, const T* __restrict__ v_pool,
-    const uint32_t* __restrict__ mask_words, uint32_t* status) {
+    DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const T* q_rot,
+    const T* k_pool, const T* v_pool, const uint32_t* mask_words, uint32_t* status) {
   using C = DecCfg<T, D, NQ>;
   extern __shared__ __align__(128) uint8_t smem[];
   T* ring = reinterpret_cast<T*>(smem);

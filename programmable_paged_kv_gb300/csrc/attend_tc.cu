@@ -133,7 +133,7 @@ __device__ __forceinline__ void store_p(uint32_t taddr, const uint32_t* r) {
 template <int NT>
 __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     DevMeta m, int G, int Hq, int Hkv, int P, float scale_log2,
-    const uint32_t* __restrict__ mask_words, tc::Out out, uint32_t* status,
+    const uint32_t* mask_words, tc::Out out, uint32_t* status,
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kgmap,
     const __grid_constant__ CUtensorMap vgmap) {

@@ -88,7 +88,7 @@ __global__ void loop_init_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int 
 // visible slots [0, kv_len) in kLoopChunk-slot chunks (chunks past kv_len are
 // empty items, whose partial state is (-inf, 0)).
 __global__ void loop_step_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int P,
-                                 const int32_t* __restrict__ frozen_len, uint32_t* status) {
+                                 const int32_t* frozen_len, uint32_t* status) {
   grid_dep_wait();  // the previous step's fold
   grid_dep_launch();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;

@@ -27,7 +27,7 @@ namespace pie {
 // 1. grid (ceil(max_nw / 32), num_blocks), 256 threads: each warp ORs every
 // 8th row of the block over 32 consecutive words.
 __global__ void __launch_bounds__(256) mask_union_kernel(DevMeta m,
-                                                         const uint32_t* __restrict__ mask) {
+                                                         const uint32_t* mask) {
   __shared__ uint32_t part[8][32];
   grid_dep_wait();    // the kernels before it
   grid_dep_launch();  // the list kernel may start (it waits for this one)
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(1024) mask_list_kernel(DevMeta m, int P, int B
 // together).  The first row group's threads also write their listed slots'
 // pool rows.
 __global__ void __launch_bounds__(256) mask_cmask_kernel(DevMeta m,
-                                                         const uint32_t* __restrict__ mask,
+                                                         const uint32_t* mask,
                                                          int Hkv, int P) {
   grid_dep_wait();  // the list kernel's lists
   grid_dep_launch();

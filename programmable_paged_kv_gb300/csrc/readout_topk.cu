@@ -329,8 +329,7 @@ __device__ void gather_list(const uint32_t (&key)[E], Tok tok, uint32_t cb, Sele
 // a row with fewer, or with more than kRowCap, takes the slices.
 template <typename T>
 __global__ void __launch_bounds__(kSampleThreads, 1) sample_kernel(
-    const T* __restrict__ logits, int64_t ld, int vocab, int k, uint32_t* __restrict__ thr,
-    int* __restrict__ cnt) {
+    const T* logits, int64_t ld, int vocab, int k, uint32_t* thr, int* cnt) {
   __shared__ int hist[4096];
   __shared__ int warp_sums[32];
   __shared__ int s_total;
@@ -416,9 +415,8 @@ __global__ void __launch_bounds__(kSampleThreads, 1) sample_kernel(
 // index checks), else the row's ragged last part (padding -inf, never listed).
 template <bool kFull, typename T>
 __device__ __forceinline__ void stream_part(const T* __restrict__ row, int n, int base, int r,
-                                            int slot, const uint32_t* __restrict__ thr,
-                                            int* __restrict__ cnt, uint2* __restrict__ cand,
-                                            float2* __restrict__ wstats, int* s_wt, int* s_base) {
+                                            int slot, const uint32_t* thr, int* cnt,
+                                            uint2* cand, float2* wstats, int* s_wt, int* s_base) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   constexpr int W = 16 / sizeof(T);
   constexpr int J = kStreamPer / W;
@@ -502,9 +500,8 @@ __device__ __forceinline__ void stream_part(const T* __restrict__ row, int n, in
 
 template <typename T>
 __global__ void __launch_bounds__(kStreamThreads) stream_kernel(
-    const T* __restrict__ logits, int64_t ld, int vocab, int nparts,
-    const uint32_t* __restrict__ thr, int* __restrict__ cnt, uint2* __restrict__ cand,
-    float2* __restrict__ wstats) {
+    const T* __restrict__ logits, int64_t ld, int vocab, int nparts, const uint32_t* thr, int* cnt,
+    uint2* cand, float2* wstats) {
   __shared__ int s_wt[kStreamThreads / 32], s_base;
   const int u = blockIdx.x, r = u / nparts, part = u % nparts;
   const int base = part * kPart;
@@ -526,9 +523,8 @@ __device__ __forceinline__ bool row_flagged(const int* cnt, int r, int kk) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) slice_kernel(const T* __restrict__ logits, int64_t ld,
                                                           int vocab, int k, int nslices,
-                                                          uint2* __restrict__ cand,
-                                                          float2* __restrict__ stats,
-                                                          const int* __restrict__ cnt, int units) {
+                                                          uint2* cand, float2* stats,
+                                                          const int* cnt, int units) {
   extern __shared__ uint32_t keys[];  // spos(kSlice) words
   __shared__ SelectSmem sel;
   __shared__ float2 red2[kThreads / 32];
@@ -665,11 +661,9 @@ __device__ __forceinline__ unsigned long long sort_word(uint32_t key, uint32_t t
 constexpr int kMergeList = 2048;
 
 __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(
-    const uint2* __restrict__ cand8, const float2* __restrict__ stats8, int nslices,
-    const uint2* __restrict__ candr, const int* __restrict__ cnt,
-    const float2* __restrict__ wstats, int nparts, int vocab, int k,
-    int32_t* __restrict__ ids, float* __restrict__ probs, float* __restrict__ z,
-    float* __restrict__ lse_out) {
+    const uint2* cand8, const float2* stats8, int nslices, const uint2* candr, const int* cnt,
+    const float2* wstats, int nparts, int vocab, int k, int32_t* ids, float* probs, float* z,
+    float* lse_out) {
   constexpr int E = kMaxSlices * kMaxK / kMergeThreads;  // candidates per thread
   constexpr int NW = kMergeThreads / 32;
   __shared__ SelectSmem sel;  // its histogram is the window histogram too

@@ -21,9 +21,8 @@ namespace pie {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(128) rope_scatter_kernel(
-    DevMeta m, int Hq, int Hkv, int P, const T* __restrict__ q, const T* __restrict__ k,
-    const T* __restrict__ v, T* __restrict__ q_rot, T* __restrict__ k_pool,
-    T* __restrict__ v_pool, const int32_t* __restrict__ frozen_len, uint32_t* status) {
+    DevMeta m, int Hq, int Hkv, int P, const T* q, const T* k, const T* v, T* q_rot,
+    T* k_pool, T* v_pool, const int32_t* frozen_len, uint32_t* status) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int HALF_UNITS = D / 2 / VEC;
   constexpr int FULL_UNITS = D / VEC;
@@ -121,8 +120,8 @@ cudaError_t launch_rope_scatter(const pie_fwd_plan_t& p, const void* q, const vo
 // Step 4 (State geometry: fold).  One thread per lane:
 //   k = 0 | n | fold_count | clamp(channel, 0, n);  frozen_len += k.
 // ---------------------------------------------------------------------------
-__global__ void fold_kernel(DevMeta m, int L, int32_t* __restrict__ frozen_len,
-                            const int32_t* __restrict__ channel, uint32_t* status) {
+__global__ void fold_kernel(DevMeta m, int L, int32_t* frozen_len, const int32_t* channel,
+                            uint32_t* status) {
   grid_dep_wait();  // the kernels before it, channel included
   const int l = blockIdx.x * blockDim.x + threadIdx.x;
   if (l >= L) return;
