@@ -89,3 +89,31 @@ def test_masked_tokens_and_equal_rows():
     _check(seen, 256, ids, probs, z, lse)
     assert ids[1].tolist() == list(range(256))
     assert ids[2, 0] == 12345 and abs(probs[2, 0] - 1.0) < 1e-6
+
+
+def test_unlucky_sample_takes_the_slices():
+    # every raised logit sits in a sampled chunk (chunks 0, 16, 32, ... of 128
+    # tokens), so the sampled bound is high and fewer than k tokens reach it:
+    # the row must take the exact slice path
+    rng = np.random.default_rng(5)
+    V = 128256
+    x = rng.normal(0, 1, size=(2, V)).astype(np.float32)
+    sampled = np.array([c * 2048 + o for c in range(V // 2048) for o in range(128)])
+    for r in range(2):
+        hot = rng.choice(sampled, size=200, replace=False)
+        x[r, hot] = 10.0 + rng.random(200).astype(np.float32)
+    seen, ids, probs, z, lse = _run(x, 256)
+    _check(seen, 256, ids, probs, z, lse)
+
+
+def test_crowded_tie_at_the_kth_value():
+    # 3,000 copies of the k-th largest value: the merge's window bin of that
+    # value overflows its places and the exact select breaks the tie by token
+    rng = np.random.default_rng(6)
+    V = 128256
+    x = rng.normal(0, 1, size=(2, V)).astype(np.float32)
+    for r in range(2):
+        x[r, rng.choice(V, size=3000, replace=False)] = 5.0
+        x[r, rng.choice(V, size=100, replace=False)] = 8.0
+    seen, ids, probs, z, lse = _run(x, 256)
+    _check(seen, 256, ids, probs, z, lse)
