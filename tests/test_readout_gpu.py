@@ -117,3 +117,32 @@ def test_crowded_tie_at_the_kth_value():
         x[r, rng.choice(V, size=100, replace=False)] = 8.0
     seen, ids, probs, z, lse = _run(x, 256)
     _check(seen, 256, ids, probs, z, lse)
+
+
+def test_back_to_back_calls_share_a_workspace():
+    # calls queued one after another on one stream with one workspace and no
+    # host synchronization between them: each call's kernels start while the
+    # previous call's drain, and every result must still be its own
+    import torch
+    from programmable_paged_kv_gb300 import readout_topk, readout_topk_workspace_bytes
+    from programmable_paged_kv_gb300.abi import PIE_F32
+    R, V, k = 4, 40000, 256
+    rng = np.random.default_rng(8)
+    arrays = [W.readout_logits(20 + i, R, V, spikes=4) for i in range(3)]
+    x = rng.normal(0, 2, size=(R, V)).astype(np.float32)
+    x[1, :] = 0.25                          # a row for the slices
+    x[2, rng.random(V) < 0.95] = -np.inf    # mostly masked
+    arrays.insert(1, x)
+    ws = torch.empty(readout_topk_workspace_bytes(PIE_F32, R, V, k), dtype=torch.uint8,
+                     device="cuda")
+    devs = [torch.from_numpy(a).cuda() for a in arrays]
+    outs = [(torch.empty((R, k), dtype=torch.int32, device="cuda"),
+             torch.empty((R, k), dtype=torch.float32, device="cuda"),
+             torch.empty(R, dtype=torch.float32, device="cuda"),
+             torch.empty(R, dtype=torch.float32, device="cuda")) for _ in arrays]
+    torch.cuda.synchronize()
+    for dev, o in zip(devs, outs):  # kernels only between the calls
+        readout_topk(dev, k, *o, workspace=ws)
+    torch.cuda.synchronize()
+    for a, o in zip(arrays, outs):
+        _check(a, k, *(t.cpu().numpy() for t in o))
