@@ -425,14 +425,13 @@ def run_ours(args, ws, rank, local, pg):
             for x in res_d]
     res_h = [torch.empty(ob + lb, dtype=torch.uint8).pin_memory() for _ in range(2)]
     in_ready = [torch.cuda.Event() for _ in range(2)]
-    in_free = [torch.cuda.Event() for _ in range(2)]
-    res_ready = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]  # inputs free, result ready
     out_free = [torch.cuda.Event() for _ in range(2)]
 
     def issue_inputs(t):
         b, j = t % 2, t % NB
         with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(in_free[b])
+            copy_stream.wait_event(step_done[b])
             qkv_d[b].copy_(qkv_h[j], non_blocking=True)
             in_ready[b].record(copy_stream)
 
@@ -442,10 +441,9 @@ def run_ours(args, ws, rank, local, pg):
         stream.wait_event(in_ready[b])
         stream.wait_event(out_free[b])
         step(t, *ins[b], o=outs[b][0], lo=outs[b][1])
-        in_free[b].record(stream)
-        res_ready[b].record(stream)
+        step_done[b].record(stream)
         with torch.cuda.stream(d2h_stream):
-            d2h_stream.wait_event(res_ready[b])
+            d2h_stream.wait_event(step_done[b])
             res_h[b].copy_(res_d[b], non_blocking=True)
             out_free[b].record(d2h_stream)
 

@@ -123,6 +123,7 @@ cudaError_t launch_rope_scatter(const pie_fwd_plan_t& p, const void* q, const vo
 __global__ void fold_kernel(DevMeta m, int L, int32_t* frozen_len, const int32_t* channel,
                             uint32_t* status) {
   grid_dep_wait();  // the kernels before it, channel included
+  grid_dep_launch();
   const int l = blockIdx.x * blockDim.x + threadIdx.x;
   if (l >= L) return;
   const int n = m.row_indptr[l + 1] - m.row_indptr[l];
