@@ -958,6 +958,20 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
         cursor[q] += 1
         left[q] -= 1
         call_set[cid], call_rows[cid] = q, 1
+    def submit_group(qs):
+        # the next calls of several agents in one native call
+        reads, writes = [], []
+        for q in qs:
+            c = cursor[q]
+            reads.append(pages64[q][:c // P + 1])
+            writes.append(pages64[q][c // P:c // P + 1])
+            cursor[q] += 1
+            left[q] -= 1
+        ids = b.submit_many([qids[q] for q in qs], [0] * len(qs), [1] * len(qs), qs,
+                            [()] * len(qs), reads, writes)
+        for cid, q in zip(ids, qs):
+            call_set[cid], call_rows[cid] = q, 1
+
     for q in range(Q):
         submit(q)
     ev = [] if kernel_ms is not None else None
@@ -1001,9 +1015,9 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
         batches += 1
         h0 = time.perf_counter()
         b.complete(ids)
-        for c in ids:
-            if left[call_set[c]] > 0:
-                submit(call_set[c])
+        again = [call_set[c] for c in ids if left[call_set[c]] > 0]
+        if again:
+            submit_group(again)
         marshal += time.perf_counter() - h0
     torch.cuda.synchronize()
     secs = time.perf_counter() - t0

@@ -66,6 +66,23 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
                        const int64_t* reads, int32_t num_reads, const int64_t* writes,
                        int32_t num_writes, int64_t* call_id);
 
+/* Enqueue n calls at once, as n calls of pie_batcher_submit in order: call i
+ * (0 <= i < n) takes queues[i], handlers[i], rows[i], keys[i] and the lists
+ * deps[dep_indptr[i] .. dep_indptr[i+1]), reads[read_indptr[i] ..
+ * read_indptr[i+1]), writes[write_indptr[i] .. write_indptr[i+1]) (offset
+ * arrays of n + 1 entries from 0, never decreasing; a flat array may be NULL
+ * when its offsets end at 0).  Call i gets id *first_id + i, so a dependency
+ * may name a call earlier in the same submission.  Every call is checked
+ * before any is enqueued: on error nothing changes.  Errors as
+ * pie_batcher_submit, and PIE_EINVAL for NULL per-call arrays or bad offset
+ * arrays. */
+int pie_batcher_submit_many(pie_batcher_t* b, int32_t n, const int32_t* queues,
+                            const int32_t* handlers, const int64_t* rows, const int64_t* keys,
+                            const int64_t* dep_indptr, const int64_t* deps,
+                            const int64_t* read_indptr, const int64_t* reads,
+                            const int64_t* write_indptr, const int64_t* writes,
+                            int64_t* first_id);
+
 /* Form and dispatch one batch (Algorithm 2's GPU-idle step): its call ids in order go to
  * calls[0..n), the lane of each call to lanes[0..n) (0, 1, ...), its handler
  * type to *handler, n to *num_calls (0 and handler -1 when no call is

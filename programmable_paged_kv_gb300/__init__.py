@@ -324,6 +324,29 @@ class Batcher:
             "pie_batcher_submit")
         return cid.value
 
+    def submit_many(self, queues, handlers, rows, keys, deps, reads, writes) -> range:
+        """Enqueue len(queues) calls in one native call (pie_batcher_submit_many):
+        per-call queue, handler, rows and key, and per-call lists of dependencies,
+        read and write resource ids; returns the range of their ids."""
+        n = len(queues)
+        i32 = lambda x: np.ascontiguousarray(x, dtype=np.int32).reshape(-1)
+        i64 = lambda x: np.ascontiguousarray(x, dtype=np.int64).reshape(-1)
+
+        def flat(lists):
+            sizes = [len(x) for x in lists]
+            indptr = np.zeros(n + 1, dtype=np.int64)
+            np.cumsum(sizes, out=indptr[1:])
+            vals = i64(np.concatenate([i64(x) for x in lists])) if indptr[-1] else i64([])
+            return indptr, vals
+        q, h, r, k = i32(queues), i32(handlers), i64(rows), i64(keys)
+        (di, dv), (ri, rv), (wi, wv) = flat(deps), flat(reads), flat(writes)
+        first = C.c_int64()
+        abi.check(self.lib.pie_batcher_submit_many(
+            self.handle, n, q.ctypes.data, h.ctypes.data, r.ctypes.data, k.ctypes.data,
+            di.ctypes.data, dv.ctypes.data, ri.ctypes.data, rv.ctypes.data, wi.ctypes.data,
+            wv.ctypes.data, C.byref(first)), "pie_batcher_submit_many")
+        return range(first.value, first.value + n)
+
     def dispatch(self):
         """(handler, call ids, lanes) of the next batch, or None."""
         n, h = C.c_int32(), C.c_int32()

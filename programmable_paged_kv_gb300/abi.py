@@ -96,6 +96,8 @@ SIGNATURES = {
     "pie_batcher_submit": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int64, C.c_int64, _P,
                                      C.c_int32, _P, C.c_int32, _P, C.c_int32,
                                      C.POINTER(C.c_int64)]),
+    "pie_batcher_submit_many": (C.c_int, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          C.POINTER(C.c_int64)]),
     "pie_batcher_dispatch": (C.c_int, [_P, _P, _P, C.c_int32, C.POINTER(C.c_int32),
                                        C.POINTER(C.c_int32)]),
     "pie_batcher_complete": (C.c_int, [_P, _P, C.c_int32]),

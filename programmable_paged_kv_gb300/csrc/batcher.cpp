@@ -134,11 +134,15 @@ int pie_batcher_add_queue(pie_batcher_t* b, int32_t priority, int32_t* queue_id)
   return PIE_OK;
 }
 
-int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t rows,
-                       int64_t key, const int64_t* deps, int32_t num_deps,
-                       const int64_t* reads, int32_t num_reads, const int64_t* writes,
-                       int32_t num_writes, int64_t* call_id) {
-  if (!b || !call_id) return set_last_error(PIE_EINVAL, "NULL argument");
+}  // extern "C"
+
+namespace {
+
+// Checks one call that would get id `id`; on success *top is its largest
+// resource id (-1 without any).
+int check_call(const pie_batcher_t* b, int64_t id, int32_t queue, int32_t handler, int64_t rows,
+               const int64_t* deps, int64_t num_deps, const int64_t* reads, int64_t num_reads,
+               const int64_t* writes, int64_t num_writes, int64_t* top) {
   if (queue < 0 || size_t(queue) >= b->queues.size()) return set_last_error(PIE_EINVAL, "unknown queue");
   if (handler < 0 || size_t(handler) >= b->ordered.size())
     return set_last_error(PIE_EINVAL, "unknown handler type");
@@ -146,23 +150,27 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
   if (num_deps < 0 || num_reads < 0 || num_writes < 0) return set_last_error(PIE_EINVAL, "negative count");
   if ((num_deps && !deps) || (num_reads && !reads) || (num_writes && !writes))
     return set_last_error(PIE_EINVAL, "NULL array with a positive count");
-  const int64_t id = int64_t(b->calls.size());
-  for (int i = 0; i < num_deps; ++i)
+  for (int64_t i = 0; i < num_deps; ++i)
     if (deps[i] < 0 || deps[i] >= id)
       return set_last_error(PIE_EINVAL, "a dependency is not an earlier call");
-  int64_t top = -1;
-  for (int i = 0; i < num_reads; ++i) top = std::max(top, reads[i]);
-  for (int i = 0; i < num_writes; ++i) top = std::max(top, writes[i]);
-  for (int i = 0; i < num_reads; ++i)
-    if (reads[i] < 0) top = kMaxResource;
-  for (int i = 0; i < num_writes; ++i)
-    if (writes[i] < 0) top = kMaxResource;
-  if (top >= kMaxResource) return set_last_error(PIE_ERANGE, "resource id outside [0, 2^26)");
+  int64_t t = -1;
+  for (int64_t i = 0; i < num_reads; ++i) t = reads[i] < 0 ? kMaxResource : std::max(t, reads[i]);
+  for (int64_t i = 0; i < num_writes; ++i) t = writes[i] < 0 ? kMaxResource : std::max(t, writes[i]);
+  if (t >= kMaxResource) return set_last_error(PIE_ERANGE, "resource id outside [0, 2^26)");
+  *top = t;
+  return PIE_OK;
+}
+
+// Records a checked call under the next id.
+void add_call(pie_batcher_t* b, int64_t top, int32_t queue, int32_t handler, int64_t rows,
+              int64_t key, const int64_t* deps, int64_t num_deps, const int64_t* reads,
+              int64_t num_reads, const int64_t* writes, int64_t num_writes) {
   if (top >= int64_t(b->rstamp.size())) {
     const size_t n = std::max<size_t>(size_t(top) + 1, 2 * b->rstamp.size());
     b->rstamp.resize(n, 0u);
     b->wstamp.resize(n, 0u);
   }
+  const int64_t id = int64_t(b->calls.size());
   CallRec c;
   c.queue = queue;
   c.handler = handler;
@@ -184,7 +192,62 @@ int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t
     b->active.push_back(queue);
   }
   ++b->queued;
-  *call_id = id;
+}
+
+// One flat list's entries of call i: [indptr[i], indptr[i+1]).
+bool check_indptr(const int64_t* indptr, int32_t n, const int64_t* flat) {
+  if (!indptr) return false;
+  if (indptr[0] != 0) return false;
+  for (int32_t i = 0; i < n; ++i)
+    if (indptr[i + 1] < indptr[i]) return false;
+  return indptr[n] == 0 || flat != nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pie_batcher_submit(pie_batcher_t* b, int32_t queue, int32_t handler, int64_t rows,
+                       int64_t key, const int64_t* deps, int32_t num_deps,
+                       const int64_t* reads, int32_t num_reads, const int64_t* writes,
+                       int32_t num_writes, int64_t* call_id) {
+  if (!b || !call_id) return set_last_error(PIE_EINVAL, "NULL argument");
+  int64_t top = -1;
+  const int rc = check_call(b, int64_t(b->calls.size()), queue, handler, rows, deps, num_deps, reads,
+                            num_reads, writes, num_writes, &top);
+  if (rc != PIE_OK) return rc;
+  *call_id = int64_t(b->calls.size());
+  add_call(b, top, queue, handler, rows, key, deps, num_deps, reads, num_reads, writes, num_writes);
+  return PIE_OK;
+}
+
+int pie_batcher_submit_many(pie_batcher_t* b, int32_t n, const int32_t* queues,
+                            const int32_t* handlers, const int64_t* rows, const int64_t* keys,
+                            const int64_t* dep_indptr, const int64_t* deps,
+                            const int64_t* read_indptr, const int64_t* reads,
+                            const int64_t* write_indptr, const int64_t* writes,
+                            int64_t* first_id) {
+  if (!b || !first_id || n < 0) return set_last_error(PIE_EINVAL, "NULL argument or n < 0");
+  const int64_t id0 = int64_t(b->calls.size());
+  *first_id = id0;
+  if (n == 0) return PIE_OK;
+  if (!queues || !handlers || !rows || !keys) return set_last_error(PIE_EINVAL, "NULL per-call array");
+  if (!check_indptr(dep_indptr, n, deps) || !check_indptr(read_indptr, n, reads) ||
+      !check_indptr(write_indptr, n, writes))
+    return set_last_error(PIE_EINVAL, "a list offset array is NULL, not from 0 or decreasing");
+  std::vector<int64_t> tops(size_t(n), -1);
+  for (int32_t i = 0; i < n; ++i) {  // every call checked before any is recorded
+    const int rc = check_call(b, id0 + i, queues[i], handlers[i], rows[i], deps + dep_indptr[i],
+                              dep_indptr[i + 1] - dep_indptr[i], reads + read_indptr[i],
+                              read_indptr[i + 1] - read_indptr[i], writes + write_indptr[i],
+                              write_indptr[i + 1] - write_indptr[i], &tops[size_t(i)]);
+    if (rc != PIE_OK) return rc;
+  }
+  for (int32_t i = 0; i < n; ++i)
+    add_call(b, tops[size_t(i)], queues[i], handlers[i], rows[i], keys[i], deps + dep_indptr[i],
+             dep_indptr[i + 1] - dep_indptr[i], reads + read_indptr[i],
+             read_indptr[i + 1] - read_indptr[i], writes + write_indptr[i],
+             write_indptr[i + 1] - write_indptr[i]);
   return PIE_OK;
 }
 

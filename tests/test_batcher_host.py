@@ -105,3 +105,67 @@ def test_batcher_refusals():
     assert lib.pie_batcher_complete(b.handle, (C.c_int64 * 1)(0), 1) == abi.PIE_EINVAL  # twice
     assert b.dispatch() is None
     b.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_submit_many_matches_one_by_one(seed):
+    # the same operations, calls submitted one by one into one batcher and in
+    # random groups into the other: the same ids and the same batches
+    rng = random.Random(seed)
+    nq = rng.randrange(1, 7)
+    ordered = [rng.random() < 0.6 for _ in range(2)]
+    a, b = Batcher(ordered, 6, 24), Batcher(ordered, 6, 24)
+    prios = [rng.randrange(3) for _ in range(nq)]
+    for p in prios:
+        a.add_queue(p)
+        b.add_queue(p)
+    submitted, flying = 0, []
+    for _ in range(300):
+        act = rng.random()
+        if act < 0.45 and submitted < 200:
+            group = []
+            for _ in range(rng.randrange(1, 6)):
+                cid = submitted + len(group)
+                deps = sorted({rng.randrange(cid) for _ in range(rng.randrange(3))}) if cid else []
+                group.append((rng.randrange(nq), rng.randrange(2), rng.randrange(1, 6),
+                              rng.randrange(-1, 3), deps,
+                              [rng.randrange(20) for _ in range(rng.randrange(4))],
+                              [rng.randrange(20) for _ in range(rng.randrange(2))]))
+            for g in group:
+                assert a.submit(g[0], g[1], g[2], g[3], g[4], g[5], g[6]) == submitted
+                submitted += 1
+            ids = b.submit_many(*[[g[f] for g in group] for f in range(7)])
+            assert list(ids) == list(range(submitted - len(group), submitted))
+        elif act < 0.65 and flying:
+            done = flying.pop(rng.randrange(len(flying)))
+            a.complete(done)
+            b.complete(done)
+        else:
+            x, y = a.dispatch(), b.dispatch()
+            assert x == y, (seed, x, y)
+            if x is not None:
+                flying.append(x[1])
+        assert a.counts() == b.counts()
+    a.close()
+    b.close()
+
+
+def test_submit_many_refusals_change_nothing():
+    b = Batcher([True], 4, 16)
+    q = b.add_queue(0)
+    assert list(b.submit_many([q], [0], [1], [-1], [[]], [[1]], [[2]])) == [0]
+    # the third call names a dependency that is not earlier: nothing is enqueued
+    with pytest.raises(Exception):
+        b.submit_many([q, q, q], [0, 0, 0], [1, 1, 1], [-1, -1, -1], [[0], [1], [5]],
+                      [[], [], []], [[], [], []])
+    assert b.counts() == (1, 0)
+    # a resource id out of range in the last call: nothing is enqueued
+    with pytest.raises(Exception):
+        b.submit_many([q, q], [0, 0], [1, 1], [-1, -1], [[], []], [[3], [1 << 26]], [[], []])
+    assert b.counts() == (1, 0)
+    # the ids continue where they were
+    assert list(b.submit_many([q, q], [0, 0], [1, 1], [-1, -1], [[], [1]], [[], []],
+                              [[], []])) == [1, 2]
+    assert list(b.submit_many([], [], [], [], [], [], [])) == []
+    assert b.counts() == (3, 0)
+    b.close()
