@@ -950,6 +950,11 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
     kv_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hkv, D), dtype=np.float32)).view(np.int16)).pin_memory()
 
     pages64 = [np.asarray(pg, np.int64) for pg in trace.queue_pages]
+    # pinned staging for each batch's gathered inputs, so their copies to the
+    # device are asynchronous
+    q_st = torch.empty_like(q_in).pin_memory()
+    kv_st = torch.empty_like(kv_in).pin_memory()
+    fr_st = torch.empty(Q, dtype=torch.int32).pin_memory()
 
     def submit(q):
         pages = pages64[q]
@@ -991,10 +996,14 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
                                                 frozen)
         N = int(p.row_indptr[-1])
         sel = torch.tensor(lane_set, dtype=torch.long)
-        qd = q_in.index_select(0, sel).cuda(non_blocking=True).view(tdt)
-        kd = kv_in.index_select(0, sel).cuda(non_blocking=True).view(tdt)
+        L = len(lane_set)
+        torch.index_select(q_in, 0, sel, out=q_st[:L])
+        torch.index_select(kv_in, 0, sel, out=kv_st[:L])
+        qd = q_st[:L].cuda(non_blocking=True).view(tdt)
+        kd = kv_st[:L].cuda(non_blocking=True).view(tdt)
         plan = ForwardPlan(desc, make_meta(p, trace.pool.num_pool_pages))
-        fr = torch.tensor([frozen[w] for w in lane_set], dtype=torch.int32).cuda(non_blocking=True)
+        fr_st[:L] = torch.tensor([frozen[w] for w in lane_set], dtype=torch.int32)
+        fr = fr_st[:L].cuda(non_blocking=True)
         q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
         plan.append_kv(qd, kd, kd, q_rot, pools.k, pools.v, fr)
         out = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
