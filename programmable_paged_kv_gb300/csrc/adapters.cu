@@ -597,13 +597,11 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
     }
     const int nmax = (p.max_tile_rows + 15) & ~15;
     const size_t smem = 1024 + ad::shrink_smem_bytes(R, nmax);  // + alignment slack
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(adapter_shrink_kernel<R>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(1024 + ad::shrink_smem_bytes(R, ad::kTileRows)));
+    static std::atomic<uint64_t> configured{0};
+    {
+      cudaError_t e = set_smem_limit(adapter_shrink_kernel<R>,
+                                     int(1024 + ad::shrink_smem_bytes(R, ad::kTileRows)), configured);
       if (e != cudaSuccess) return e;
-      configured = true;
     }
     uint32_t tmem_cols = 32;
     while (tmem_cols < uint32_t(nmax)) tmem_cols <<= 1;
@@ -622,13 +620,11 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
     return 1024 + ys + ops + 256;
   };
   const size_t smem = expand_smem(p.max_tile_rows);
-  static bool configured_e = false;
-  if (!configured_e) {
-    cudaError_t e = cudaFuncSetAttribute(adapter_expand_kernel<R>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(expand_smem(ad::kTileRows)));
+  static std::atomic<uint64_t> configured_e{0};
+  {
+    cudaError_t e = set_smem_limit(adapter_expand_kernel<R>, int(expand_smem(ad::kTileRows)),
+                                   configured_e);
     if (e != cudaSuccess) return e;
-    configured_e = true;
   }
   // TMEM: two M tiles of up to nmax columns, a power of two of at least 32
   uint32_t tmem_cols = 0;

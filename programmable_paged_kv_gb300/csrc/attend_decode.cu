@@ -144,12 +144,7 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
   uint64_t* full = reinterpret_cast<uint64_t*>(abuf + C::ABUF_FLOATS);
   uint64_t* empty = full + C::STAGES;
 
-  const DecItem it = m.dec_items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kb = it.kv_begin, ke = it.kv_end;
-  const int nstages = ke > kb ? (ke - kb + kStageSlots - 1) / kStageSlots : 0;
-  const int nqv = it.nrows * G;  // valid query vectors
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -158,10 +153,17 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
     fence_barrier_init();
   }
   __syncthreads();
-  // set-up above overlaps the kernel before (RoPE and scatter of this pass's
-  // K/V and queries); everything below reads its results
+  // The barrier set-up above overlaps the kernel before; everything below,
+  // the work item included, is read after the wait: the items may come from
+  // a kernel queued just before this one (the decode loop's geometry step,
+  // the no-allocation entry point's item kernel), whose writes are only
+  // guaranteed visible once griddepcontrol.wait has returned.
   grid_dep_wait();
   grid_dep_launch();
+  const DecItem it = m.dec_items[blockIdx.x];
+  const int kb = it.kv_begin, ke = it.kv_end;
+  const int nstages = ke > kb ? (ke - kb + kStageSlots - 1) / kStageSlots : 0;
+  const int nqv = it.nrows * G;  // valid query vectors
 
   if (warp == C::WARPS) {
     // ---------------- producer warp: TMA bulk copies of K/V pages ----------
@@ -367,13 +369,9 @@ static cudaError_t launch_dec(const pie_fwd_plan_t& p, const void* q_rot, const 
                               const void* v_pool, const uint32_t* mask_words, uint32_t* status,
                               cudaStream_t s) {
   using C = DecCfg<T, D, NQ>;
-  static bool configured = false;  // per instantiation; attribute is per device function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_decode_kernel<T, D, NQ>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per instantiation and device
+  cudaError_t e = set_smem_limit(attend_decode_kernel<T, D, NQ>, int(C::SMEM), configured);
+  if (e != cudaSuccess) return e;
   return launch_dependent(attend_decode_kernel<T, D, NQ>, dim3(p.num_dec_items), dim3(C::THREADS),
                           C::SMEM, s, true, p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
                           p.desc.page_size, p.desc.sm_scale * kLog2e, static_cast<const T*>(q_rot),

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::kThreads, 1) attend_tc_kernel(
     const int tiles = (U + BN - 1) / BN;
     // the chunks this unit uses now that its list length is known; the
     // provisioned items past them have nothing to do and write nothing
-    const int nch = masked_chunks(tiles, it.nchunks, *m.mask_tiles, Hkv);
+    const int nch = masked_chunks(tiles, it.nchunks, *m.mask_tiles, Hkv, m.num_sms);
     if (it.chunk >= nch) return;
     kb = (it.chunk * tiles / nch) * BN;
     ke = min(U, ((it.chunk + 1) * tiles / nch) * BN);
@@ -555,13 +555,9 @@ static cudaError_t launch_nt(const pie_fwd_plan_t& p, const uint32_t* mask_words
                              const CUtensorMap& vm, const CUtensorMap& kgm,
                              const CUtensorMap& vgm, cudaStream_t s) {
   const size_t smem = sizeof(tc::Smem<NT>) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = set_smem_limit(attend_tc_kernel<NT>, int(smem), configured);
+  if (e != cudaSuccess) return e;
   return launch_dependent(attend_tc_kernel<NT>, dim3(p.num_tc_items), dim3(tc::Cfg<NT>::kThreads),
                           smem, s, true, p.dev, p.G, p.desc.num_q_heads, p.desc.num_kv_heads,
                           p.desc.page_size, p.desc.sm_scale * 1.4426950408889634f, mask_words, out,

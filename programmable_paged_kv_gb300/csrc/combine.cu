@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
   // a masked tensor-core block uses as many chunks as its list length gives
   const int nch = ce.mblock < 0 ? ce.nchunks
                                 : masked_chunks((m.list_len[ce.mblock] + tc_bn - 1) / tc_bn,
-                                                ce.nchunks, *m.mask_tiles, Hkv);
+                                                ce.nchunks, *m.mask_tiles, Hkv, m.num_sms);
   float o[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) o[e] = 0.f;

@@ -64,21 +64,26 @@ constexpr int kStageSlots = 64;   // slots per pipeline stage of the decode kern
 constexpr int kWarpSlots = 16;    // slots per compute warp per stage
 constexpr int kTcTileSlots = 128; // slots per KV tile of the tensor-core kernel
 constexpr int kTcTileQueries = 128;
-constexpr int kTcTargetSms = 152;  // SMs of the part the item counts are sized for
+// SMs the tensor-core work is sized for when no device is visible (host-only
+// planning, e.g. pie_fwd_workspace_bytes on a machine without a GPU); with a
+// device, its multiprocessor count is used (device_sm_count).
+constexpr int kTcDefaultSms = 152;
+int device_sm_count();
 
 // KV slots per tile of the tensor-core kernel with nt query tiles per item
 // (two score buffers per query tile and every tile's O share 512 TMEM columns)
 constexpr int tc_kv_tile(int nt) { return nt == 1 ? 128 : 64; }
 
 // Chunks a masked tensor-core unit (row block x kv head) splits its list
-// into: its share of one wave of kTcTargetSms items, in proportion to its
+// into: its share of one wave of `sms` items (one per SM), in proportion to its
 // KV tiles among all masked units' (total_tiles counts each row block's tiles
 // once; every block has Hkv units), at least 1 and at most the provisioned
 // items and its tiles.  The kernel and the combine step both use it.
-__host__ __device__ inline int masked_chunks(int tiles, int provisioned, int total_tiles, int Hkv) {
+__host__ __device__ inline int masked_chunks(int tiles, int provisioned, int total_tiles, int Hkv,
+                                             int sms) {
   if (tiles <= 1) return 1;
   const long long want =
-      static_cast<long long>(tiles) * kTcTargetSms / (static_cast<long long>(total_tiles > 0 ? total_tiles : 1) * Hkv);
+      static_cast<long long>(tiles) * sms / (static_cast<long long>(total_tiles > 0 ? total_tiles : 1) * Hkv);
   long long n = want < 1 ? 1 : want;
   if (n > provisioned) n = provisioned;
   if (n > tiles) n = tiles;
@@ -116,6 +121,7 @@ struct DevMeta {
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
   int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
   int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
+  int32_t num_sms;                  // SMs the masked tensor-core chunks are sized for
 };
 
 // Pinned host staging block: metadata uploads copy from pinned memory so that

@@ -16,6 +16,7 @@
 // the readout rows.
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -87,7 +88,7 @@ void pinned_release(PinnedBlock* b) {
 // host plan: validated metadata + work lists, before layout
 // ---------------------------------------------------------------------------
 struct HostPlan {
-  int L = 0, N = 0, R = 0, G = 1, nq = 4, tc_nt = 1;
+  int L = 0, N = 0, R = 0, G = 1, nq = 4, tc_nt = 1, sms = kTcDefaultSms;
   std::vector<int32_t> ro_indptr, ro_idx;
   std::vector<MaskBlock> mblocks;
   int64_t list_total = 0, cmask_total = 0;
@@ -131,8 +132,26 @@ static int choose_chunk(int64_t total_slots_x_heads) {
 
 // Lanes with at least this many query vectors per kv head use the
 // tensor-core kernel (bf16 only).
-static bool g_tc_enabled = true;
 constexpr int kTcMinQueries = 16;
+
+// Multiprocessors of the current device, looked up once per device; the
+// default when no device is visible (planning on a host without a GPU).
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return kTcDefaultSms;
+  }
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    (void)cudaGetLastError();
+    return kTcDefaultSms;
+  }
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
 
 static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, HostPlan& H) {
   if (!desc || !meta) return fail(PIE_EINVAL, "desc and meta are required");
@@ -179,6 +198,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   H.L = L;
   H.N = N;
   H.G = G;
+  H.sms = device_sm_count();
   H.total_pages = total_pages;
   H.row_lane.assign(N, 0);
   H.any_channel = false;
@@ -273,7 +293,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
     return std::min(kv, mx + 1);
   };
   // (the tensor-core kernel addresses pool rows with 32-bit TMA coordinates)
-  const bool tc_ok = g_tc_enabled && D.dtype == PIE_BF16 && D.head_dim == 128 &&
+  const bool tc_ok = D.dtype == PIE_BF16 && D.head_dim == 128 &&
                      kTcTileQueries % G == 0 &&
                      static_cast<int64_t>(M.num_pool_pages) * Hkv * D.page_size <= INT32_MAX;
   auto lane_tc = [&](int l) {
@@ -303,7 +323,7 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
       tc_units += Hkv;
     }
   }
-  const int64_t tc_target = 4 * kTcTargetSms;
+  const int64_t tc_target = 4 * static_cast<int64_t>(H.sms);
   const int64_t tc_ch = tc_units >= tc_target ? INT32_MAX
                         : std::max<int64_t>(512, (tc_total + tc_target - 1) / tc_target);
   H.comb.clear();
@@ -596,6 +616,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
   dm.list_mode = reinterpret_cast<int32_t*>(w + Y.list_mode);
   dm.mask_tiles = reinterpret_cast<int32_t*>(w + Y.mask_tiles);
+  dm.num_sms = H.sms;
   p->staging = blk;
   *out = p;
   return PIE_OK;

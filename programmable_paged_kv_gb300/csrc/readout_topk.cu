@@ -950,12 +950,12 @@ extern "C" int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t r
   float2* wstats = reinterpret_cast<float2*>(w + Y.wstats);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t smem1 = sizeof(uint32_t) * (ro::kSlice + ro::kSlice / 32);
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(ro::slice_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem1));
-    cudaFuncSetAttribute(ro::slice_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         int(smem1));
-    configured = true;
+  static std::atomic<uint64_t> configured_f{0}, configured_b{0};
+  {
+    cudaError_t e = set_smem_limit(ro::slice_kernel<float>, int(smem1), configured_f);
+    if (e == cudaSuccess) e = set_smem_limit(ro::slice_kernel<__nv_bfloat16>, int(smem1), configured_b);
+    if (e != cudaSuccess)
+      return set_last_error(PIE_ECUDA, std::string("readout set-up: ") + cudaGetErrorString(e));
   }
   // the rows' bounds from a sample; one pass over the logits lists the
   // candidates; rows whose lists missed or overflowed go through the slices;
