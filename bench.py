@@ -63,6 +63,8 @@ def parse():
                              "adapters_decode", "adapters_prefill", "batcher"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="leave out the other configurations' figures from the default line")
     ap.add_argument("--pool-pages", type=int, default=65536,
                     help="pages per K/V pool (smaller pools serve profiler captures)")
     return ap.parse_args()
@@ -150,6 +152,14 @@ def peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def peaks_tensor() -> float:
+    """Measured dense bf16 TFLOP/s (burst: the kernels are timed alone)."""
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 class ClockSampler:
@@ -249,36 +259,45 @@ def oracle_rate(seed: int, seconds: float, threads: int = 0):
     return tok * passes / total, cores, passes, total
 
 
+def headline_config(pool_pages: int) -> dict:
+    """The decode-batch configuration both arms report."""
+    return {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1, "q_heads": 32,
+            "kv_heads": 8, "head_dim": 128, "page_size": 16, "pool_pages": pool_pages,
+            "kv_len": "C+t+1 at step t, C~U[512,4096]",
+            "l2": "inputs larger than L2 (~600 MB of KV read per step)",
+            "step": "plan+append_kv+attend+fold"}
+
+
 def run_reference(args, ws, rank):
+    """The oracle as the reference arm: step t is decode step t of the
+    decode batch (each lane's row at slot C+t, C+t+1 slots read, folded),
+    the steps applied in order to one pool, on every host core."""
     if rank != 0:
         return
     import oracle as O
     O.build()
-    sc = W.decode_batch(args.seed, lanes=64)
-    p = sc.passes[0]
-    cp = sc.compact_page_ids(p.page_ids)
+    sc = W.decode_loop(args.seed, lanes=64, steps=args.warmup + args.steps)
+    k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
     cores = os.cpu_count() or 1
-    tok = attended_tokens(p)
-    for _ in range(args.warmup):
-        k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
-        O.run_pass(sc.desc, p, k, v, fr, page_ids=cp, num_threads=cores)
-    times = []
-    for _ in range(args.steps):
-        k, v, fr = sc.k_init.copy(), sc.v_init.copy(), sc.frozen_len0.copy()
+    cp = sc.compact_page_ids(sc.passes[0].page_ids)
+    times, tok = [], 0
+    for t, p in enumerate(sc.passes):
         ts = time.perf_counter()
         r = O.run_pass(sc.desc, p, k, v, fr, page_ids=cp, num_threads=cores)
-        times.append(time.perf_counter() - ts)
+        dt = time.perf_counter() - ts
         assert r["err"] == O.OK
+        if t >= args.warmup:
+            times.append(dt)
+            tok += attended_tokens(p)
     el = sum(times)
-    val = tok * args.steps / el
-    sample = "one full decode-batch pass (64 lanes x 1 row) per step, all host cores"
+    val = tok / el
+    sample = ("decode steps of the decode batch (64 lanes x 1 row, step t at slot C+t), one "
+              "full pass per step, all host cores")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1,
-                                        "q_heads": 32, "kv_heads": 8, "head_dim": 128,
-                                        "page_size": 16, "kv_len": "C+1, C~U[512,4096]"},
+        "data": "synthetic", "config": headline_config(args.pool_pages),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -475,6 +494,13 @@ def run_ours(args, ws, rank, local, pg):
 
     if rank != 0:
         return
+    side = None
+    if ws == 1 and not args.no_side_workloads:
+        # the headline's 4 GiB pools are not needed any more
+        k_pool = v_pool = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        side = side_workloads(args.seed, local)
     hbm, peak_kind = peaks()
     att_s = sum(attend_ms) / len(attend_ms) / 1e3
     ker_s = sum(kernel_ms) / len(kernel_ms) / 1e3
@@ -483,11 +509,7 @@ def run_ours(args, ws, rank, local, pg):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": Wm,
         "ms_per_step": el_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "lanes": 64, "rows_per_lane": 1, "q_heads": Hq,
-                   "kv_heads": Hkv, "head_dim": D, "page_size": desc.page_size,
-                   "pool_pages": NP, "kv_len": "C+t+1, C~U[512,4096]",
-                   "l2": "inputs larger than L2 (~600 MB of KV read per step)",
-                   "step": "plan+append_kv+attend+fold"},
+        "config": headline_config(NP),
         "gpu_launches": 4 * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": profiled_traffic(),
@@ -504,6 +526,18 @@ def run_ours(args, ws, rank, local, pg):
     }
     if clk:
         line["clocks"] = clk
+    if side:
+        g = side["guidance_prefill"]
+        tf = peaks_tensor()
+        line["roofline_prefill"] = {
+            "bound": "tensor", "achieved": g["kernel_tflops"], "peak": tf, "unit": "TFLOP/s",
+            "frac": g["kernel_tflops"] / tf, "traffic": None,
+            "kernel": "attend_tc_kernel (tcgen05 attention, guidance-pair prefill: 64 lanes x "
+                      "64 rows over a shared 1,024-slot prefix; events recorded by the library "
+                      "around its launch)",
+            "peak_kind": "measured bf16 burst" if tf != 1900.0 else "fallback",
+            "alg_flops_per_launch": g["alg_flops"], "launch_us": g["kernel_us"]}
+        line["workloads"] = side
     if ws == 1 and not args.no_cpu_baseline:
         import oracle as O
         O.build()
@@ -571,19 +605,31 @@ WORKLOADS = {
 
 
 def run_workload(args, local):
+    """One JSON line for `--workload W` (see measure_workload)."""
+    import torch
+    torch.cuda.set_device(local)
+    print(json.dumps(measure_workload(args.workload, args.seed, args.steps, args.warmup, local)))
+
+
+def measure_workload(name, seed, K, Wm, local, device_fill=False):
     """Time one pass of another configuration (first pass of its scenario):
     every row's output and the readout rows; frozen lengths are restored
-    before every step so each step is identical."""
+    before every step so each step is identical.  With device_fill the
+    scenario's cached K/V are drawn on the device (same N(0,1) distribution,
+    seeded) instead of on the host."""
     import torch
     from programmable_paged_kv_gb300 import (ForwardPlan, build, make_desc, make_meta, runner,
                                              set_timing_events)
-    torch.cuda.set_device(local)
     build()
-    sc = WORKLOADS[args.workload](args.seed)
+    if device_fill:
+        with W.geometry_only():
+            sc = WORKLOADS[name](seed)
+    else:
+        sc = WORKLOADS[name](seed)
     d = sc.desc
     p = sc.passes[0]
     desc = make_desc(d)
-    pools = runner.DevicePools(sc)
+    pools = runner.DevicePools(sc, seed=seed)
     frozen0 = torch.from_numpy(sc.frozen_len0.astype(np.int32)).cuda()
     frozen = frozen0.clone()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -609,7 +655,6 @@ def run_workload(args, local):
     chan = None if p.channel is None else torch.from_numpy(p.channel.astype(np.int32)).cuda()
     stream = torch.cuda.current_stream()
     live = []
-    K, Wm = args.steps, args.warmup
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -647,11 +692,16 @@ def run_workload(args, local):
     # K more passes, instrumented (events between kernels stop each from
     # starting while the one before drains, so the throughput above is taken
     # without them); a sleep kernel first lets the host queue all K passes, so
-    # the events time the GPU's work, not host gaps
+    # the events time the GPU's work, not host gaps.  L2 is flushed before
+    # each instrumented pass (a 256 MB write, outside its events), so no
+    # pass starts with the previous one's K/V cached
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     torch.cuda._sleep(int(K * 1e6))
     for i in range(K):
+        flush.fill_(i & 0xFF)
         step(ev[i], kev[i])
     torch.cuda.synchronize()
+    del flush
     clk = clocks.stop()
     el = t0.elapsed_time(t1) / 1e3
     att = sorted(a.elapsed_time(b) for a, b in ev)
@@ -660,12 +710,9 @@ def run_workload(args, local):
     ker_med = ker[len(ker) // 2] / 1e3
     tok, byts, flops = pass_accounting(p, d)
     hbm, kind = peaks()
-    try:
-        tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
-    except Exception:
-        tf = 1900.0
+    tf = peaks_tensor()
     t_roof = max(byts / (hbm * 1e9), flops / (tf * 1e12))
-    line = {"workload": args.workload, "metric": METRIC, "unit": UNIT,
+    line = {"workload": name, "metric": METRIC, "unit": UNIT,
             "value": tok * K / el, "ms_per_step": 1e3 * el / K, "steps": K, "warmup": Wm,
             "attend_ms_median": att_med * 1e3, "attended_tokens_per_step": tok,
             "attend_alg_bytes": byts, "attend_alg_flops": flops,
@@ -681,7 +728,35 @@ def run_workload(args, local):
         line["clocks"] = clk
     for pl in live:
         pl.close()
-    print(json.dumps(line))
+    del pools
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+# The configurations beside the headline whose figures the default run adds
+# to its line: the tensor-core path (prefill TFLOP/s against the bf16 peak)
+# and the verify and masked passes.
+SIDE_WORKLOADS = ("guidance_prefill", "spec_verify", "masked_window", "masked_tova")
+
+
+def side_workloads(seed, local, steps=5, warmup=3):
+    """Kernel and call figures of the other configurations, a few passes
+    each (inputs drawn on the device), for the default line."""
+    out = {}
+    for name in SIDE_WORKLOADS:
+        r = measure_workload(name, seed, steps, warmup, local, device_fill=True)
+        out[name] = {
+            "kernel_us": 1e3 * r["kernel_ms_median"], "call_us": 1e3 * r["attend_ms_median"],
+            "kernel_tensor_frac": r["kernel_tensor_frac"], "kernel_hbm_frac": r["kernel_hbm_frac"],
+            "call_tensor_frac": r["attend_tensor_frac"], "call_hbm_frac": r["attend_hbm_frac"],
+            "call_roofline_frac": r["attend_roofline_frac"],
+            "kernel_tflops": r["attend_alg_flops"] / (r["kernel_ms_median"] * 1e-3) / 1e12,
+            "alg_bytes": r["attend_alg_bytes"], "alg_flops": r["attend_alg_flops"],
+            "attended_tokens_per_pass": r["attended_tokens_per_step"],
+            "pass_ms": r["ms_per_step"], "steps": steps, "status": r["status"],
+            "clocks": r.get("clocks")}
+    return out
 
 
 def run_readout(args, local):

@@ -40,9 +40,11 @@ def to_host(t, dtype: int) -> np.ndarray:
 
 class DevicePools:
     """Full-size K/V pools on the device, canary-filled, with the scenario's
-    initial pages written at their physical ids."""
+    initial pages written at their physical ids.  A scenario built without
+    its cached contents (workloads.geometry_only) gets its pages filled here
+    with N(0,1) values from a seeded device generator instead."""
 
-    def __init__(self, sc):
+    def __init__(self, sc, seed: int = 0):
         import torch
         d = sc.desc
         shape = (sc.num_pool_pages, d.num_kv_heads, d.page_size, d.head_dim)
@@ -54,8 +56,18 @@ class DevicePools:
             self.k.view(torch.int16).fill_(-1)
         self.v = self.k.clone()
         idx = torch.from_numpy(sc.pool_pages.astype(np.int64)).cuda()
-        self.k.index_copy_(0, idx, to_device(sc.k_init, d.dtype))
-        self.v.index_copy_(0, idx, to_device(sc.v_init, d.dtype))
+        if sc.k_init is None:
+            g = torch.Generator(device="cuda")
+            g.manual_seed(seed)
+            tdt = torch.float32 if d.dtype == 0 else torch.bfloat16
+            for t in (self.k, self.v):
+                for i in range(0, idx.numel(), 4096):
+                    part = idx[i:i + 4096]
+                    t.index_copy_(0, part, torch.randn((part.numel(),) + shape[1:], generator=g,
+                                                       device="cuda").to(tdt))
+        else:
+            self.k.index_copy_(0, idx, to_device(sc.k_init, d.dtype))
+            self.v.index_copy_(0, idx, to_device(sc.v_init, d.dtype))
         self.used = idx
 
 

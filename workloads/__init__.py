@@ -181,12 +181,37 @@ def mask_from_visible(visible_rows: List[np.ndarray]):
     return np.asarray(indptr, np.int64), allw.astype(np.uint32)
 
 
+# When False, generators leave a scenario's cached K/V unset (k_init and
+# v_init are None): the metadata and the per-row q/k/v are drawn as usual,
+# and whoever runs the scenario fills the pool pages itself (the benchmark
+# does so on the device with the same N(0,1) distribution, which is much
+# faster than drawing hundreds of MB on the host).  See geometry_only().
+_POOL_DATA = True
+
+
+class geometry_only:
+    """Context in which generators skip drawing the cached pool contents."""
+
+    def __enter__(self):
+        global _POOL_DATA
+        self._old, _POOL_DATA = _POOL_DATA, False
+        return self
+
+    def __exit__(self, *exc):
+        global _POOL_DATA
+        _POOL_DATA = self._old
+        return False
+
+
 def _fill_pool_init(desc: Desc, pool_pages: np.ndarray, lane_pages, cached, rng):
     """Random cached K/V for slots [0, cached[l]) of each lane; canary elsewhere.
 
     lane_pages[l] are the lane's physical pages in slot order.  Pages shared by
-    several lanes are filled once (by the first lane that lists them).
+    several lanes are filled once (by the first lane that lists them).  Inside
+    geometry_only() nothing is drawn and (None, None) is returned.
     """
+    if not _POOL_DATA:
+        return None, None
     U = pool_pages.size
     H, P, d = desc.num_kv_heads, desc.page_size, desc.head_dim
     k = canary_array((U, H, P, d), desc.dtype)
