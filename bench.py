@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "guidance_prefill", "spec_verify", "masked_window",
-                             "masked_tova", "decode_pass", "readout_topk", "decode_loop",
+                             "masked_tova", "masked_decode_window", "masked_decode_tova",
+                             "decode_pass", "readout_topk", "decode_loop",
                              "adapters_decode", "adapters_prefill", "batcher"],
                     help="decode_batch (default) is the benchmark line; the others time one "
                          "pass of another configuration")
@@ -600,6 +601,8 @@ WORKLOADS = {
     "spec_verify": lambda s: W.spec_verify(s),
     "masked_window": lambda s: W.masked_long(s, "window"),
     "masked_tova": lambda s: W.masked_long(s, "tova"),
+    "masked_decode_window": lambda s: W.masked_long(s, "window", rows=1),
+    "masked_decode_tova": lambda s: W.masked_long(s, "tova", rows=1),
     "decode_pass": lambda s: W.decode_batch(s),
 }
 
@@ -737,7 +740,8 @@ def measure_workload(name, seed, K, Wm, local, device_fill=False):
 # The configurations beside the headline whose figures the default run adds
 # to its line: the tensor-core path (prefill TFLOP/s against the bf16 peak)
 # and the verify and masked passes.
-SIDE_WORKLOADS = ("guidance_prefill", "spec_verify", "masked_window", "masked_tova")
+SIDE_WORKLOADS = ("guidance_prefill", "spec_verify", "masked_window", "masked_tova",
+                  "masked_decode_window", "masked_decode_tova")
 
 
 def side_workloads(seed, local, steps=5, warmup=3):

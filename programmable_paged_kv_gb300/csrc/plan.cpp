@@ -296,8 +296,14 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   const bool tc_ok = D.dtype == PIE_BF16 && D.head_dim == 128 &&
                      kTcTileQueries % G == 0 &&
                      static_cast<int64_t>(M.num_pool_pages) * Hkv * D.page_size <= INT32_MAX;
+  // A masked lane goes to the tensor-core kernel whatever its row count: that
+  // kernel walks the compacted list of the slots its rows see (whole pages of
+  // a window, single rows of a scattered mask), so a masked decode row reads
+  // only what it attends; its padding query rows cost MMA time, which a
+  // decode row's memory-bound work hides.
   auto lane_tc = [&](int l) {
-    return tc_ok && (M.row_indptr[l + 1] - M.row_indptr[l]) * G >= kTcMinQueries;
+    const int n = M.row_indptr[l + 1] - M.row_indptr[l];
+    return tc_ok && n > 0 && (n * G >= kTcMinQueries || H.has_mask);
   };
   // split-KV items: chunk length from the total work
   int64_t work = 0;

@@ -66,6 +66,8 @@ FULL_SAMPLING = {  # rows per lane the oracle recomputes, per pass kind
     "spec_verify": 1,
     "masked_window": 2,
     "masked_tova": 1,
+    "masked_decode_window": None,
+    "masked_decode_tova": None,
 }
 
 
@@ -116,6 +118,14 @@ MASKED_VARIANTS = {
                           dict(kind="tova", lanes=2, kv=900, rows=24)),
     "window_g1_two_tiles_p16": (W.Desc(8, 8, 128, 16, W.BF16),
                                 dict(kind="window", lanes=2, kv=777, rows=150, window=200)),
+    # decode rows (one or two per lane, G = 4 and 8): fewer than 16 query
+    # vectors per kv head, served by the tensor-core kernel's compacted lists
+    "window_decode_p16": (W.Desc(32, 8, 128, 16, W.BF16),
+                          dict(kind="window", lanes=3, kv=2000, rows=1, window=500)),
+    "tova_decode_p8": (W.Desc(32, 8, 128, 8, W.BF16),
+                       dict(kind="tova", lanes=3, kv=1500, rows=1)),
+    "window_two_rows_g8_p32": (W.Desc(16, 2, 128, 32, W.BF16),
+                               dict(kind="window", lanes=2, kv=1700, rows=2, window=333)),
 }
 
 

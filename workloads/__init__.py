@@ -494,6 +494,10 @@ def small(name: str, seed: int = 0) -> Scenario:
         return masked_long(seed, "window", lanes=2, kv=1100, rows=40, window=300)
     if name == "masked_tova":
         return masked_long(seed, "tova", lanes=2, kv=1100, rows=40)
+    if name == "masked_decode_window":
+        return masked_long(seed, "window", lanes=3, kv=1300, rows=1, window=300)
+    if name == "masked_decode_tova":
+        return masked_long(seed, "tova", lanes=3, kv=1300, rows=1)
     raise ValueError(name)
 
 
@@ -635,5 +639,8 @@ FULL = {
     "spec_verify": lambda seed=0: spec_verify(seed),
     "masked_window": lambda seed=0: masked_long(seed, "window"),
     "masked_tova": lambda seed=0: masked_long(seed, "tova"),
+    # masked decode: one row per lane at the end of the same working sets
+    "masked_decode_window": lambda seed=0: masked_long(seed, "window", rows=1),
+    "masked_decode_tova": lambda seed=0: masked_long(seed, "tova", rows=1),
 }
 SMALL_NAMES = list(FULL.keys())
