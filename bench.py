@@ -663,9 +663,19 @@ def measure_workload(name, seed, K, Wm, local, device_fill=False):
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
 
-    def step(e=None, ke=None):
+    mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+
+    def step(e=None, ke=None, me=None):
         frozen.copy_(frozen0, non_blocking=True)
         plan = ForwardPlan(desc, meta, workspace=ws)
+        if mw is not None:
+            # the pass's mask lists, built once for every layer's attend
+            if me is not None:
+                me[0].record(stream)
+            plan.set_mask(mw)
+            if me is not None:
+                me[1].record(stream)
         plan.append_kv(q, k, v, q_rot, pools.k, pools.v, frozen, status)
         if e is not None:
             e[0].record(stream)
@@ -702,7 +712,7 @@ def measure_workload(name, seed, K, Wm, local, device_fill=False):
     torch.cuda._sleep(int(K * 1e6))
     for i in range(K):
         flush.fill_(i & 0xFF)
-        step(ev[i], kev[i])
+        step(ev[i], kev[i], mev[i])
     torch.cuda.synchronize()
     del flush
     clk = clocks.stop()
@@ -711,6 +721,8 @@ def measure_workload(name, seed, K, Wm, local, device_fill=False):
     att_med = att[len(att) // 2] / 1e3
     ker = sorted(a.elapsed_time(b) for a, b in kev)
     ker_med = ker[len(ker) // 2] / 1e3
+    msk = sorted(a.elapsed_time(b) for a, b in mev) if mw is not None else [0.0]
+    msk_med = msk[len(msk) // 2] / 1e3
     tok, byts, flops = pass_accounting(p, d)
     hbm, kind = peaks()
     tf = peaks_tensor()
@@ -723,6 +735,7 @@ def measure_workload(name, seed, K, Wm, local, device_fill=False):
             "attend_tflops": flops / att_med / 1e12, "attend_tensor_frac": flops / att_med / 1e12 / tf,
             "attend_roofline_frac": t_roof / att_med,
             "kernel_ms_median": ker_med * 1e3,
+            "mask_lists_ms_median": msk_med * 1e3,
             "kernel_hbm_frac": byts / ker_med / 1e9 / hbm,
             "kernel_tensor_frac": flops / ker_med / 1e12 / tf,
             "status": int(status.item()),
@@ -752,6 +765,7 @@ def side_workloads(seed, local, steps=5, warmup=3):
         r = measure_workload(name, seed, steps, warmup, local, device_fill=True)
         out[name] = {
             "kernel_us": 1e3 * r["kernel_ms_median"], "call_us": 1e3 * r["attend_ms_median"],
+            "mask_lists_us_per_pass": 1e3 * r["mask_lists_ms_median"],
             "kernel_tensor_frac": r["kernel_tensor_frac"], "kernel_hbm_frac": r["kernel_hbm_frac"],
             "call_tensor_frac": r["attend_tensor_frac"], "call_hbm_frac": r["attend_hbm_frac"],
             "call_roofline_frac": r["attend_roofline_frac"],

@@ -185,6 +185,23 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
                    float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
                    void* stream);
 
+/* The pass's attention mask, once for every layer ("The forward pass",
+ * Attention masks: the mask belongs to the ForwardPass, and every attention
+ * layer of the pass applies it).  For the row blocks served by the
+ * tensor-core kernel, attention walks a compacted list of the slots some row
+ * of the block sees (and each row's mask re-expressed over that list), built
+ * from the mask words and the page table -- data of the pass, not of the
+ * layer.  pie_fwd_set_mask builds those lists on `stream` into the plan's
+ * workspace and records `mask_words`; every later pie_fwd_attend call on this
+ * plan given the same mask_words pointer reuses them instead of building them
+ * again (so an L-layer model builds them once, not L times).  The words must
+ * not change while the plan uses them; an attend call given another pointer
+ * builds the lists itself, as it does when set_mask was never called.
+ * mask_words: device uint32 words, as for pie_fwd_attend.  Not thread-safe
+ * with other calls on the same plan.  Errors: PIE_EINVAL (NULL plan or
+ * words, a plan without a mask), PIE_ECUDA (launch). */
+int pie_fwd_set_mask(pie_fwd_plan_t* plan, const uint32_t* mask_words, void* stream);
+
 /* Step 4 (State geometry: fold).  frozen_len[l] += k_l with k_l = 0 (NONE),
  * n_l (ALL), fold_count[l] (COUNT) or clamp(channel[l], 0, n_l) (CHANNEL;
  * PIE_STATUS_FOLD_CLAMP when clamped).  channel: device int32 [L], written
@@ -245,6 +262,14 @@ int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t rows, int32_
  *            step's rotated queries on return).
  *   out [steps][L][Hq][d] (pass dtype), lse [steps][L][Hq] (fp32, or NULL):
  *            each step's attention output of every lane.
+ *   channel [steps][L]: device int32, or NULL (every step folds its token).
+ *            Step t of lane l freezes clamp(channel[t][l], 0, 1) slots (State
+ *            geometry, speculative-decoding paragraph: the accepted count comes
+ *            from a device channel; out-of-range counts are clamped and set
+ *            PIE_STATUS_FOLD_CLAMP).  A lane that freezes 0 keeps its frozen
+ *            length, so its next step writes the same slot at the same
+ *            position and the rejected token is overwritten before it is read.
+ *            channel[t] must be written on `stream` before step t's fold.
  *   workspace: device, 256-byte aligned, at least
  *            pie_fwd_decode_loop_workspace_bytes(); status: device uint32 or
  *            NULL.
@@ -257,8 +282,8 @@ int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, int32_t ste
                         const int32_t* page_indptr, const int32_t* page_ids,
                         int32_t max_pages_per_lane, int32_t* frozen_len, const void* q,
                         const void* k, const void* v, void* q_rot, void* k_pool, void* v_pool,
-                        void* out, float* lse, void* workspace, size_t ws_bytes,
-                        uint32_t* status, void* stream);
+                        void* out, float* lse, const int32_t* channel, void* workspace,
+                        size_t ws_bytes, uint32_t* status, void* stream);
 
 /* Per-lane adapters at a projection site ("The forward pass", section
  * Adapters: an adapter is a function of a projection's input x and base

@@ -103,9 +103,10 @@ def decode_loop_workspace_bytes(desc: abi.pie_fwd_desc, num_lanes: int, max_page
 
 def decode_loop(desc: abi.pie_fwd_desc, page_indptr, page_ids, max_pages_per_lane: int,
                 frozen_len, q, k, v, q_rot, k_pool, v_pool, out, lse=None, status=None,
-                workspace=None, stream=None):
+                workspace=None, stream=None, channel=None):
     """pie_fwd_decode_loop: q [steps, L, Hq, d], k/v [steps, L, Hkv, d], out
-    like q; page_indptr / page_ids / frozen_len int32 CUDA tensors."""
+    like q; page_indptr / page_ids / frozen_len int32 CUDA tensors; channel:
+    optional int32 CUDA tensor [steps, L] of per-step fold counts."""
     import torch
     steps, L = int(q.shape[0]), int(q.shape[1])
     if workspace is None:
@@ -115,7 +116,8 @@ def decode_loop(desc: abi.pie_fwd_desc, page_indptr, page_ids, max_pages_per_lan
         C.byref(desc), L, steps, _ptr(page_indptr, "page_indptr"), _ptr(page_ids, "page_ids"),
         max_pages_per_lane, _ptr(frozen_len, "frozen_len"), _ptr(q, "q"), _ptr(k, "k"),
         _ptr(v, "v"), _ptr(q_rot, "q_rot"), _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
-        _ptr(out, "out"), _ptr(lse, "lse", False), _ptr(workspace, "workspace"), workspace.numel(),
+        _ptr(out, "out"), _ptr(lse, "lse", False), _ptr(channel, "channel", False),
+        _ptr(workspace, "workspace"), workspace.numel(),
         _ptr(status, "status", False), _stream(stream)), "pie_fwd_decode_loop")
 
 
@@ -195,6 +197,12 @@ class ForwardPlan:
             self.handle, _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(q_rot, "q_rot"),
             _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"), _ptr(frozen_len, "frozen_len"),
             _ptr(status, "status", False), _stream(stream)), "pie_fwd_append_kv")
+
+    def set_mask(self, mask_words, stream=None):
+        """pie_fwd_set_mask: build the pass's compacted mask lists once; later
+        attend calls given the same mask_words tensor reuse them."""
+        abi.check(self.lib.pie_fwd_set_mask(self.handle, _ptr(mask_words, "mask_words"),
+                                            _stream(stream)), "pie_fwd_set_mask")
 
     def attend(self, q_rot, k_pool, v_pool, mask_words=None, out_readout=None, lse_readout=None,
                out_all=None, lse_all=None, status=None, stream=None):

@@ -69,12 +69,14 @@ SIGNATURES = {
     "pie_fwd_last_error": (C.c_char_p, []),
     "pie_fwd_abi_version": (C.c_int, []),
     "pie_fwd_set_timing_events": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "pie_fwd_set_mask": (C.c_int, [_P, _P, _P]),
     "pie_fwd_decode_loop_workspace_bytes": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32,
                                                       C.c_int32, C.POINTER(C.c_size_t)]),
     "pie_fwd_decode_loop": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32, C.c_int32, C.c_void_p,
                                       C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                                      C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]),
+                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
+                                      C.c_void_p]),
     "pie_fwd_readout_topk_workspace_bytes": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                                        C.POINTER(C.c_size_t)]),
     "pie_fwd_readout_topk": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int64,

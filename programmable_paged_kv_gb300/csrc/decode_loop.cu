@@ -15,6 +15,15 @@
 // A lane whose pages hold no slot for its next token (frozen_len[l] >= its
 // pages x page_size) writes nothing, gets a zero output and -inf lse, does not
 // advance, and sets PIE_STATUS_LOOP_FULL.
+//
+// With a channel (device int32 [steps][L]), step t freezes clamp(channel[t][l],
+// 0, 1) slots instead of one (State geometry, speculative-decoding paragraph:
+// the count comes from a device channel; a count outside [0, 1] is clamped and
+// sets PIE_STATUS_FOLD_CLAMP).  A lane whose count is 0 keeps its frozen
+// length: its next step writes the same slot again, at the same position, so
+// the rejected token's K/V is overwritten before anything reads it.  Whatever
+// device code decides the counts (a stop-token test, a draft acceptance) writes
+// channel[t] before step t's fold on the stream.
 
 #include <cmath>
 #include <cstring>
@@ -88,7 +97,7 @@ __global__ void loop_init_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int 
 // visible slots [0, kv_len) in kLoopChunk-slot chunks (chunks past kv_len are
 // empty items, whose partial state is (-inf, 0)).
 __global__ void loop_step_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int P,
-                                 const int32_t* frozen_len, uint32_t* status) {
+                                 const int32_t* frozen_len, int fold_mode, uint32_t* status) {
   grid_dep_wait();  // the previous step's fold
   grid_dep_launch();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -105,7 +114,7 @@ __global__ void loop_step_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int 
       const_cast<int32_t*>(m.positions)[l] = f;
       const_cast<int32_t*>(m.slots)[l] = ok ? f : -1;  // -1: no slot, nothing is written
       const_cast<int32_t*>(m.kv_len)[l] = ext;
-      const_cast<int32_t*>(m.fold_mode)[l] = ok ? PIE_FOLD_ALL : PIE_FOLD_NONE;
+      const_cast<int32_t*>(m.fold_mode)[l] = ok ? fold_mode : PIE_FOLD_NONE;
       if (!ok) set_status(status, PIE_STATUS_LOOP_FULL);
     }
   }
@@ -151,8 +160,8 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
                                    int32_t max_pages_per_lane, int32_t* frozen_len,
                                    const void* q, const void* k, const void* v, void* q_rot,
                                    void* k_pool, void* v_pool, void* out, float* lse,
-                                   void* workspace, size_t ws_bytes, uint32_t* status,
-                                   void* stream) {
+                                   const int32_t* channel, void* workspace, size_t ws_bytes,
+                                   uint32_t* status, void* stream) {
   int G = 0, nq = 0, MC = 0;
   int rc = loop_check(desc, num_lanes, max_pages_per_lane, G, nq, MC);
   if (rc != PIE_OK) return rc;
@@ -213,7 +222,8 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
   const int items = L * Hkv * MC;
   for (int t = 0; t < steps && e == cudaSuccess; ++t) {
     e = launch_dependent(loop_step_kernel, dim3((items + 255) / 256), dim3(256), 0, s, true, m, L,
-                         Hkv, MC, nq, D.page_size, frozen_len, status);
+                         Hkv, MC, nq, D.page_size, frozen_len,
+                         channel ? PIE_FOLD_CHANNEL : PIE_FOLD_ALL, status);
     if (e == cudaSuccess)
       e = launch_rope_scatter(p, static_cast<const char*>(q) + t * q_step,
                               static_cast<const char*>(k) + t * kv_step,
@@ -224,7 +234,8 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
     if (e == cudaSuccess)
       e = launch_combine(p, static_cast<char*>(out) + t * q_step, lse ? lse + size_t(t) * L * Hq : nullptr,
                          nullptr, nullptr, s);
-    if (e == cudaSuccess) e = launch_fold(p, frozen_len, nullptr, status, s);
+    if (e == cudaSuccess)
+      e = launch_fold(p, frozen_len, channel ? channel + size_t(t) * L : nullptr, status, s);
   }
   if (e != cudaSuccess)
     return set_last_error(PIE_ECUDA, std::string("decode loop launch: ") + cudaGetErrorString(e));

@@ -154,6 +154,8 @@ struct pie_fwd_plan {
   int32_t mblock_max_rows;   // most rows in a masked row block
   int64_t num_part_slots;
   int32_t num_comb_merge;    // combine entries with chunks to merge (0: no combine launch)
+  const uint32_t* mask_set;  // mask words whose compacted lists the workspace holds
+                             // (pie_fwd_set_mask), or NULL
   pie::DevMeta dev;
   pie::PinnedBlock* staging;
 };

@@ -483,7 +483,7 @@ extern "C" {
 
 const char* pie_fwd_last_error(void) { return g_last_error.c_str(); }
 
-int pie_fwd_abi_version(void) { return 102; }
+int pie_fwd_abi_version(void) { return 103; }
 
 static thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 
@@ -662,7 +662,10 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
     return fail(PIE_EINVAL, "attend: out_readout (or out_all) is required");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (plan->num_mblocks > 0) e = launch_mask_compact(*plan, mask_words, s);
+  // the compacted lists are a function of the pass (mask words and page
+  // table), not of the layer: after pie_fwd_set_mask they are reused
+  if (plan->num_mblocks > 0 && mask_words != plan->mask_set)
+    e = launch_mask_compact(*plan, mask_words, s);
   if (e == cudaSuccess && g_ev_start) e = cudaEventRecord(g_ev_start, s);
   if (e == cudaSuccess && plan->num_dec_items > 0)
     e = launch_attend_decode(*plan, q_rot, k_pool, v_pool, mask_words, status, s);
@@ -673,6 +676,20 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
   if (e == cudaSuccess && plan->num_comb_merge > 0)
     e = launch_combine(*plan, out_readout, lse_readout, out_all, lse_all, s);
   if (e != cudaSuccess) return fail(PIE_ECUDA, std::string("attend launch: ") + cudaGetErrorString(e));
+  return PIE_OK;
+}
+
+int pie_fwd_set_mask(pie_fwd_plan_t* plan, const uint32_t* mask_words, void* stream) {
+  if (!plan) return fail(PIE_EINVAL, "plan is NULL");
+  if (!plan->has_mask) return fail(PIE_EINVAL, "set_mask: the plan has no mask");
+  if (!mask_words) return fail(PIE_EINVAL, "set_mask: mask_words is NULL");
+  plan->mask_set = nullptr;
+  if (plan->num_mblocks > 0) {
+    cudaError_t e = launch_mask_compact(*plan, mask_words, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+      return fail(PIE_ECUDA, std::string("set_mask launch: ") + cudaGetErrorString(e));
+  }
+  plan->mask_set = mask_words;
   return PIE_OK;
 }
 

@@ -21,7 +21,7 @@ def _lib():
     build()
 
 
-def _run_loop(sc, steps, frozen0=None):
+def _run_loop(sc, steps, frozen0=None, channel=None):
     import torch
     from programmable_paged_kv_gb300 import decode_loop, make_desc, runner
     d = sc.desc
@@ -41,8 +41,9 @@ def _run_loop(sc, steps, frozen0=None):
     out = torch.empty_like(q)
     lse = torch.empty((steps, L, Hq), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ch = None if channel is None else torch.from_numpy(np.asarray(channel, np.int32)).cuda()
     decode_loop(desc, page_indptr, page_ids, maxp, frozen, q, k, v, q_rot, pools.k, pools.v, out,
-                lse, status)
+                lse, status, channel=ch)
     torch.cuda.synchronize()
     k_used = runner.to_host(pools.k.index_select(0, pools.used), d.dtype)
     v_used = runner.to_host(pools.v.index_select(0, pools.used), d.dtype)
@@ -90,3 +91,39 @@ def test_lanes_without_a_free_slot_write_nothing():
     for t in range(2):
         assert not np.any(gouts[t].astype(np.float64))
         assert np.all(np.isneginf(glse[t]))
+
+
+def test_channel_fold_matches_the_pass_by_pass_oracle():
+    """Step t folds clamp(channel[t][l], 0, 1): a lane given 0 keeps its frozen
+    length, so its next step rewrites the same slot at the same position (the
+    rejected token's K/V is overwritten, never read); counts outside [0, 1]
+    (-1, 2, 7) are clamped and set PIE_STATUS_FOLD_CLAMP.  The oracle runs the
+    same steps one pass at a time with the geometry each count implies."""
+    steps, lanes = 8, 6
+    sc = W.decode_loop(7, lanes=lanes, steps=steps, c_lo=1, c_hi=900, num_pool_pages=700,
+                       desc=W.Desc(32, 8, 128, 16, W.BF16))
+    rng = np.random.default_rng(11)
+    channel = rng.choice([0, 1, 1, 1, -1, 2, 7], size=(steps, lanes)).astype(np.int32)
+    gk, gv, gfrozen, gouts, glse, gstatus, untouched = _run_loop(sc, steps, channel=channel)
+    # the oracle: step t at position = slot = F_t, kv_len F_t + 1, fold from
+    # the channel (the oracle clamps and flags)
+    k_pool, v_pool = sc.k_init.copy(), sc.v_init.copy()
+    frozen = sc.frozen_len0.copy().astype(np.int32)
+    ostatus = 0
+    cp = sc.compact_page_ids(sc.passes[0].page_ids)
+    for t in range(steps):
+        p = sc.passes[t]
+        F = frozen.copy()
+        pt = W.Pass(p.row_indptr, F.copy(), F.copy(), (F + 1).astype(np.int32), p.page_indptr,
+                    p.page_ids, np.full(lanes, W.FOLD_CHANNEL, np.int32), p.fold_count, p.q, p.k,
+                    p.v, channel=channel[t])
+        r = O.run_pass(sc.desc, pt, k_pool, v_pool, frozen, page_ids=cp, num_threads=4)
+        assert r["err"] == O.OK
+        ostatus |= r["status"]
+        assert_out_close(gouts[t], r["out"], sc.desc.dtype, f"step {t} out")
+        assert_lse_close(glse[t], r["lse"], sc.desc.dtype, f"step {t} lse")
+    assert untouched
+    assert np.array_equal(gfrozen, frozen)
+    assert gstatus == ostatus and (gstatus & 2)  # PIE_STATUS_FOLD_CLAMP
+    assert_rope_close(gk, k_pool, sc.desc.dtype, "K pool")
+    assert_bits_equal(gv, v_pool, "V pool")

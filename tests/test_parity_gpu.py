@@ -137,6 +137,48 @@ def test_masked_list_modes(var):
     compare_scenario(sc, gpu, orc)
 
 
+def test_set_mask_lists_serve_every_layer():
+    """pie_fwd_set_mask builds a pass's compacted lists once; attend on two
+    layers (two pairs of pools, the same mask) reuses them and returns what
+    a plan that builds its own lists at every attend returns, bit for bit."""
+    import torch
+    from programmable_paged_kv_gb300 import ForwardPlan, make_desc, make_meta, runner
+    for sc in (W.small("masked_window", 2), W.small("masked_decode_tova", 2)):
+        d, p = sc.desc, sc.passes[0]
+        desc = make_desc(d)
+        layers = [runner.DevicePools(sc), runner.DevicePools(sc)]
+        # the second layer's cached K/V differ from the first's
+        g = torch.Generator(device="cuda").manual_seed(5)
+        for t in (layers[1].k, layers[1].v):
+            t.index_copy_(0, layers[1].used, torch.randn(
+                (layers[1].used.numel(),) + tuple(t.shape[1:]), generator=g,
+                device="cuda").to(t.dtype))
+        N, Hq, D = p.num_rows, d.num_q_heads, d.head_dim
+        mw = torch.from_numpy(p.mask_words.view(np.int32)).cuda()
+        q_rot = torch.empty((N, Hq, D), dtype=torch.bfloat16, device="cuda")
+        outs = {}
+        for mode in ("set_mask", "per_call"):
+            plan = ForwardPlan(desc, make_meta(p, sc.num_pool_pages))
+            frozen = torch.from_numpy(sc.frozen_len0.astype(np.int32)).cuda()
+            q, k, v = (runner.to_device(x, d.dtype) for x in (p.q, p.k, p.v))
+            if mode == "set_mask":
+                plan.set_mask(mw)
+            for li, pools in enumerate(layers):
+                kk, vv = pools.k.clone(), pools.v.clone()
+                plan.append_kv(q, k, v, q_rot, kk, vv, frozen)
+                o = torch.empty((N, Hq, D), dtype=torch.bfloat16, device="cuda")
+                lse = torch.empty((N, Hq), dtype=torch.float32, device="cuda")
+                ro = torch.empty((plan.num_readout, Hq, D), dtype=torch.bfloat16, device="cuda")
+                plan.attend(q_rot, kk, vv, mw, ro, None, o, lse)
+                outs[(mode, li)] = (o.view(torch.int16).cpu(), lse.cpu())
+            torch.cuda.synchronize()
+            plan.close()
+        for li in range(2):
+            a, b = outs[("set_mask", li)], outs[("per_call", li)]
+            assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        assert not torch.equal(outs[("set_mask", 0)][0], outs[("set_mask", 1)][0])
+
+
 # ---------------------------------------------------------------- edge cases
 def _one_pass_scenario(desc, p, frozen0, pool_pages_n, fill_slots):
     """Scenario around one hand-made pass; fill_slots[l] cached slots random."""
