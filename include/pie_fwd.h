@@ -84,6 +84,10 @@ extern "C" {
 /* ---- device status bits ---------------------------------------------------- */
 #define PIE_STATUS_FROZEN_WRITE 1u /* a row's slot was frozen; its K/V write was skipped */
 #define PIE_STATUS_FOLD_CLAMP 2u   /* a channel count outside [0, n] was clamped          */
+#define PIE_STATUS_BOUNDS 4u       /* a device-supplied page id outside the pool, or a
+                                      kv_len past the lane's pages, was skipped or cut
+                                      (decode loop, no-allocation decode); outputs of the
+                                      lanes concerned are invalid                         */
 #define PIE_STATUS_FOLD_GAP 8u     /* a folding lane's first slot != its frozen length    */
 #define PIE_STATUS_TIMEOUT 16u     /* a kernel's bounded wait expired; outputs invalid    */
 #define PIE_STATUS_LOOP_FULL 64u     /* decode loop: a lane had no slot left for a token   */
@@ -254,6 +258,9 @@ int pie_fwd_readout_topk(const void* logits, int32_t dtype, int32_t rows, int32_
  * never synchronizes the host and may be captured in a CUDA graph.
  *   page_indptr [L+1], page_ids: device, the lanes' page lists (as in
  *            pie_fwd_meta); each lane's capacity is its pages x page_size.
+ *   num_pool_pages: host, pages per pool; the kernels check every page id
+ *            they read against it (an id outside [0, num_pool_pages) is
+ *            neither written nor read and sets PIE_STATUS_BOUNDS).
  *   max_pages_per_lane: host, a bound on every lane's page count (sizes the
  *            work-item grid and the workspace).
  *   frozen_len [L]: device int32, read and advanced on the device.
@@ -280,7 +287,8 @@ int pie_fwd_decode_loop_workspace_bytes(const pie_fwd_desc* desc, int32_t num_la
                                         int32_t max_pages_per_lane, size_t* bytes);
 int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, int32_t steps,
                         const int32_t* page_indptr, const int32_t* page_ids,
-                        int32_t max_pages_per_lane, int32_t* frozen_len, const void* q,
+                        int32_t num_pool_pages, int32_t max_pages_per_lane,
+                        int32_t* frozen_len, const void* q,
                         const void* k, const void* v, void* q_rot, void* k_pool, void* v_pool,
                         void* out, float* lse, const int32_t* channel, void* workspace,
                         size_t ws_bytes, uint32_t* status, void* stream);
@@ -351,6 +359,19 @@ void pie_fwd_adapter_plan_destroy(pie_fwd_adapter_plan_t* plan);
  * turns the hook off.  Returns PIE_EINVAL when exactly one is NULL. */
 int pie_fwd_set_timing_events(void* start_event, void* stop_event);
 
+/* Test hook (the Pie pages have no counterpart: it exists so that tests can
+ * run the bounded-wait failure path without faulting or hanging a GPU).  After
+ * pie_fwd_test_wait_expiry(stage, wait_us) with stage >= 0, every split-KV
+ * attention kernel that the calling thread launches (pie_fwd_attend, the
+ * decode loop, the no-allocation decode) has its producer warp stop before
+ * stage `stage` of every work item -- so no copy of that stage, or of any
+ * later one, is ever in flight -- and gives each of its waits `wait_us`
+ * microseconds: the compute warps' wait for that stage expires, the kernel
+ * sets PIE_STATUS_TIMEOUT, writes whatever partial state it has and returns.
+ * Items with fewer stages are not affected.  (-1, 0) turns the hook off.
+ * Errors: PIE_EINVAL for stage < -1, or stage >= 0 with wait_us == 0. */
+int pie_fwd_test_wait_expiry(int32_t stage, uint32_t wait_us);
+
 /* ABI version of this header (major * 100 + minor). */
 int pie_fwd_abi_version(void);
 
@@ -367,6 +388,10 @@ int pie_fwd_abi_version(void);
  * pie_fwd_attend does for a plan whose lanes have one row each.
  *   slots, kv_len: device int32 [num_lanes]; page_indptr: device int32
  *   [num_lanes + 1]; page_ids: device int32 (pool layout as above);
+ *   num_pool_pages: pages per pool.  These arrays are device data, so they
+ *   are checked on the device: a lane's extent is cut to the slots its pages
+ *   hold, and a page id outside [0, num_pool_pages) is not read; either sets
+ *   PIE_STATUS_BOUNDS (that lane's output is then invalid);
  *   q_rot: device [num_lanes][Hq][d] (e.g. from pie_fwd_append_kv);
  *   k_pool, v_pool: device pools, read only;
  *   out: device [num_lanes][Hq][d] in the dtype; lse: device float
@@ -386,7 +411,8 @@ int pie_fwd_abi_version(void);
 int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t num_lanes,
                                   int32_t max_kv_len, const int32_t* slots,
                                   const int32_t* kv_len, const int32_t* page_indptr,
-                                  const int32_t* page_ids, const void* q_rot,
+                                  const int32_t* page_ids, int32_t num_pool_pages,
+                                  const void* q_rot,
                                   const void* k_pool, const void* v_pool, void* out,
                                   float* lse, uint32_t* status, void* stream);
 

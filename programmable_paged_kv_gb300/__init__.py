@@ -114,7 +114,8 @@ def decode_loop(desc: abi.pie_fwd_desc, page_indptr, page_ids, max_pages_per_lan
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     abi.check(abi.load().pie_fwd_decode_loop(
         C.byref(desc), L, steps, _ptr(page_indptr, "page_indptr"), _ptr(page_ids, "page_ids"),
-        max_pages_per_lane, _ptr(frozen_len, "frozen_len"), _ptr(q, "q"), _ptr(k, "k"),
+        int(k_pool.shape[0]), max_pages_per_lane, _ptr(frozen_len, "frozen_len"), _ptr(q, "q"),
+        _ptr(k, "k"),
         _ptr(v, "v"), _ptr(q_rot, "q_rot"), _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
         _ptr(out, "out"), _ptr(lse, "lse", False), _ptr(channel, "channel", False),
         _ptr(workspace, "workspace"), workspace.numel(),

@@ -73,7 +73,8 @@ SIGNATURES = {
     "pie_fwd_decode_loop_workspace_bytes": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32,
                                                       C.c_int32, C.POINTER(C.c_size_t)]),
     "pie_fwd_decode_loop": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32, C.c_int32, C.c_void_p,
-                                      C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_void_p,
                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
                                       C.c_void_p]),
@@ -83,7 +84,9 @@ SIGNATURES = {
                                        C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_void_p, C.c_size_t, C.c_void_p]),
     "pie_fwd_decode_attend_noalloc": (C.c_int, [C.POINTER(pie_fwd_desc), C.c_int32, C.c_int32,
-                                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+                                                _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, _P,
+                                                _P, _P]),
+    "pie_fwd_test_wait_expiry": (C.c_int, [C.c_int32, C.c_uint32]),
     "pie_fwd_adapter_workspace_bytes": (C.c_int, [C.c_int32, _P, C.c_int32,
                                                   C.POINTER(C.c_size_t)]),
     "pie_fwd_adapter_plan": (C.c_int, [C.c_int32, _P, _P, C.c_int32, C.c_int32, _P, C.c_size_t,

@@ -165,13 +165,18 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
   const int nstages = ke > kb ? (ke - kb + kStageSlots - 1) / kStageSlots : 0;
   const int nqv = it.nrows * G;  // valid query vectors
 
+  // every wait gives up after the limit (the test hook may shorten it)
+  const uint64_t wait_ns = m.test_wait_us ? uint64_t(m.test_wait_us) * 1000ull : kWaitLimitNs;
+
   if (warp == C::WARPS) {
     // ---------------- producer warp: TMA bulk copies of K/V pages ----------
     // Lanes 2i and 2i + 1 copy the K and the V block of page (stage start /
     // P + i) of every stage (a warp's copies issue one after another, so
     // each comes from its own lane); the page ids of the next stage are
     // fetched while this one is issued, so no copy waits on a dependent
-    // global load.
+    // global load.  A page id outside the pool is not copied (its slots keep
+    // whatever the stage held) and sets PIE_STATUS_BOUNDS: page tables that
+    // device code supplies are checked here.
     const uint64_t pol = policy_evict_first();
     const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
     const int64_t head_stride = int64_t(P) * D;  // elements per (page, kv head) block
@@ -183,17 +188,27 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
     };
     int64_t pid = nstages > 0 ? page_of(0) : 0;
     for (int s = 0; s < nstages; ++s) {
+      // test hook: stop before this stage (no copy of it is ever issued, so
+      // none is in flight when the compute warps' waits for it expire)
+      if (s == m.test_stall - 1) break;
       const int st = s % C::STAGES, use = s / C::STAGES;
-      if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1)) {
+      if (use > 0 && !mbar_wait_ns(&empty[st], (use - 1) & 1, wait_ns)) {
         if (lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
         break;
       }
       const int sb = kb + s * kStageSlots;
       const int se = min(sb + kStageSlots, ke);
       const int p0 = sb / P, p1 = (se - 1) / P;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * blk * uint32_t(p1 - p0 + 1));
+      const bool mine = (lane >> 1) <= p1 - p0;
+      const bool in_pool = pid >= 0 && pid < m.num_pool_pages;
+      const bool issue = mine && in_pool;
+      const uint32_t copies = __popc(__ballot_sync(0xffffffffu, issue));
+      if (lane == 0) {
+        if (copies != 2u * uint32_t(p1 - p0 + 1)) set_status(status, PIE_STATUS_BOUNDS);
+        mbar_arrive_expect_tx(&full[st], blk * copies);
+      }
       __syncwarp();
-      if ((lane >> 1) <= p1 - p0) {
+      if (issue) {
         const bool is_v = lane & 1;
         T* dst = ring + size_t(st) * 2 * kStageSlots * D + (is_v ? kStageSlots * D : 0);
         const int64_t src = (pid * Hkv + it.kv_head) * head_stride;
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(DecCfg<T, D, NQ>::THREADS, DecCfg<T, D, NQ>::M
 
   for (int s = 0; s < nstages; ++s) {
     const int st = s % C::STAGES;
-    if (!mbar_wait(&full[st], (s / C::STAGES) & 1)) {
+    if (!mbar_wait_ns(&full[st], (s / C::STAGES) & 1, wait_ns)) {
       timed_out = true;
       break;
     }
@@ -372,8 +387,10 @@ static cudaError_t launch_dec(const pie_fwd_plan_t& p, const void* q_rot, const 
   static std::atomic<uint64_t> configured{0};  // per instantiation and device
   cudaError_t e = set_smem_limit(attend_decode_kernel<T, D, NQ>, int(C::SMEM), configured);
   if (e != cudaSuccess) return e;
+  DevMeta m = p.dev;
+  test_wait_hook(&m.test_stall, &m.test_wait_us);
   return launch_dependent(attend_decode_kernel<T, D, NQ>, dim3(p.num_dec_items), dim3(C::THREADS),
-                          C::SMEM, s, true, p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
+                          C::SMEM, s, true, m, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
                           p.desc.page_size, p.desc.sm_scale * kLog2e, static_cast<const T*>(q_rot),
                           static_cast<const T*>(k_pool), static_cast<const T*>(v_pool), mask_words,
                           status);

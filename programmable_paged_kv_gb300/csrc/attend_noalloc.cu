@@ -59,10 +59,13 @@ static cudaError_t noalloc_scratch(void** out) {
 // Work items: (lane l, kv head g, chunk c) -> slots [c*CH, min(extent, (c+1)*CH))
 // of lane l's single row, where extent = min(kv_len[l], slots[l] + 1) (default
 // visibility).  Chunks past the extent are empty items whose partial state is
-// (-inf, 0).  extent is clamped to max_kv_len (PIE_STATUS_NOALLOC_TRUNC).
-__global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_len,
+// (-inf, 0).  extent is clamped to max_kv_len (PIE_STATUS_NOALLOC_TRUNC) and to
+// the slots the lane's pages hold (PIE_STATUS_BOUNDS: the page table is device
+// data, so it is checked here rather than on the host).
+__global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_len, int P,
                                      const int32_t* __restrict__ slots,
-                                     const int32_t* __restrict__ kv_len, DecItem* items,
+                                     const int32_t* __restrict__ kv_len,
+                                     const int32_t* __restrict__ page_indptr, DecItem* items,
                                      CombEntry* comb, int32_t* readout, uint32_t* status) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < L * Hkv * MC) {
@@ -71,6 +74,11 @@ __global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_
     if (ext > max_kv_len) {
       ext = max_kv_len;
       if (g == 0 && c == 0) set_status(status, PIE_STATUS_NOALLOC_TRUNC);
+    }
+    const int cap = max(0, page_indptr[l + 1] - page_indptr[l]) * P;
+    if (ext > cap) {
+      ext = cap;
+      if (g == 0 && c == 0) set_status(status, PIE_STATUS_BOUNDS);
     }
     ext = max(ext, 0);
     const int kb = c * kNoAllocChunk;
@@ -90,7 +98,8 @@ using namespace pie;
 extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t num_lanes,
                                              int32_t max_kv_len, const int32_t* slots,
                                              const int32_t* kv_len, const int32_t* page_indptr,
-                                             const int32_t* page_ids, const void* q_rot,
+                                             const int32_t* page_ids, int32_t num_pool_pages,
+                                             const void* q_rot,
                                              const void* k_pool, const void* v_pool, void* out,
                                              float* lse, uint32_t* status, void* stream) {
   if (!desc) return nofail(PIE_EINVAL, "desc is NULL");
@@ -103,7 +112,8 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
     return nofail(PIE_EUNSUPPORTED, "head_dim 64/128, page_size 8/16/32, f32/bf16 only");
   const int G = D.num_q_heads / D.num_kv_heads;
   if (G > 8) return nofail(PIE_EUNSUPPORTED, "more than 8 q heads per kv head is not built");
-  if (num_lanes < 0 || max_kv_len < 0) return nofail(PIE_EINVAL, "negative size");
+  if (num_lanes < 0 || max_kv_len < 0 || num_pool_pages < 0)
+    return nofail(PIE_EINVAL, "negative size");
   if (num_lanes == 0) return PIE_OK;
   if (!slots || !kv_len || !page_indptr || !page_ids || !q_rot || !k_pool || !v_pool || !out)
     return nofail(PIE_EINVAL, "a required pointer is NULL");
@@ -144,6 +154,7 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
   p.dev.kv_len = kv_len;
   p.dev.page_indptr = page_indptr;
   p.dev.page_ids = page_ids;
+  p.dev.num_pool_pages = num_pool_pages;
   p.dev.dec_items = reinterpret_cast<const DecItem*>(sc + off_items);
   p.dev.comb = reinterpret_cast<const CombEntry*>(sc + off_comb);
   p.dev.readout = reinterpret_cast<const int32_t*>(sc + off_ro);
@@ -155,7 +166,8 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
   const int threads = 256;
   const int blocks = static_cast<int>((n_items + threads - 1) / threads);
   noalloc_items_kernel<<<blocks, threads, 0, s>>>(
-      L, Hkv, MC, nq, max_kv_len, slots, kv_len, reinterpret_cast<DecItem*>(sc + off_items),
+      L, Hkv, MC, nq, max_kv_len, D.page_size, slots, kv_len, page_indptr,
+      reinterpret_cast<DecItem*>(sc + off_items),
       reinterpret_cast<CombEntry*>(sc + off_comb), reinterpret_cast<int32_t*>(sc + off_ro), status);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_attend_decode(p, q_rot, k_pool, v_pool, nullptr, status, s);

@@ -144,12 +144,16 @@ __device__ __forceinline__ uint64_t global_ns() {
 // seconds (the caller then records PIE_STATUS_TIMEOUT and stops waiting).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
 
 // Programmatic dependent launch.  grid_dep_wait: wait until the grids this

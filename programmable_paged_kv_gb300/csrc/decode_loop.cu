@@ -157,7 +157,8 @@ extern "C" int pie_fwd_decode_loop_workspace_bytes(const pie_fwd_desc* desc, int
 
 extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, int32_t steps,
                                    const int32_t* page_indptr, const int32_t* page_ids,
-                                   int32_t max_pages_per_lane, int32_t* frozen_len,
+                                   int32_t num_pool_pages, int32_t max_pages_per_lane,
+                                   int32_t* frozen_len,
                                    const void* q, const void* k, const void* v, void* q_rot,
                                    void* k_pool, void* v_pool, void* out, float* lse,
                                    const int32_t* channel, void* workspace, size_t ws_bytes,
@@ -165,7 +166,7 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
   int G = 0, nq = 0, MC = 0;
   int rc = loop_check(desc, num_lanes, max_pages_per_lane, G, nq, MC);
   if (rc != PIE_OK) return rc;
-  if (steps < 0) return set_last_error(PIE_EINVAL, "negative steps");
+  if (steps < 0 || num_pool_pages < 0) return set_last_error(PIE_EINVAL, "negative size");
   if (num_lanes == 0 || steps == 0) return PIE_OK;
   if (!page_indptr || !page_ids || !frozen_len || !q || !k || !v || !q_rot || !k_pool ||
       !v_pool || !out)
@@ -211,6 +212,7 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
   m.part_o = reinterpret_cast<float*>(w + Y.part_o);
   m.page_indptr = page_indptr;
   m.page_ids = page_ids;
+  m.num_pool_pages = num_pool_pages;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int init_n = std::max(L * Hkv, std::max(L + 1, d / 2));

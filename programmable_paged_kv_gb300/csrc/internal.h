@@ -122,6 +122,10 @@ struct DevMeta {
   int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
   int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
   int32_t num_sms;                  // SMs the masked tensor-core chunks are sized for
+  int32_t num_pool_pages;           // page ids at or past it are skipped (PIE_STATUS_BOUNDS)
+  int32_t test_stall;               // test hook: 0 none; s + 1: the split-KV producer stops
+                                    //   before stage s of every item
+  uint32_t test_wait_us;            // test hook: 0, or the split-KV kernel's wait limit in us
 };
 
 // Pinned host staging block: metadata uploads copy from pinned memory so that
@@ -187,5 +191,9 @@ int set_last_error(int code, const std::string& msg);
 // The calling thread's timing events of pie_fwd_set_timing_events (both NULL
 // when the hook is off).
 void timing_events(cudaEvent_t* start, cudaEvent_t* stop);
+// The calling thread's wait-expiry test hook (pie_fwd_test_wait_expiry): the
+// stage before which the split-KV producer stops (0: none, else stage + 1) and
+// the wait limit in microseconds (0: the default).
+void test_wait_hook(int32_t* stall, uint32_t* wait_us);
 
 }  // namespace pie

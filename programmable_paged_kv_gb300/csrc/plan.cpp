@@ -502,6 +502,22 @@ void pie::timing_events(cudaEvent_t* start, cudaEvent_t* stop) {
   *stop = g_ev_stop;
 }
 
+static thread_local int32_t g_test_stall = 0;
+static thread_local uint32_t g_test_wait_us = 0;
+
+extern "C" int pie_fwd_test_wait_expiry(int32_t stage, uint32_t wait_us) {
+  if (stage < -1) return fail(PIE_EINVAL, "test_wait_expiry: stage must be -1 or >= 0");
+  if (stage >= 0 && wait_us == 0) return fail(PIE_EINVAL, "test_wait_expiry: give a wait limit");
+  g_test_stall = stage + 1;
+  g_test_wait_us = stage >= 0 ? wait_us : 0;
+  return PIE_OK;
+}
+
+void pie::test_wait_hook(int32_t* stall, uint32_t* wait_us) {
+  *stall = g_test_stall;
+  *wait_us = g_test_wait_us;
+}
+
 extern "C" {
 
 // One host plan per calling thread, reused so that its vectors keep their
@@ -623,6 +639,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.list_mode = reinterpret_cast<int32_t*>(w + Y.list_mode);
   dm.mask_tiles = reinterpret_cast<int32_t*>(w + Y.mask_tiles);
   dm.num_sms = H.sms;
+  dm.num_pool_pages = M.num_pool_pages;
   p->staging = blk;
   *out = p;
   return PIE_OK;

@@ -44,14 +44,21 @@ __global__ void __launch_bounds__(128) rope_scatter_kernel(
     s_sin[i] = sn;
   }
   const int frozen = frozen_len[lane];
-  const bool write_kv = slot >= frozen;
+  bool write_kv = slot >= frozen;
   if (threadIdx.x == 0) {
     if (!write_kv && slot >= 0) set_status(status, PIE_STATUS_FROZEN_WRITE);
     if (r == m.row_indptr[lane] && m.fold_mode[lane] != PIE_FOLD_NONE && slot != frozen)
       set_status(status, PIE_STATUS_FOLD_GAP);
   }
-  // (a row that writes nothing -- a frozen slot, or none at all -- reads no page)
-  const int64_t page = write_kv ? m.page_ids[m.page_indptr[lane] + slot / P] : 0;
+  // (a row that writes nothing -- a frozen slot, or none at all -- reads no
+  // page; a page id outside the pool, possible where device code supplies the
+  // page table, is not written and sets PIE_STATUS_BOUNDS)
+  int64_t page = write_kv ? m.page_ids[m.page_indptr[lane] + slot / P] : 0;
+  if (write_kv && (page < 0 || page >= m.num_pool_pages)) {
+    if (threadIdx.x == 0) set_status(status, PIE_STATUS_BOUNDS);
+    write_kv = false;
+    page = 0;
+  }
   const int64_t slot_off = page * Hkv * P + (slot % P);  // (page, head 0, slot) in rows of D
   __syncthreads();
 

@@ -21,7 +21,7 @@ def _lib():
     build()
 
 
-def _run_loop(sc, steps, frozen0=None, channel=None):
+def _run_loop(sc, steps, frozen0=None, channel=None, page_ids=None):
     import torch
     from programmable_paged_kv_gb300 import decode_loop, make_desc, runner
     d = sc.desc
@@ -32,7 +32,8 @@ def _run_loop(sc, steps, frozen0=None, channel=None):
     f0 = sc.frozen_len0 if frozen0 is None else frozen0
     frozen = torch.from_numpy(np.asarray(f0, np.int32)).cuda()
     page_indptr = torch.from_numpy(p0.page_indptr.astype(np.int32)).cuda()
-    page_ids = torch.from_numpy(p0.page_ids.astype(np.int32)).cuda()
+    page_ids = torch.from_numpy(
+        (p0.page_ids if page_ids is None else page_ids).astype(np.int32)).cuda()
     maxp = int(np.diff(p0.page_indptr).max())
     q = torch.stack([runner.to_device(sc.passes[t].q, d.dtype) for t in range(steps)])
     k = torch.stack([runner.to_device(sc.passes[t].k, d.dtype) for t in range(steps)])
@@ -127,3 +128,27 @@ def test_channel_fold_matches_the_pass_by_pass_oracle():
     assert gstatus == ostatus and (gstatus & 2)  # PIE_STATUS_FOLD_CLAMP
     assert_rope_close(gk, k_pool, sc.desc.dtype, "K pool")
     assert_bits_equal(gv, v_pool, "V pool")
+
+
+def test_out_of_pool_page_ids_are_skipped():
+    """The loop's page table is device data: a page id outside the pool is
+    neither written (RoPE/scatter) nor read (attention), PIE_STATUS_BOUNDS is
+    set, nothing outside the working sets is touched, and the other lanes get
+    the oracle's result."""
+    steps, bad = 3, 1
+    sc = W.decode_loop(8, lanes=4, steps=steps, c_lo=40, c_hi=300, num_pool_pages=256,
+                       desc=W.Desc(8, 2, 128, 16, W.BF16))
+    p0 = sc.passes[0]
+    ids = p0.page_ids.copy()
+    f = int(sc.frozen_len0[bad])
+    ids[p0.page_indptr[bad] + f // sc.desc.page_size] = 1 << 28   # the page of its next slot
+    ids[p0.page_indptr[bad]] = -5                                   # and its first page
+    gk, gv, gfrozen, gouts, glse, gstatus, untouched = _run_loop(sc, steps, page_ids=ids)
+    ok_, ov, ofrozen, ores = O.run_scenario(sc, num_threads=4)
+    assert gstatus & 4  # PIE_STATUS_BOUNDS
+    assert untouched
+    good = [l for l in range(p0.num_lanes) if l != bad]
+    assert np.array_equal(gfrozen, ofrozen)
+    for t in range(steps):
+        assert_out_close(gouts[t][good], ores[t]["out"][good], sc.desc.dtype, f"step {t} out")
+        assert_lse_close(glse[t][good], ores[t]["lse"][good], sc.desc.dtype, f"step {t} lse")

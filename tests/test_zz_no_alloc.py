@@ -17,7 +17,9 @@ parity tests use:
   * a call whose max_kv_len is below some lane's kv_len: the status bit is
     set and the output is attention over the first max_kv_len slots, as the
     oracle computes it;
-  * a call needing more scratch than the array holds is refused.
+  * a call needing more scratch than the array holds is refused;
+  * device page tables are checked: a kv_len past a lane's pages is cut, a
+    page id outside the pool is not read, and the status says so.
 This file is collected last so that a failure here never hides another
 test's result.
 """
@@ -79,7 +81,8 @@ def _noalloc(lib, desc, n, max_kv, slots_d, kv_d, pind_d, pids_d, q_rot, pools, 
              status):
     return lib.pie_fwd_decode_attend_noalloc(
         C.byref(desc), n, int(max_kv), slots_d.data_ptr(), kv_d.data_ptr(), pind_d.data_ptr(),
-        pids_d.data_ptr(), q_rot.data_ptr(), pools.k.data_ptr(), pools.v.data_ptr(),
+        pids_d.data_ptr(), int(pools.k.shape[0]), q_rot.data_ptr(), pools.k.data_ptr(),
+        pools.v.data_ptr(),
         out.data_ptr(), lse.data_ptr(), status.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
 
@@ -204,7 +207,39 @@ def test_no_alloc_refuses_scratch_overflow():
     one = torch.zeros(8, dtype=torch.int32, device="cuda")
     rc = lib.pie_fwd_decode_attend_noalloc(
         C.byref(desc), 256, 1 << 20, one.data_ptr(), one.data_ptr(), one.data_ptr(),
-        one.data_ptr(), one.data_ptr(), one.data_ptr(), one.data_ptr(), one.data_ptr(), None,
+        one.data_ptr(), 1, one.data_ptr(), one.data_ptr(), one.data_ptr(), one.data_ptr(), None,
         None, torch.cuda.current_stream().cuda_stream)
     assert rc == abi.PIE_ERANGE
     assert b"static scratch" in lib.pie_fwd_last_error()
+
+
+def test_no_alloc_checks_device_page_tables():
+    """The page table is device data: a lane whose kv_len runs past its pages
+    is cut to them, and a page id outside the pool is not read; both set
+    PIE_STATUS_BOUNDS, and every other lane still gets the planned path's
+    output."""
+    from programmable_paged_kv_gb300 import abi
+    lib = abi.load()
+    sc = W.decode_batch(13, lanes=10, c_lo=100, c_hi=900, num_pool_pages=2048)
+    p = sc.passes[0]
+    desc, pools, q_rot, tdt = _setup(sc)
+    ref, ref_lse = _planned(sc, desc, pools, q_rot, tdt, p.kv_len, p.slots)
+    L = p.num_lanes
+    kv_bad = p.kv_len.copy()
+    slots_bad = p.slots.copy()
+    cap = np.diff(p.page_indptr) * sc.desc.page_size
+    kv_bad[2] = cap[2] + 500         # past lane 2's pages
+    slots_bad[2] = cap[2] + 499
+    ids_bad = p.page_ids.copy()
+    ids_bad[p.page_indptr[5] + 1] = 1 << 30   # outside the pool
+    ids_bad[p.page_indptr[7]] = -3
+    out = torch.full_like(ref, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = _noalloc(lib, desc, L, int(kv_bad.max()), _dev32(slots_bad), _dev32(kv_bad),
+                  _dev32(p.page_indptr), _dev32(ids_bad), q_rot, pools, out, lse, status)
+    assert rc == abi.PIE_OK, lib.pie_fwd_last_error()
+    torch.cuda.synchronize()
+    assert int(status.item()) & 4  # PIE_STATUS_BOUNDS
+    good = [l for l in range(L) if l not in (2, 5, 7)]
+    _close(out[good], lse[good], ref[good], ref_lse[good])
