@@ -1020,86 +1020,80 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
     """Closed loop of the work-conserving batcher over the ForwardPass: every
     agent (command queue) submits its next decode call only when its previous
     one has completed (an inferlet awaiting its result); on each GPU-idle
-    instant one batch is dispatched as one multi-lane pass.  Returns (seconds,
-    calls, batches, attended tokens, host dispatch seconds)."""
+    instant one batch is dispatched as one multi-lane pass.  Each agent's
+    working set is registered with the batcher once, so a call crosses the
+    API boundary as (queue, key, rows, first slot) and a batch's pass is
+    built and planned by pie_batcher_plan_forward.  Returns (seconds, calls, batches, attended
+    tokens, host seconds by part: dispatch, pass and plan set-up, completion
+    and the next submissions)."""
     import torch
-    from programmable_paged_kv_gb300 import (Batcher, ForwardPlan, make_desc, make_meta, runner,
-                                             set_timing_events)
-    from programmable_paged_kv_gb300.batching import forward_batch_pass
+    from programmable_paged_kv_gb300 import Batcher, abi, make_desc, runner, set_timing_events
+    from programmable_paged_kv_gb300.abi import PieError
     d = trace.pool.desc
     desc = make_desc(d)
     P, Hq, Hkv, D = d.page_size, d.num_q_heads, d.num_kv_heads, d.head_dim
+    NP = trace.pool.num_pool_pages
     tdt = torch.bfloat16
     pools = runner.DevicePools(trace.pool)
     b = Batcher([True], max_calls, max_rows)
     Q = len(trace.queue_pages)
-    qids = [b.add_queue(0) for _ in range(Q)]
-    frozen = [int(c) for c in trace.cached]
-    cursor = list(frozen)
-    left = [steps] * Q
-    call_set, call_rows = {}, {}
-    rng = np.random.default_rng(5)
-    q_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hq, D), dtype=np.float32)).view(np.int16)).pin_memory()
-    kv_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hkv, D), dtype=np.float32)).view(np.int16)).pin_memory()
-
-    pages64 = [np.asarray(pg, np.int64) for pg in trace.queue_pages]
-    # pinned staging for each batch's gathered inputs, so their copies to the
-    # device are asynchronous
-    q_st = torch.empty_like(q_in).pin_memory()
-    kv_st = torch.empty_like(kv_in).pin_memory()
-    fr_st = torch.empty(Q, dtype=torch.int32).pin_memory()
-
-    def submit(q):
-        pages = pages64[q]
-        c = cursor[q]
-        cid = b.submit(qids[q], 0, 1, key=q, reads=pages[:c // P + 1], writes=pages[c // P:c // P + 1])
-        cursor[q] += 1
-        left[q] -= 1
-        call_set[cid], call_rows[cid] = q, 1
-    def submit_group(qs):
-        # the next calls of several agents in one native call
-        reads, writes = [], []
-        for q in qs:
-            c = cursor[q]
-            reads.append(pages64[q][:c // P + 1])
-            writes.append(pages64[q][c // P:c // P + 1])
-            cursor[q] += 1
-            left[q] -= 1
-        ids = b.submit_many([qids[q] for q in qs], [0] * len(qs), [1] * len(qs), qs,
-                            [()] * len(qs), reads, writes)
-        for cid, q in zip(ids, qs):
-            call_set[cid], call_rows[cid] = q, 1
-
+    qids = np.asarray([b.add_queue(0) for _ in range(Q)], np.int32)
     for q in range(Q):
-        submit(q)
+        b.set_pages(q, trace.queue_pages[q])  # working set q = agent q
+    frozen = np.asarray(trace.cached, np.int32).copy()
+    cursor = frozen.astype(np.int64)
+    left = np.full(Q, steps, np.int64)
+    rng = np.random.default_rng(5)
+    # the batch's new rows' q, k, v on the device in pass row order, as a
+    # model's projections of the batch would leave them
+    q_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hq, D), dtype=np.float32)).view(np.int16)).cuda().view(tdt)
+    kv_in = torch.from_numpy(W.f32_to_bf16_bits(rng.standard_normal((Q, Hkv, D), dtype=np.float32)).view(np.int16)).cuda().view(tdt)
+    # pinned staging for each batch's frozen lengths (one asynchronous copy),
+    # device buffers for the largest batch, one workspace grown when the
+    # planner refuses it
+    fr_st = torch.empty(max_calls, dtype=torch.int32).pin_memory()
+    fr_np = fr_st.numpy()
+    out_h = torch.empty((max_calls, Hq, D), dtype=tdt).pin_memory()
+    q_rot_d = torch.empty((max_calls, Hq, D), dtype=tdt, device="cuda")
+    out_d = torch.empty((max_calls, Hq, D), dtype=tdt, device="cuda")
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+    ones = np.ones(Q, np.int64)
+
+    def submit(qs):
+        b.submit_forward(qids[qs], qs, ones[:len(qs)], cursor[qs], P)
+        cursor[qs] += 1
+        left[qs] -= 1
+
+    submit(np.arange(Q))
     ev = [] if kernel_ms is not None else None
     calls = batches = tokens = 0
-    host = 0.0    # native dispatch calls
-    marshal = 0.0  # completion events and the next calls' submission
+    host = np.zeros(3)  # dispatch, pass and plan set-up, completion and submission
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     while True:
         h0 = time.perf_counter()
-        r = b.dispatch()
-        host += time.perf_counter() - h0
+        r = b.dispatch(arrays=True)
+        h1 = time.perf_counter()
+        host[0] += h1 - h0
         if r is None:
             break
         _, ids, lanes = r
-        p, lane_set, first = forward_batch_pass(ids, lanes, call_set, call_rows, trace.queue_pages,
-                                                frozen)
-        N = int(p.row_indptr[-1])
-        sel = torch.tensor(lane_set, dtype=torch.long)
-        L = len(lane_set)
-        torch.index_select(q_in, 0, sel, out=q_st[:L])
-        torch.index_select(kv_in, 0, sel, out=kv_st[:L])
-        qd = q_st[:L].cuda(non_blocking=True).view(tdt)
-        kd = kv_st[:L].cuda(non_blocking=True).view(tdt)
-        plan = ForwardPlan(desc, make_meta(p, trace.pool.num_pool_pages))
-        fr_st[:L] = torch.tensor([frozen[w] for w in lane_set], dtype=torch.int32)
+        while True:  # the pass built and planned natively; a refused workspace grows
+            try:
+                plan, lane_keys, first, kv_len, N = b.plan_forward(ids, lanes, frozen, desc, NP, ws)
+                break
+            except PieError as e:
+                if e.code != abi.PIE_ENOSPACE:
+                    raise
+                ws = torch.empty(2 * ws.numel(), dtype=torch.uint8, device="cuda")
+        L = len(lane_keys)
+        fr_np[:L] = frozen[lane_keys]
         fr = fr_st[:L].cuda(non_blocking=True)
-        q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+        qd, kd = q_in[:N], kv_in[:N]
+        host[1] += time.perf_counter() - h1
+        q_rot = q_rot_d[:N]
         plan.append_kv(qd, kd, kd, q_rot, pools.k, pools.v, fr)
-        out = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
+        out = out_d[:N]
         if ev is not None:
             e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             set_timing_events(*e)
@@ -1108,26 +1102,24 @@ def batcher_closed_loop(trace, steps, max_calls, max_rows, kernel_ms=None):
         if ev is not None:
             set_timing_events()
         plan.fold(fr)
-        out_h = out.cpu()  # the agents' results (a completion event each)
+        out_h[:N].copy_(out)  # the agents' results (a completion event each)
         plan.close()
-        for w, n in zip(lane_set, np.diff(p.row_indptr)):
-            frozen[w] += int(n)
-        tokens += int(p.kv_len.sum())
+        h2 = time.perf_counter()
+        frozen[lane_keys] = kv_len  # every new row folded
+        tokens += int(kv_len.sum())
         calls += len(ids)
         batches += 1
-        h0 = time.perf_counter()
         b.complete(ids)
-        again = [call_set[c] for c in ids if left[call_set[c]] > 0]
-        if again:
-            submit_group(again)
-        marshal += time.perf_counter() - h0
+        again = lane_keys[left[lane_keys] > 0]  # one call per agent in flight: lane = agent
+        if again.size:
+            submit(again)
+        host[2] += time.perf_counter() - h2
     torch.cuda.synchronize()
     secs = time.perf_counter() - t0
     if ev is not None:
         kernel_ms.extend(a.elapsed_time(c) for a, c in ev)
-    del out_h
     b.close()
-    return secs, calls, batches, tokens, host, marshal
+    return secs, calls, batches, tokens, host
 
 
 def run_batcher(args, local):
@@ -1150,8 +1142,8 @@ def run_batcher(args, local):
     clocks.start()
     time.sleep(0.3)
     kms = []
-    secs, calls, batches, tokens, host, marshal = batcher_closed_loop(trace, steps, 64, 4096, kms)
-    s1, c1, b1, t1, h1, m1 = batcher_closed_loop(trace, steps, 1, 4096)
+    secs, calls, batches, tokens, host = batcher_closed_loop(trace, steps, 64, 4096, kms)
+    s1, c1, b1, t1, h1 = batcher_closed_loop(trace, steps, 1, 4096)
     clk = clocks.stop()
     # the oracle batcher on the same closed loop's decisions (dispatch + complete)
     ob = OB.Batcher({q: 0 for q in range(64)}, {0: True}, 64, 4096)
@@ -1184,12 +1176,18 @@ def run_batcher(args, local):
             "speedup_vs_one_call_per_pass": (calls / secs) / (c1 / s1),
             "batches": batches, "mean_batch_calls": calls / batches,
             "attended_tokens_per_s": tokens / secs,
-            "dispatch_us_per_batch_native": host / batches * 1e6,
-            "complete_and_submit_us_per_batch": marshal / batches * 1e6,
+            "host_us_per_batch": {"dispatch": host[0] / batches * 1e6,
+                                  "pass_and_plan": host[1] / batches * 1e6,
+                                  "complete_and_submit": host[2] / batches * 1e6,
+                                  "total": host.sum() / batches * 1e6},
             "attention_kernel_ms_per_batch": sum(kms) / len(kms) if kms else None,
             "e2e": {"value": calls / secs, "unit": "calls/s",
-                    "h2d_bytes_per_step": 64 * (32 + 8) * 128 * 2,
-                    "d2h_bytes_per_step": 64 * 32 * 128 * 2},
+                    "h2d_bytes_per_step": 64 * 4,
+                    "d2h_bytes_per_step": 64 * 32 * 128 * 2,
+                    "inputs": "the batch's q/k/v on the device in pass row order (a model's "
+                              "projections of the batch); a batch copies its frozen lengths "
+                              "in and the pass's metadata through the planner, and its "
+                              "outputs out"},
             "gpu_launches": batches * 5,
             "roofline": {"bound": "hbm", "achieved": kbytes / kern / 1e9 if kern else None,
                          "peak": hbm, "unit": "GB/s",
@@ -1203,7 +1201,7 @@ def run_batcher(args, local):
                              "cores": 1, "kind": "oracle",
                              "sample": f"the oracle batcher on the same closed loop ({batches} "
                                        f"dispatches); the native one took "
-                                       f"{host / batches * 1e6:.1f} us per dispatch"}}
+                                       f"{host[0] / batches * 1e6:.1f} us per dispatch"}}
     if clk:
         line["clocks"] = clk
     print(json.dumps(line))

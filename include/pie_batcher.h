@@ -36,6 +36,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pie_fwd.h"
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -95,6 +97,74 @@ int pie_batcher_dispatch(pie_batcher_t* b, int64_t* calls, int32_t* lanes, int32
  * that depend on them become eligible.  Errors: PIE_EINVAL if a call is not in
  * flight (unknown, still queued or already completed); nothing is changed. */
 int pie_batcher_complete(pie_batcher_t* b, const int64_t* calls, int32_t n);
+
+/* ---- forward calls on registered working sets ------------------------------
+ * A working set (a lane's KV state, Pie "The forward pass": State geometry) is
+ * a list of pool pages in slot order: slot s lies in page pages[s / page_size].
+ * The batcher keeps these lists so that the control loop hands it no per-page
+ * data per call: a forward call's read set is the pages holding every slot up
+ * to its last row's, its write set the pages holding its new slots (the sets
+ * Eq. (4) compares), and a dispatched batch of forward calls becomes the
+ * geometry of one pass without a host-side copy loop. */
+
+/* Registers (or replaces) the page list of working set `key` (0 <= key <
+ * 2^26; page ids in [0, 2^26)).  The list is copied.  Calls already queued
+ * keep the read/write sets they were given.  Errors: PIE_EINVAL (NULL batcher,
+ * negative count, NULL pages with a positive count), PIE_ERANGE (key or a page
+ * id outside [0, 2^26)). */
+int pie_batcher_set_pages(pie_batcher_t* b, int64_t key, const int32_t* pages, int32_t num_pages);
+
+/* Enqueue n forward calls of handler type `handler`, as n calls of
+ * pie_batcher_submit without dependencies: call i (ids *first_id + i) goes to
+ * queues[i], names working set keys[i] (registered) and writes rows[i] >= 1
+ * rows at slots [first_slot[i], first_slot[i] + rows[i]); it reads the pages
+ * of slots [0, first_slot[i] + rows[i]) and writes the pages of its new slots.
+ * Every call is checked before any is enqueued.  Errors: as
+ * pie_batcher_submit; PIE_EINVAL for NULL arrays, page_size < 1 or a key with
+ * no registered pages; PIE_ERANGE for slots past the working set's pages. */
+int pie_batcher_submit_forward(pie_batcher_t* b, int32_t n, const int32_t* queues, int32_t handler,
+                               const int64_t* keys, const int64_t* rows, const int64_t* first_slot,
+                               int32_t page_size, int64_t* first_id);
+
+/* The pass of a dispatched batch of forward calls (calls[0..n), lanes[0..n) as
+ * pie_batcher_dispatch returned them), in pie_fwd_meta's layout: lane l holds
+ * the calls numbered l, all on one working set k = lane_keys[l] (a working set
+ * appears in one lane); its rows are its calls' rows concatenated in batch
+ * order at slots frozen[k], frozen[k] + 1, ... (position = slot, so the
+ * output arrays `positions` serve as slots too), kv_len[l] = frozen[k] + rows,
+ * and its pages are the working set's registered pages.  first_row[i] is call
+ * i's first row in the pass.  frozen[0..num_keys) is the caller's frozen length
+ * per key.  Every pass folds all of its rows (PIE_FOLD_ALL).  Outputs:
+ * row_indptr [L+1], positions [N], kv_len [L], page_indptr [L+1], page_ids
+ * [pages], lane_keys [L] with L <= max_lanes, N <= max_rows, pages <=
+ * max_pages; *num_lanes, *num_rows and *num_pages are set even when the
+ * capacities are too small (then PIE_ENOSPACE and nothing else is written).
+ * Errors: PIE_EINVAL (NULL arguments, an unknown call, a lane outside [0, n)
+ * or holding no call, a lane spanning two working sets, a working set in two
+ * lanes, a key with no registered pages or >= num_keys), PIE_ERANGE (negative
+ * frozen length, a pass over 2^31 rows or pages), PIE_ENOSPACE.  No CUDA call;
+ * the batcher is not changed. */
+int pie_batcher_forward_pass(const pie_batcher_t* b, const int64_t* calls, const int32_t* lanes,
+                             int32_t n, const int32_t* frozen, int64_t num_keys, int32_t max_lanes,
+                             int64_t max_rows, int64_t max_pages, int32_t* row_indptr,
+                             int32_t* positions, int32_t* kv_len, int32_t* page_indptr,
+                             int32_t* page_ids, int64_t* lane_keys, int32_t* first_row,
+                             int32_t* num_lanes, int32_t* num_rows, int64_t* num_pages);
+
+/* pie_batcher_forward_pass and pie_fwd_plan (pie_fwd.h) in one call: the pass
+ * of a dispatched forward batch is built in the batcher's own buffers and
+ * planned against `desc`, `num_pool_pages`, the workspace and the stream as
+ * pie_fwd_plan does (no fold count, mask or readout list: the default readout
+ * of the last row of every lane).  Outputs: *plan, lane_keys [n] (the working
+ * set of each lane), first_row [n], kv_len [n] (may be NULL), *num_lanes,
+ * *num_rows.  Errors: those of both calls, PIE_EINVAL for n < 1; *plan is NULL
+ * on error. */
+int pie_batcher_plan_forward(pie_batcher_t* b, const int64_t* calls, const int32_t* lanes, int32_t n,
+                             const int32_t* frozen, int64_t num_keys, const pie_fwd_desc* desc,
+                             int32_t num_pool_pages, void* dev_workspace, size_t ws_bytes,
+                             void* stream, pie_fwd_plan_t** plan, int64_t* lane_keys,
+                             int32_t* first_row, int32_t* kv_len, int32_t* num_lanes,
+                             int32_t* num_rows);
 
 /* Calls waiting in queues and calls in flight. */
 int pie_batcher_counts(const pie_batcher_t* b, int64_t* queued, int64_t* in_flight);

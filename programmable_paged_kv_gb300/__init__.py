@@ -10,6 +10,7 @@ if the library is missing every call raises.
 from __future__ import annotations
 
 import ctypes as C
+import types
 from typing import Optional
 
 import numpy as np
@@ -193,6 +194,19 @@ class ForwardPlan:
         self.handle = h
         self.num_readout = int(self.lib.pie_fwd_plan_num_readout(h))
 
+    @classmethod
+    def _adopt(cls, handle, desc: abi.pie_fwd_desc, workspace):
+        """A ForwardPlan around a plan handle made elsewhere in the library
+        (pie_batcher_plan_forward); it owns the handle from now on."""
+        self = cls.__new__(cls)
+        self.lib = abi.load()
+        self.desc = desc
+        self.meta = None
+        self.workspace = workspace
+        self.handle = handle
+        self.num_readout = int(self.lib.pie_fwd_plan_num_readout(handle))
+        return self
+
     def append_kv(self, q, k, v, q_rot, k_pool, v_pool, frozen_len, status=None, stream=None):
         abi.check(self.lib.pie_fwd_append_kv(
             self.handle, _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(q_rot, "q_rot"),
@@ -356,15 +370,106 @@ class Batcher:
             wv.ctypes.data, C.byref(first)), "pie_batcher_submit_many")
         return range(first.value, first.value + n)
 
-    def dispatch(self):
-        """(handler, call ids, lanes) of the next batch, or None."""
+    def dispatch(self, arrays: bool = False):
+        """(handler, call ids, lanes) of the next batch, or None; with
+        arrays=True the ids and lanes are numpy arrays (copies)."""
         n, h = C.c_int32(), C.c_int32()
         abi.check(self.lib.pie_batcher_dispatch(self.handle, self._calls, self._lanes,
                                                 self.max_calls, C.byref(n), C.byref(h)),
                   "pie_batcher_dispatch")
         if n.value == 0:
             return None
+        if arrays:
+            return (h.value, np.ctypeslib.as_array(self._calls)[:n.value].copy(),
+                    np.ctypeslib.as_array(self._lanes)[:n.value].copy())
         return h.value, list(self._calls[:n.value]), list(self._lanes[:n.value])
+
+    def set_pages(self, key: int, pages) -> None:
+        """pie_batcher_set_pages: working set `key`'s pool pages in slot order."""
+        pages = np.ascontiguousarray(pages, dtype=np.int32).reshape(-1)
+        abi.check(self.lib.pie_batcher_set_pages(self.handle, key, pages.ctypes.data, pages.size),
+                  "pie_batcher_set_pages")
+
+    def submit_forward(self, queues, keys, rows, first_slots, page_size: int,
+                       handler: int = 0) -> range:
+        """pie_batcher_submit_forward: forward calls on registered working
+        sets, their read/write page sets derived natively; returns their ids."""
+        q = np.ascontiguousarray(queues, dtype=np.int32).reshape(-1)
+        k, r, f = (np.ascontiguousarray(x, dtype=np.int64).reshape(-1)
+                   for x in (keys, rows, first_slots))
+        first = C.c_int64()
+        abi.check(self.lib.pie_batcher_submit_forward(
+            self.handle, q.size, q.ctypes.data, handler, k.ctypes.data, r.ctypes.data,
+            f.ctypes.data, page_size, C.byref(first)), "pie_batcher_submit_forward")
+        return range(first.value, first.value + q.size)
+
+    def plan_forward(self, ids, lanes, frozen, desc: abi.pie_fwd_desc, num_pool_pages: int,
+                     workspace, stream=None):
+        """pie_batcher_plan_forward: the pass of a dispatched forward batch,
+        built and planned in one native call.  Returns (ForwardPlan, the working
+        set of each lane, each call's first row, each lane's kv_len, rows).
+        A workspace the planner refuses raises PieError(PIE_ENOSPACE)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+        lanes = np.ascontiguousarray(lanes, dtype=np.int32).reshape(-1)
+        frozen = np.ascontiguousarray(frozen, dtype=np.int32).reshape(-1)
+        n = ids.size
+        bufs = getattr(self, "_pf", None)
+        if bufs is None or bufs[0].size < n:
+            bufs = self._pf = (np.zeros(max(n, 1), np.int64), np.zeros(max(n, 1), np.int32),
+                               np.zeros(max(n, 1), np.int32))
+        keys, first, kv = bufs
+        h, nl, nr = C.c_void_p(), C.c_int32(), C.c_int32()
+        abi.check(self.lib.pie_batcher_plan_forward(
+            self.handle, ids.ctypes.data, lanes.ctypes.data, n, frozen.ctypes.data, frozen.size,
+            C.byref(desc), num_pool_pages, _ptr(workspace, "workspace"), workspace.numel(),
+            _stream(stream), C.byref(h), keys.ctypes.data, first.ctypes.data, kv.ctypes.data,
+            C.byref(nl), C.byref(nr)), "pie_batcher_plan_forward")
+        L = nl.value
+        return (ForwardPlan._adopt(h, desc, workspace), keys[:L], first[:n], kv[:L], nr.value)
+
+    def forward_pass(self, ids, lanes, frozen):
+        """pie_batcher_forward_pass: the pass fields (as make_meta takes them)
+        of a dispatched forward batch, the working set of each lane and each
+        call's first row.  frozen: int32 array of frozen lengths by key.  The
+        returned arrays are views of buffers reused by the next call."""
+        ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+        lanes = np.ascontiguousarray(lanes, dtype=np.int32).reshape(-1)
+        frozen = np.ascontiguousarray(frozen, dtype=np.int32).reshape(-1)
+        n = ids.size
+        nl, nr, npg = C.c_int32(), C.c_int32(), C.c_int64()
+        for _ in range(2):
+            bufs = getattr(self, "_fp", None)
+            if bufs is None:
+                bufs = self._fp = dict(L=0, N=0, P=0)
+            if bufs["L"] >= max(n, 1) and bufs["N"] >= max(nr.value, 1) and \
+                    bufs["P"] >= max(npg.value, 1):
+                pass
+            else:
+                L, N, P = max(n, 1, bufs["L"]), max(nr.value, 1, bufs["N"]), max(npg.value, 1, bufs["P"])
+                bufs.update(L=L, N=N, P=P, row_indptr=np.zeros(L + 1, np.int32),
+                            positions=np.zeros(N, np.int32), kv_len=np.zeros(L, np.int32),
+                            page_indptr=np.zeros(L + 1, np.int32), page_ids=np.zeros(P, np.int32),
+                            lane_keys=np.zeros(L, np.int64), first_row=np.zeros(L, np.int32),
+                            fold_mode=np.full(L, abi.PIE_FOLD_ALL, np.int32),
+                            fold_count=np.zeros(L, np.int32))
+            rc = self.lib.pie_batcher_forward_pass(
+                self.handle, ids.ctypes.data, lanes.ctypes.data, n, frozen.ctypes.data,
+                frozen.size, bufs["L"], bufs["N"], bufs["P"], bufs["row_indptr"].ctypes.data,
+                bufs["positions"].ctypes.data, bufs["kv_len"].ctypes.data,
+                bufs["page_indptr"].ctypes.data, bufs["page_ids"].ctypes.data,
+                bufs["lane_keys"].ctypes.data, bufs["first_row"].ctypes.data, C.byref(nl),
+                C.byref(nr), C.byref(npg))
+            if rc != abi.PIE_ENOSPACE:
+                break
+        abi.check(rc, "pie_batcher_forward_pass")
+        L, N, P = nl.value, nr.value, int(npg.value)
+        pos = bufs["positions"][:N]
+        p = types.SimpleNamespace(
+            row_indptr=bufs["row_indptr"][:L + 1], positions=pos, slots=pos,
+            kv_len=bufs["kv_len"][:L], page_indptr=bufs["page_indptr"][:L + 1],
+            page_ids=bufs["page_ids"][:P], fold_mode=bufs["fold_mode"][:L],
+            fold_count=bufs["fold_count"][:L], mask_word_indptr=None, readout=None)
+        return p, bufs["lane_keys"][:L], bufs["first_row"][:n]
 
     def complete(self, ids):
         ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)

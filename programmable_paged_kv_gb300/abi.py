@@ -107,6 +107,16 @@ SIGNATURES = {
                                        C.POINTER(C.c_int32)]),
     "pie_batcher_complete": (C.c_int, [_P, _P, C.c_int32]),
     "pie_batcher_counts": (C.c_int, [_P, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "pie_batcher_set_pages": (C.c_int, [_P, C.c_int64, _P, C.c_int32]),
+    "pie_batcher_submit_forward": (C.c_int, [_P, C.c_int32, _P, C.c_int32, _P, _P, _P, C.c_int32,
+                                             C.POINTER(C.c_int64)]),
+    "pie_batcher_plan_forward": (C.c_int, [_P, _P, _P, C.c_int32, _P, C.c_int64, _P, C.c_int32,
+                                           _P, C.c_size_t, _P, C.POINTER(C.c_void_p), _P, _P, _P,
+                                           C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+    "pie_batcher_forward_pass": (C.c_int, [_P, _P, _P, C.c_int32, _P, C.c_int64, C.c_int32,
+                                           C.c_int64, C.c_int64, _P, _P, _P, _P, _P, _P, _P,
+                                           C.POINTER(C.c_int32), C.POINTER(C.c_int32),
+                                           C.POINTER(C.c_int64)]),
 }
 
 

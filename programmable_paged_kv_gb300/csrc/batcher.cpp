@@ -3,7 +3,8 @@
 // call, is stated in include/pie_batcher.h; this file holds the bookkeeping.
 //
 // Per call: queue, handler type, rows, working-set key, state (queued, in
-// flight, done), dependencies and sorted, de-duplicated read/write sets.  Per
+// flight, done), dependencies and read/write sets as given (the Eq. (4) test
+// marks and checks one stamp per resource, so neither order nor repeats matter).  Per
 // queue: its priority and its queued calls in arrival order.  A dispatch walks
 // the queues that hold calls (a list kept in insertion order, compacted as
 // queues empty), builds each ready queue's group, buckets the groups by
@@ -13,6 +14,13 @@
 // Resource ids are small non-negative integers (KV page ids), so the taken
 // sets are two arrays indexed by resource id holding the stamp of the last
 // candidate that marked the resource: marking and testing cost one access.
+//
+// Forward calls on registered working sets: the batcher holds each working
+// set's pages in slot order, derives a forward call's read set (the pages of
+// every slot up to its last row's) and write set (the pages of its new
+// slots) from them, and turns a dispatched batch into the pass's geometry
+// (the folding geometry of "The forward pass", State geometry), so that no
+// per-page list crosses the API boundary on the control loop's path.
 
 #include <algorithm>
 #include <cstring>
@@ -32,7 +40,7 @@ enum State : uint8_t { kQueued = 0, kInFlight = 1, kDone = 2 };
 struct CallRec {
   int32_t queue, handler;
   int64_t rows, key;
-  std::vector<int64_t> deps, reads, writes;  // reads/writes sorted, unique
+  std::vector<int64_t> deps, reads, writes;
 };
 
 struct Queue {
@@ -61,6 +69,12 @@ struct pie_batcher {
   int64_t queued = 0, in_flight = 0;
   std::vector<uint32_t> rstamp, wstamp;  // per resource: stamp of the candidate that read / wrote it
   uint32_t stamp = 0;
+  std::vector<std::vector<int32_t>> ws_pages;  // per working-set key: its pages in slot order
+  std::vector<uint8_t> ws_known;               // per key: pages registered
+  std::vector<int64_t> scratch;                // per-call read/write lists being built
+  // the last planned pass's geometry (pie_batcher_plan_forward), kept until
+  // the next one: row_indptr, positions, kv_len, page_indptr, page_ids, fold_mode
+  std::vector<int32_t> pass_i32[6];
 
   // a new candidate: a fresh stamp (arrays cleared when the counter wraps)
   uint32_t next_stamp() {
@@ -179,10 +193,6 @@ void add_call(pie_batcher_t* b, int64_t top, int32_t queue, int32_t handler, int
   c.deps.assign(deps, deps + num_deps);
   c.reads.assign(reads, reads + num_reads);
   c.writes.assign(writes, writes + num_writes);
-  for (auto* v : {&c.reads, &c.writes}) {
-    std::sort(v->begin(), v->end());
-    v->erase(std::unique(v->begin(), v->end()), v->end());
-  }
   b->calls.push_back(std::move(c));
   b->state.push_back(kQueued);
   Queue& Q = b->queues[size_t(queue)];
@@ -380,6 +390,179 @@ int pie_batcher_complete(pie_batcher_t* b, const int64_t* calls, int32_t n) {
     }
   }
   return PIE_OK;
+}
+
+int pie_batcher_set_pages(pie_batcher_t* b, int64_t key, const int32_t* pages, int32_t num_pages) {
+  if (!b || num_pages < 0 || (num_pages > 0 && !pages))
+    return set_last_error(PIE_EINVAL, "NULL batcher, negative count or NULL pages");
+  if (key < 0 || key >= kMaxResource) return set_last_error(PIE_ERANGE, "key outside [0, 2^26)");
+  for (int32_t i = 0; i < num_pages; ++i)
+    if (pages[i] < 0 || pages[i] >= kMaxResource)
+      return set_last_error(PIE_ERANGE, "page id outside [0, 2^26)");
+  if (size_t(key) >= b->ws_pages.size()) {
+    b->ws_pages.resize(size_t(key) + 1);
+    b->ws_known.resize(size_t(key) + 1, 0);
+  }
+  b->ws_pages[size_t(key)].assign(pages, pages + num_pages);
+  b->ws_known[size_t(key)] = 1;
+  return PIE_OK;
+}
+
+int pie_batcher_submit_forward(pie_batcher_t* b, int32_t n, const int32_t* queues, int32_t handler,
+                               const int64_t* keys, const int64_t* rows, const int64_t* first_slot,
+                               int32_t page_size, int64_t* first_id) {
+  if (!b || !first_id || n < 0) return set_last_error(PIE_EINVAL, "NULL argument or n < 0");
+  const int64_t id0 = int64_t(b->calls.size());
+  *first_id = id0;
+  if (n == 0) return PIE_OK;
+  if (!queues || !keys || !rows || !first_slot) return set_last_error(PIE_EINVAL, "NULL per-call array");
+  if (page_size < 1) return set_last_error(PIE_EINVAL, "page_size < 1");
+  // every call checked before any is recorded
+  for (int32_t i = 0; i < n; ++i) {
+    int64_t top = -1;
+    const int rc = check_call(b, id0 + i, queues[i], handler, rows[i], nullptr, 0, nullptr, 0,
+                              nullptr, 0, &top);
+    if (rc != PIE_OK) return rc;
+    const int64_t k = keys[i];
+    if (k < 0 || size_t(k) >= b->ws_known.size() || !b->ws_known[size_t(k)])
+      return set_last_error(PIE_EINVAL, "a call names a working set with no registered pages");
+    const int64_t end = first_slot[i] + rows[i];  // one past the call's last slot
+    if (first_slot[i] < 0 || end > int64_t(b->ws_pages[size_t(k)].size()) * page_size)
+      return set_last_error(PIE_ERANGE, "a call's slots lie outside its working set's pages");
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const std::vector<int32_t>& pg = b->ws_pages[size_t(keys[i])];
+    const int64_t last = (first_slot[i] + rows[i] - 1) / page_size;  // page of the last new slot
+    const int64_t w0 = first_slot[i] / page_size;
+    // reads: the pages of slots [0, last slot]; writes: those of the new slots
+    std::vector<int64_t>& r = b->scratch;
+    r.assign(pg.begin(), pg.begin() + (last + 1));
+    int64_t top = -1;
+    for (int64_t x : r) top = std::max(top, x);
+    add_call(b, top, queues[i], handler, rows[i], keys[i], nullptr, 0, r.data(), int64_t(r.size()),
+             r.data() + w0, last + 1 - w0);
+  }
+  return PIE_OK;
+}
+
+int pie_batcher_forward_pass(const pie_batcher_t* b, const int64_t* calls, const int32_t* lanes,
+                             int32_t n, const int32_t* frozen, int64_t num_keys, int32_t max_lanes,
+                             int64_t max_rows, int64_t max_pages, int32_t* row_indptr,
+                             int32_t* positions, int32_t* kv_len, int32_t* page_indptr,
+                             int32_t* page_ids, int64_t* lane_keys, int32_t* first_row,
+                             int32_t* num_lanes, int32_t* num_rows, int64_t* num_pages) {
+  if (!b || n < 0 || (n > 0 && (!calls || !lanes || !frozen || !first_row)) || !num_lanes ||
+      !num_rows || !num_pages)
+    return set_last_error(PIE_EINVAL, "NULL argument or n < 0");
+  int32_t L = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (calls[i] < 0 || size_t(calls[i]) >= b->calls.size())
+      return set_last_error(PIE_EINVAL, "unknown call id");
+    if (lanes[i] < 0 || lanes[i] >= n) return set_last_error(PIE_EINVAL, "lane outside [0, n)");
+    L = std::max(L, lanes[i] + 1);
+  }
+  // each lane's working set and rows; a working set in one lane only
+  std::vector<int64_t> key(size_t(L), -1), lrows(size_t(L), 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const CallRec& c = b->calls[size_t(calls[i])];
+    const int32_t l = lanes[i];
+    if (c.key < 0 || size_t(c.key) >= b->ws_known.size() || !b->ws_known[size_t(c.key)] ||
+        c.key >= num_keys)
+      return set_last_error(PIE_EINVAL, "a call's working set has no registered pages or frozen length");
+    if (key[size_t(l)] >= 0 && key[size_t(l)] != c.key)
+      return set_last_error(PIE_EINVAL, "a lane of the batch spans two working sets");
+    key[size_t(l)] = c.key;
+    lrows[size_t(l)] += c.rows;
+  }
+  int64_t N = 0, NP = 0;
+  for (int32_t l = 0; l < L; ++l) {
+    if (key[size_t(l)] < 0) return set_last_error(PIE_EINVAL, "a lane number holds no call");
+    N += lrows[size_t(l)];
+    NP += int64_t(b->ws_pages[size_t(key[size_t(l)])].size());
+  }
+  {
+    std::vector<int64_t> sorted(key);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+      return set_last_error(PIE_EINVAL, "a working set appears in two lanes of one batch");
+  }
+  *num_lanes = L;
+  *num_rows = int32_t(std::min<int64_t>(N, INT32_MAX));
+  *num_pages = NP;
+  if (L > max_lanes || N > max_rows || NP > max_pages)
+    return set_last_error(PIE_ENOSPACE, "the pass needs more lanes, rows or pages than given");
+  if (N >= INT32_MAX || NP >= INT32_MAX) return set_last_error(PIE_ERANGE, "pass too large");
+  if (!row_indptr || !positions || !kv_len || !page_indptr || !page_ids || !lane_keys)
+    return set_last_error(PIE_EINVAL, "NULL output array");
+  // lanes: rows at the working set's next free slots (position = slot), all
+  // of the working set's pages, kv_len = frozen + rows
+  row_indptr[0] = 0;
+  page_indptr[0] = 0;
+  for (int32_t l = 0; l < L; ++l) {
+    const int64_t k = key[size_t(l)];
+    const int32_t f = frozen[k];
+    if (f < 0) return set_last_error(PIE_ERANGE, "negative frozen length");
+    const std::vector<int32_t>& pg = b->ws_pages[size_t(k)];
+    const int32_t r0 = row_indptr[l];
+    row_indptr[l + 1] = r0 + int32_t(lrows[size_t(l)]);
+    for (int32_t r = 0; r < int32_t(lrows[size_t(l)]); ++r) positions[r0 + r] = f + r;
+    kv_len[l] = f + int32_t(lrows[size_t(l)]);
+    std::memcpy(page_ids + page_indptr[l], pg.data(), pg.size() * sizeof(int32_t));
+    page_indptr[l + 1] = page_indptr[l] + int32_t(pg.size());
+    lane_keys[l] = k;
+  }
+  // each call's first row: its lane's rows in batch order
+  std::vector<int32_t> cursor(row_indptr, row_indptr + L);
+  for (int32_t i = 0; i < n; ++i) {
+    first_row[i] = cursor[size_t(lanes[i])];
+    cursor[size_t(lanes[i])] += int32_t(b->calls[size_t(calls[i])].rows);
+  }
+  return PIE_OK;
+}
+
+int pie_batcher_plan_forward(pie_batcher_t* b, const int64_t* calls, const int32_t* lanes, int32_t n,
+                             const int32_t* frozen, int64_t num_keys, const pie_fwd_desc* desc,
+                             int32_t num_pool_pages, void* dev_workspace, size_t ws_bytes,
+                             void* stream, pie_fwd_plan_t** plan, int64_t* lane_keys,
+                             int32_t* first_row, int32_t* kv_len, int32_t* num_lanes,
+                             int32_t* num_rows) {
+  if (!b || !plan || !lane_keys || !num_lanes || !num_rows || n < 1)
+    return set_last_error(PIE_EINVAL, "NULL argument or an empty batch");
+  *plan = nullptr;
+  // sizes first (the capacity check of pie_batcher_forward_pass reports them)
+  int32_t L = 0, N = 0;
+  int64_t NP = 0;
+  int rc = pie_batcher_forward_pass(b, calls, lanes, n, frozen, num_keys, 0, 0, 0, nullptr,
+                                    nullptr, nullptr, nullptr, nullptr, nullptr, first_row, &L, &N,
+                                    &NP);
+  *num_lanes = L;
+  *num_rows = N;
+  if (rc != PIE_OK && rc != PIE_ENOSPACE) return rc;
+  std::vector<int32_t>* v = b->pass_i32;
+  v[0].resize(size_t(L) + 1);
+  v[1].resize(std::max<size_t>(size_t(N), 1));
+  v[2].resize(std::max<size_t>(size_t(L), 1));
+  v[3].resize(size_t(L) + 1);
+  v[4].resize(std::max<size_t>(size_t(NP), 1));
+  v[5].assign(std::max<size_t>(size_t(L), 1), PIE_FOLD_ALL);
+  rc = pie_batcher_forward_pass(b, calls, lanes, n, frozen, num_keys, L, N, NP, v[0].data(),
+                                v[1].data(), v[2].data(), v[3].data(), v[4].data(), lane_keys,
+                                first_row, &L, &N, &NP);
+  if (rc != PIE_OK) return rc;
+  if (kv_len) std::memcpy(kv_len, v[2].data(), size_t(L) * sizeof(int32_t));
+  pie_fwd_meta m;
+  std::memset(&m, 0, sizeof(m));
+  m.num_lanes = L;
+  m.num_rows = N;
+  m.row_indptr = v[0].data();
+  m.positions = v[1].data();
+  m.slots = v[1].data();  // position = slot
+  m.kv_len = v[2].data();
+  m.page_indptr = v[3].data();
+  m.page_ids = v[4].data();
+  m.num_pool_pages = num_pool_pages;
+  m.fold_mode = v[5].data();
+  return pie_fwd_plan(desc, &m, dev_workspace, ws_bytes, stream, plan);
 }
 
 int pie_batcher_counts(const pie_batcher_t* b, int64_t* queued, int64_t* in_flight) {

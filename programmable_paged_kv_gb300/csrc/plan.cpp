@@ -483,7 +483,7 @@ extern "C" {
 
 const char* pie_fwd_last_error(void) { return g_last_error.c_str(); }
 
-int pie_fwd_abi_version(void) { return 103; }
+int pie_fwd_abi_version(void) { return 104; }
 
 static thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 

@@ -20,25 +20,32 @@ def _lib():
     build()
 
 
-def submit_trace(trace, batcher):
+def submit_trace(trace, batcher, native=False):
     """Queue every call of the trace; its reads are the pages it attends over,
-    its writes the pages of its new slots.  Returns the call tables."""
+    its writes the pages of its new slots (native: the batcher derives both
+    from the queue's registered working set).  Returns the call tables."""
     P = trace.pool.desc.page_size
     qids = [batcher.add_queue(int(p)) for p in trace.priority]
     cursor = [int(c) for c in trace.cached]
     call_set, call_rows, call_inputs = {}, {}, {}
+    if native:
+        for q, pages in enumerate(trace.queue_pages):
+            batcher.set_pages(q, pages)
     for q, qq, kk, vv in trace.calls:
         n = qq.shape[0]
         pages = trace.queue_pages[q]
         writes = sorted({int(pages[s // P]) for s in range(cursor[q], cursor[q] + n)})
         reads = [int(x) for x in pages[:(cursor[q] + n + P - 1) // P]]
-        cid = batcher.submit(qids[q], 0, n, key=q, reads=reads, writes=writes)
+        if native:
+            cid = batcher.submit_forward([qids[q]], [q], [n], [cursor[q]], P)[0]
+        else:
+            cid = batcher.submit(qids[q], 0, n, key=q, reads=reads, writes=writes)
         cursor[q] += n
         call_set[cid], call_rows[cid], call_inputs[cid] = q, n, (qq, kk, vv)
     return call_set, call_rows, call_inputs
 
 
-def run_batched(trace, max_calls, max_rows):
+def run_batched(trace, max_calls, max_rows, native=False):
     import torch
     from programmable_paged_kv_gb300 import Batcher, ForwardPlan, make_desc, make_meta, runner
     from programmable_paged_kv_gb300.batching import forward_batch_pass
@@ -46,8 +53,9 @@ def run_batched(trace, max_calls, max_rows):
     desc = make_desc(d)
     pools = runner.DevicePools(trace.pool)
     b = Batcher([True], max_calls, max_rows)
-    call_set, call_rows, call_inputs = submit_trace(trace, b)
+    call_set, call_rows, call_inputs = submit_trace(trace, b, native)
     frozen = {q: int(c) for q, c in enumerate(trace.cached)}
+    frozen_arr = np.asarray(trace.cached, np.int32).copy()
     tdt = torch.bfloat16 if d.dtype == W.BF16 else torch.float32
     Hq, Hkv, D = d.num_q_heads, d.num_kv_heads, d.head_dim
     outs, batches = {}, []
@@ -56,16 +64,27 @@ def run_batched(trace, max_calls, max_rows):
         if r is None:
             break
         _, ids, lanes = r
-        p, lane_set, first = forward_batch_pass(ids, lanes, call_set, call_rows,
-                                                trace.queue_pages, frozen)
-        N = int(p.row_indptr[-1])
+        if native:
+            # built and planned in one native call
+            ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+            plan, keys, first_arr, kv_len, N = b.plan_forward(ids, lanes, frozen_arr, desc,
+                                                              trace.pool.num_pool_pages, ws)
+            lane_set = [int(x) for x in keys]
+            first = {c: int(f) for c, f in zip(ids, first_arr)}
+            kv_len = kv_len.copy()
+            rows_of = [int(x) - frozen[w] for x, w in zip(kv_len, lane_set)]
+        else:
+            p, lane_set, first = forward_batch_pass(ids, lanes, call_set, call_rows,
+                                                    trace.queue_pages, frozen)
+            N = int(p.row_indptr[-1])
+            plan = ForwardPlan(desc, make_meta(p, trace.pool.num_pool_pages))
+            kv_len, rows_of = p.kv_len, np.diff(p.row_indptr)
         q = np.empty((N, Hq, D), trace.calls[0][1].dtype)
         k = np.empty((N, Hkv, D), q.dtype)
         v = np.empty((N, Hkv, D), q.dtype)
         for c in ids:
             s = slice(first[c], first[c] + call_rows[c])
             q[s], k[s], v[s] = call_inputs[c]
-        plan = ForwardPlan(desc, make_meta(p, trace.pool.num_pool_pages))
         fr = torch.tensor([frozen[w] for w in lane_set], dtype=torch.int32, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
@@ -77,14 +96,14 @@ def run_batched(trace, max_calls, max_rows):
         plan.fold(fr, None, st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        rows_of = np.diff(p.row_indptr)
-        assert np.array_equal(fr.cpu().numpy(), p.kv_len), "fold must freeze every new row"
+        assert np.array_equal(fr.cpu().numpy(), kv_len), "fold must freeze every new row"
         out_h, lse_h = runner.to_host(out, d.dtype), lse.cpu().numpy()
         for c in ids:
             s = slice(first[c], first[c] + call_rows[c])
             outs[c] = (out_h[s], lse_h[s])
         for w, n in zip(lane_set, rows_of):
             frozen[w] += int(n)
+            frozen_arr[w] += int(n)
         plan.close()
         b.complete(ids)
         batches.append((ids, lanes))
@@ -120,13 +139,14 @@ def run_alone(trace):
     return outs, k, v
 
 
-@pytest.mark.parametrize("limits", [(16, 512), (4, 64), (1, 1)],
-                         ids=["wide", "narrow", "one_call"])
-def test_batched_calls_equal_calls_run_alone(limits):
+@pytest.mark.parametrize("limits,native", [((16, 512), False), ((4, 64), False), ((1, 1), False),
+                                           ((16, 512), True), ((4, 64), True)],
+                         ids=["wide", "narrow", "one_call", "wide_native", "narrow_native"])
+def test_batched_calls_equal_calls_run_alone(limits, native):
     trace = W.forward_calls(3, queues=12, calls_per_queue=5, prefix=64, private_hi=40,
                             prefill_lo=4, prefill_hi=40, desc=W.Desc(8, 2, 128, 16, W.BF16),
                             num_pool_pages=1024)
-    outs, k_used, v_used, batches, untouched = run_batched(trace, *limits)
+    outs, k_used, v_used, batches, untouched = run_batched(trace, *limits, native)
     ref, k_ref, v_ref = run_alone(trace)
     dt = trace.pool.desc.dtype
     assert untouched
