@@ -140,6 +140,7 @@ extern "C" int pie_fwd_decode_attend_noalloc(const pie_fwd_desc* desc, int32_t n
 
   pie_fwd_plan_t p;
   std::memset(&p, 0, sizeof(p));
+  p.device_tables = true;  // the items kernel writes them
   p.desc = D;
   if (p.desc.sm_scale == 0.0f) p.desc.sm_scale = 1.0f / sqrtf(static_cast<float>(d));
   p.L = L;

@@ -18,20 +18,32 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv, int G, int N,
                                                       int R, int with_all, int tc_bn,
-                                                      T* out_readout, float* lse_readout,
-                                                      T* out_all, float* lse_all) {
+                                                      int tables_early, T* out_readout,
+                                                      float* lse_readout, T* out_all,
+                                                      float* lse_all) {
   constexpr int DPL = D / 32;
-  grid_dep_wait();  // the attention kernels' partial states
-  grid_dep_launch();
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int targets = R + (with_all ? N : 0);
-  if (gw >= targets * Hq) return;
-  const int tgt = gw / Hq, h = gw % Hq;
+  const bool active = gw < targets * Hq;
+  // tables_early: the plan's own tables (uploaded before any kernel of the
+  // pass ran) are read while the attention kernels still run; tables that
+  // device code wrote, and the partial states, only after the wait
+  const int tgt = active ? gw / Hq : 0, h = active ? gw % Hq : 0;
   const bool is_ro = tgt < R;
-  const int row = is_ro ? m.readout[tgt] : tgt - R;
-  const CombEntry ce = m.comb[int64_t(m.row_block[row]) * Hkv + h / G];
-  if (ce.nchunks < 0) return;  // written directly by the tensor-core kernel
+  CombEntry ce{0, -1, 0, 0, -1, 0, 0, 0};
+  int row = 0;
+  auto read_tables = [&] {
+    if (active) {
+      row = is_ro ? m.readout[tgt] : tgt - R;
+      ce = m.comb[int64_t(m.row_block[row]) * Hkv + h / G];
+    }
+  };
+  if (tables_early) read_tables();
+  grid_dep_wait();  // the attention kernels' partial states
+  grid_dep_launch();
+  if (!tables_early) read_tables();
+  if (!active || ce.nchunks < 0) return;  // < 0: written directly by the tensor-core kernel
   const int qi = (row - ce.row0) * G + h % G;
   // a masked tensor-core block uses as many chunks as its list length gives
   const int nch = ce.mblock < 0 ? ce.nchunks
@@ -114,7 +126,8 @@ static cudaError_t launch_comb(const pie_fwd_plan_t& p, void* out_readout, float
   if (warps == 0) return cudaSuccess;
   return launch_dependent(combine_kernel<T, D>, dim3(int((warps + 3) / 4)), dim3(128), 0, s, true,
                           p.dev, p.desc.num_q_heads, p.desc.num_kv_heads, p.G, p.N, p.R, with_all,
-                          tc_kv_tile(p.tc_nt), static_cast<T*>(out_readout), lse_readout,
+                          tc_kv_tile(p.tc_nt), p.device_tables ? 0 : 1,
+                          static_cast<T*>(out_readout), lse_readout,
                           static_cast<T*>(out_all), lse_all);
 }
 

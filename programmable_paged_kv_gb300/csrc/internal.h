@@ -149,6 +149,10 @@ struct pie_fwd_plan {
   int32_t num_pool_pages;
   bool has_mask;
   bool any_channel;
+  // the combine step's tables (row blocks, combine entries, readout rows) are
+  // written by device code of the same stream rather than uploaded with the
+  // plan: the combine kernel reads them only after its dependency wait
+  bool device_tables;
   int32_t nq;                // query vectors per decode item (2, 4 or 8)
   int32_t num_dec_items;
   int32_t num_tc_items;
