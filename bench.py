@@ -1010,7 +1010,10 @@ def run_adapters(args, local):
             "unit": "rows/s", "value": rows / dev_s, "ms_per_step": dev_s * 1e3,
             "steps": Kst, "warmup": Wm, "device_ms_per_apply": dev_s * 1e3,
             "eager_call_ms_median": med * 1e3, "eager_rows_per_s": rows / med,
-            "alg_bytes": byts, "gpu_launches": 2 * (Kst + reps * NB),
+            "alg_bytes": byts,
+            # kernels per apply: one for a grouped plan (a cluster per adapter), else two
+            "gpu_launches": (1 if plan.num_groups > 0 else 2) * (Kst + reps * NB),
+            "adapter_path": "grouped" if plan.num_groups > 0 else "tiles",
             "roofline": {"bound": "hbm", "achieved": byts / dev_s / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": byts / dev_s / 1e9 / hbm, "traffic": None,
                          "peak_kind": kind},

@@ -328,6 +328,11 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
                          pie_fwd_adapter_plan_t** out);
 /* Number of tiles of a plan (rows of lanes with an adapter, 128 per tile). */
 int32_t pie_fwd_adapter_plan_num_tiles(const pie_fwd_adapter_plan_t* plan);
+/* Number of adapter groups when every adapter in use serves at most 16 rows
+ * (a decode-shaped plan): each apply with rank > 0 then runs one kernel, a
+ * cluster of 8 CTAs per group; 0 when the plan applies by tiles (two kernels,
+ * shrink and expand).  -1 for a NULL plan. */
+int32_t pie_fwd_adapter_plan_num_groups(const pie_fwd_adapter_plan_t* plan);
 /* Apply the adapters at one site.
  *   x: device bf16 [num_rows][d_in]; y: device bf16 [num_rows][d_out], both
  *            contiguous and 16-byte aligned.
@@ -339,7 +344,8 @@ int32_t pie_fwd_adapter_plan_num_tiles(const pie_fwd_adapter_plan_t* plan);
  * Supported: dtype PIE_BF16, rank in {0, 8, 16, 32, 64} and <= max_rank,
  * d_in a multiple of 64, d_out a multiple of 256 (PIE_EUNSUPPORTED / ERANGE
  * otherwise); PIE_EINVAL for NULL or misaligned required pointers.  Up to two
- * kernels on `stream`; no host synchronization. */
+ * kernels on `stream` (one for a grouped plan, see
+ * pie_fwd_adapter_plan_num_groups); no host synchronization. */
 int pie_fwd_adapter_apply(const pie_fwd_adapter_plan_t* plan, int32_t dtype, int32_t d_in,
                           int32_t d_out, int32_t rank, const void* x, void* y, const void* lora_a,
                           const void* lora_b, const float* scale, const void* ia3,

@@ -283,6 +283,7 @@ class AdapterPlan:
             "pie_fwd_adapter_plan")
         self.handle = h
         self.num_tiles = int(self.lib.pie_fwd_adapter_plan_num_tiles(h))
+        self.num_groups = int(self.lib.pie_fwd_adapter_plan_num_groups(h))
 
     def apply(self, x, y, lora_a=None, lora_b=None, scale=None, ia3=None, status=None,
               stream=None):

@@ -92,6 +92,7 @@ SIGNATURES = {
     "pie_fwd_adapter_plan": (C.c_int, [C.c_int32, _P, _P, C.c_int32, C.c_int32, _P, C.c_size_t,
                                        _P, C.POINTER(C.c_void_p)]),
     "pie_fwd_adapter_plan_num_tiles": (C.c_int32, [_P]),
+    "pie_fwd_adapter_plan_num_groups": (C.c_int32, [_P]),
     "pie_fwd_adapter_apply": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P,
                                         _P, _P, _P, _P, _P, _P]),
     "pie_fwd_adapter_plan_destroy": (None, [_P]),

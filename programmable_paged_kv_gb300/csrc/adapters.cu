@@ -30,10 +30,21 @@
 // by HBM, so it stays off the tensor cores; the shrink does r multiply-adds
 // per 2 bytes of x, the contraction that needs them.  Every wait is bounded
 // in time (PIE_STATUS_TIMEOUT).
+//
+// Plans whose adapters each serve few rows (decode: a row per lane) take one
+// kernel instead, grouped by adapter: a cluster of 8 CTAs per adapter in use.
+// CTA c forms the rank-r partial sums of the group's rows over its eighth of
+// d_in (CUDA cores, fp32), the cluster adds the eight partials up through
+// distributed shared memory, and CTA c applies y' = (y + c_a B_a t) * s_a to
+// its eighth of d_out, with its B_a rows and y values loaded before the
+// exchange.  Two kernels and the partial sums' round trip through global
+// memory would cost more than the whole of this work.
 
 #include <algorithm>
 #include <cstring>
 #include <vector>
+
+#include <cooperative_groups.h>
 
 #include "internal.h"
 #include "tc_util.cuh"
@@ -513,6 +524,169 @@ __global__ void __launch_bounds__(ad::kExpandThreads) adapter_expand_kernel(
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Grouped adapters for few rows per adapter: one cluster of kGCluster CTAs
+// per adapter in use (see the top of this file).
+// ---------------------------------------------------------------------------
+namespace ad {
+
+constexpr int kGCluster = 8;      // CTAs per adapter: d_in and d_out cut in eighths
+constexpr int kGMaxRows = 16;     // rows an adapter may serve on this path
+constexpr int kGThreads = 256;
+
+// An adapter in use and its rows: rows[row_off .. row_off + n).
+struct alignas(16) Group {
+  int32_t row_off, n, adapter, pad;
+};
+
+}  // namespace ad
+
+template <int R, int NR>
+__global__ void __cluster_dims__(ad::kGCluster, 1, 1) __launch_bounds__(ad::kGThreads)
+    adapter_group_kernel(const ad::Group* __restrict__ groups, const int32_t* __restrict__ rows,
+                         int d_in, int d_out, const __nv_bfloat16* __restrict__ x,
+                         __nv_bfloat16* y, const __nv_bfloat16* __restrict__ lora_a,
+                         const __nv_bfloat16* __restrict__ lora_b,
+                         const float* __restrict__ scale, const __nv_bfloat16* __restrict__ ia3) {
+  using namespace ad;
+  namespace cg = cooperative_groups;
+  constexpr int kWarps = kGThreads / 32;
+  constexpr int KPW = (R + kWarps - 1) / kWarps;  // ranks per warp
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = int(cluster.block_rank());
+  const Group g = groups[blockIdx.x / kGCluster];
+  const int n = g.n, a = g.adapter;  // n <= NR
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float part[NR * R];  // this CTA's partial sums
+  __shared__ float tot[NR * R];   // the cluster's, scaled by c_a
+  int my_rows[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) my_rows[r] = rows[g.row_off + (r < n ? r : 0)];
+  // this CTA's eighth of d_in, in 16-byte vectors of x and A; a lane takes
+  // vectors lane, lane + 32, ... of it
+  const int units = d_in / 8;
+  const int u0 = c * units / kGCluster, u1 = (c + 1) * units / kGCluster;
+
+  // the expand's operands first (they do not depend on the exchange): this
+  // thread's first pair of output columns, its B_a rows (bf16 pairs) and y
+  const int ncols = d_out / kGCluster, col0 = c * ncols, pairs = ncols / 2;
+  const __nv_bfloat16* Ba = lora_b + int64_t(a) * d_out * R;
+  uint32_t bq[2][R / 2];
+  __nv_bfloat162 yq[NR];
+  auto load_pair = [&](int cp) {
+    const int o = col0 + 2 * cp;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4* src = reinterpret_cast<const uint4*>(Ba + int64_t(o + k) * R);
+#pragma unroll
+      for (int v = 0; v < R / 8; ++v) {
+        const uint4 u = src[v];
+        bq[k][4 * v] = u.x;
+        bq[k][4 * v + 1] = u.y;
+        bq[k][4 * v + 2] = u.z;
+        bq[k][4 * v + 3] = u.w;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      yq[r] = *reinterpret_cast<const __nv_bfloat162*>(y + int64_t(my_rows[r]) * d_out + o);
+  };
+  if (tid < pairs) load_pair(tid);
+
+  // shrink: warp w takes ranks w, w + 8, ... in passes of KB ranks (at most
+  // 32 (rank, row) accumulator pairs live); per step of 32 vectors the A_a
+  // and x vectors of the pass's ranks and all rows are loaded together, then
+  // one dot product per (rank, row) is reduced across the warp.  Rows past n
+  // repeat the first row (finite) and are never stored.
+  constexpr int KB = (32 / NR) < KPW ? (32 / NR < 1 ? 1 : 32 / NR) : KPW;
+  const uint4* Aa = reinterpret_cast<const uint4*>(lora_a + int64_t(a) * R * d_in);
+#pragma unroll 1
+  for (int i0 = 0; i0 < KPW; i0 += KB) {
+    float acc[KB][NR], acc2[KB][NR];  // even and odd elements (one packed FMA)
+#pragma unroll
+    for (int i = 0; i < KB; ++i)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) acc[i][r] = acc2[i][r] = 0.f;
+    for (int u = u0 + lane; u < u1; u += 32) {
+      uint4 av[KB], xv[NR];
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        const int k = warp + kWarps * (i0 + i);
+        av[i] = k < R ? Aa[int64_t(k) * units + u] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        xv[r] = reinterpret_cast<const uint4*>(x + int64_t(my_rows[r]) * d_in)[u];
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        float af[8];
+        unpack16<__nv_bfloat16>(av[i], af);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float xf[8];
+          unpack16<__nv_bfloat16>(xv[r], xf);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            ffma2(acc[i][r], acc2[i][r], af[e], af[e + 1], xf[e], xf[e + 1], acc[i][r], acc2[i][r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+      const int k = warp + kWarps * (i0 + i);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float v = acc[i][r] + acc2[i][r];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0 && k < R && r < n) part[r * R + k] = v;
+      }
+    }
+  }
+  // the cluster's eight partials, summed and scaled by c_a, in every CTA
+  cluster.sync();
+  const float ca = scale[a];
+  for (int i = tid; i < n * R; i += kGThreads) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kGCluster; ++q) v += cluster.map_shared_rank(part, q)[i];
+    tot[i] = v * ca;
+  }
+  // no CTA leaves, and with it its shared memory, before every peer has read it
+  cluster.sync();
+
+  // expand: y' = (y + c_a B_a t) * s_a over this CTA's columns, two per thread
+  for (int cp = tid; cp < pairs; cp += kGThreads) {
+    if (cp != tid) load_pair(cp);
+    const int o = col0 + 2 * cp;
+    float s0 = 1.f, s1 = 1.f;
+    if (ia3) {
+      s0 = __bfloat162float(ia3[int64_t(a) * d_out + o]);
+      s1 = __bfloat162float(ia3[int64_t(a) * d_out + o + 1]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (r < n) {
+        float d0 = 0.f, d1 = 0.f;
+        const float* tr = tot + r * R;
+#pragma unroll
+        for (int k = 0; k < R / 2; ++k) {
+          const float t0 = tr[2 * k], t1 = tr[2 * k + 1];
+          const uint32_t b0 = bq[0][k], b1 = bq[1][k];
+          d0 = fmaf(t0, __uint_as_float(b0 << 16), d0);
+          d0 = fmaf(t1, __uint_as_float(b0 & 0xFFFF0000u), d0);
+          d1 = fmaf(t0, __uint_as_float(b1 << 16), d1);
+          d1 = fmaf(t1, __uint_as_float(b1 & 0xFFFF0000u), d1);
+        }
+        const float2 yv = __bfloat1622float2(yq[r]);
+        *reinterpret_cast<__nv_bfloat162*>(y + int64_t(my_rows[r]) * d_out + o) =
+            __floats2bfloat162_rn((yv.x + d0) * s0, (yv.y + d1) * s1);
+      }
+    }
+  }
+}
+
 }  // namespace pie
 
 // ---------------------------------------------------------------------------
@@ -525,6 +699,11 @@ struct pie_fwd_adapter_plan {
   int* counters;         // device: finished d_in ranges per tile (zero between applies)
   float* t_part;         // device scratch: [kMaxSplits][num_rows][rank] partial sums
   float* t_final;        // device scratch: [num_rows][rank], c_a A_a x
+  // grouped path (every adapter serves at most kGMaxRows rows): one cluster
+  // per adapter in use; num_groups 0 when the plan does not take it
+  int32_t num_groups, max_group_rows;
+  pie::ad::Group* groups;  // device, in the workspace
+  int32_t* group_rows;     // device: the groups' rows
   pie::PinnedBlock* staging;
 };
 
@@ -551,15 +730,19 @@ bool rank_built(int r) { return r == 0 || r == 8 || r == 16 || r == 32 || r == 6
 
 // workspace: tiles | counters (both uploaded, counters as zeros) | t_part | t_final
 struct WsLayout {
-  size_t tiles = 0, counters = 0, t_part = 0, t_final = 0, total = 0;
+  size_t tiles = 0, counters = 0, groups = 0, group_rows = 0, t_part = 0, t_final = 0, total = 0;
 };
 
+// tiles, per-tile counters, groups (at most one per tile) and their rows are
+// uploaded in one copy; the partial sums follow
 WsLayout ws_layout(int64_t num_tiles, int64_t num_rows, int max_rank) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   WsLayout Y;
   Y.tiles = 0;
   Y.counters = up(size_t(num_tiles) * sizeof(pie::ad::Tile));
-  Y.t_part = Y.counters + up(size_t(num_tiles) * 4);
+  Y.groups = Y.counters + up(size_t(num_tiles) * 4);
+  Y.group_rows = Y.groups + up(size_t(num_tiles) * sizeof(pie::ad::Group));
+  Y.t_part = Y.group_rows + up(size_t(num_rows) * 4);
   Y.t_final =
       Y.t_part + up(size_t(pie::ad::kMaxSplits) * size_t(num_rows) * size_t(max_rank) * 4);
   Y.total = Y.t_final + up(size_t(num_rows) * size_t(max_rank) * 4);
@@ -571,6 +754,23 @@ cudaError_t launch_adapter(const pie_fwd_adapter_plan_t& p, int d_in, int d_out,
                            void* y, const void* lora_a, const void* lora_b, const float* scale,
                            const void* ia3, uint32_t* status, cudaStream_t s) {
   using namespace pie;
+  if constexpr (R > 0) {
+    if (p.num_groups > 0) {
+      // few rows per adapter: one kernel, a cluster per adapter in use, its
+      // row loops sized for the plan's largest group
+      auto go = [&](auto kernel) {
+        kernel<<<p.num_groups * ad::kGCluster, ad::kGThreads, 0, s>>>(
+            p.groups, p.group_rows, d_in, d_out, static_cast<const __nv_bfloat16*>(x),
+            static_cast<__nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(lora_a),
+            static_cast<const __nv_bfloat16*>(lora_b), scale,
+            static_cast<const __nv_bfloat16*>(ia3));
+        return cudaGetLastError();
+      };
+      if (p.max_group_rows <= 4) return go(adapter_group_kernel<R, 4>);
+      if (p.max_group_rows <= 8) return go(adapter_group_kernel<R, 8>);
+      return go(adapter_group_kernel<R, ad::kGMaxRows>);
+    }
+  }
   int splits = 1;
   if constexpr (R > 0) {
     int dev = 0, sms = 152;
@@ -699,14 +899,41 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
   if (reinterpret_cast<uintptr_t>(dev_workspace) % 256 != 0)
     return set_last_error(PIE_EINVAL, "workspace must be 256-byte aligned");
 
-  // one copy: the tiles, then zeroed per-tile counters
-  const size_t copy = tiles.empty() ? 0 : Y.counters + tiles.size() * 4;
+  // the grouped path when every adapter in use serves at most kGMaxRows rows:
+  // one group per adapter, its rows in row order
+  std::vector<ad::Group> groups;
+  std::vector<int32_t> group_rows;
+  {
+    std::vector<std::vector<int32_t>> by_adapter(size_t(std::max(num_adapters, 0)));
+    bool few = true;
+    for (int l = 0; l < num_lanes && few; ++l) {
+      const int a = adapter_of_lane[l];
+      if (a < 0) continue;
+      for (int r = row_indptr[l]; r < row_indptr[l + 1]; ++r) by_adapter[size_t(a)].push_back(r);
+      few = by_adapter[size_t(a)].size() <= size_t(ad::kGMaxRows);
+    }
+    if (few) {
+      for (int a = 0; a < num_adapters; ++a) {
+        std::vector<int32_t>& v = by_adapter[size_t(a)];
+        if (v.empty()) continue;
+        std::sort(v.begin(), v.end());
+        groups.push_back({int32_t(group_rows.size()), int32_t(v.size()), a, 0});
+        group_rows.insert(group_rows.end(), v.begin(), v.end());
+      }
+    }
+  }
+  // one copy: the tiles, zeroed per-tile counters, the groups and their rows
+  const size_t copy = tiles.empty() ? 0 : Y.group_rows + group_rows.size() * 4;
   int err = PIE_OK;
   PinnedBlock* blk = pinned_acquire(std::max<size_t>(copy, 1), &err);
   if (!blk) return err;
   if (copy) {
     std::memset(blk->ptr, 0, copy);
     std::memcpy(blk->ptr, tiles.data(), tiles.size() * sizeof(ad::Tile));
+    std::memcpy(static_cast<char*>(blk->ptr) + Y.groups, groups.data(),
+                groups.size() * sizeof(ad::Group));
+    std::memcpy(static_cast<char*>(blk->ptr) + Y.group_rows, group_rows.data(),
+                group_rows.size() * 4);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (copy && cudaMemcpyAsync(static_cast<char*>(dev_workspace) + Y.tiles, blk->ptr, copy,
@@ -730,6 +957,11 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
   p->counters = reinterpret_cast<int*>(static_cast<char*>(dev_workspace) + Y.counters);
   p->t_part = reinterpret_cast<float*>(static_cast<char*>(dev_workspace) + Y.t_part);
   p->t_final = reinterpret_cast<float*>(static_cast<char*>(dev_workspace) + Y.t_final);
+  p->num_groups = int32_t(groups.size());
+  p->max_group_rows = 0;
+  for (const ad::Group& gr : groups) p->max_group_rows = std::max(p->max_group_rows, gr.n);
+  p->groups = reinterpret_cast<ad::Group*>(static_cast<char*>(dev_workspace) + Y.groups);
+  p->group_rows = reinterpret_cast<int32_t*>(static_cast<char*>(dev_workspace) + Y.group_rows);
   p->staging = blk;
   *out = p;
   return PIE_OK;
@@ -737,6 +969,10 @@ int pie_fwd_adapter_plan(int32_t num_lanes, const int32_t* row_indptr,
 
 int32_t pie_fwd_adapter_plan_num_tiles(const pie_fwd_adapter_plan_t* plan) {
   return plan ? plan->num_tiles : -1;
+}
+
+int32_t pie_fwd_adapter_plan_num_groups(const pie_fwd_adapter_plan_t* plan) {
+  return plan ? plan->num_groups : -1;
 }
 
 int pie_fwd_adapter_apply(const pie_fwd_adapter_plan_t* plan, int32_t dtype, int32_t d_in,

@@ -159,10 +159,11 @@ def test_adapter_plan_refuses_bad_lanes_before_any_cuda_call(lib):
     ri = i32([0, 1, 130, 130, 131])
     assert ws(4, ri.ctypes.data, 16, C.byref(n)) == abi.PIE_OK
     # tiles: 1 + 2 + 0 + 1 rows-of-128 blocks, 16 bytes each, and a counter
-    # each (256-aligned); then 8 ranges x 131 rows x 16 fp32 partial sums and
-    # 131 x 16 final sums
+    # each (256-aligned); groups of the grouped path (at most one per tile,
+    # 16 bytes each) and their rows (131 int32); then 8 ranges x 131 rows x 16
+    # fp32 partial sums and 131 x 16 final sums
     up = lambda v: (v + 255) // 256 * 256
-    assert n.value == 256 + 256 + up(8 * 131 * 16 * 4) + up(131 * 16 * 4)
+    assert n.value == 256 + 256 + 256 + up(131 * 4) + up(8 * 131 * 16 * 4) + up(131 * 16 * 4)
     assert ws(4, ri.ctypes.data, 12, C.byref(n)) == abi.PIE_EUNSUPPORTED   # rank not built
     assert ws(2, i32([0, 3, 2]).ctypes.data, 16, C.byref(n)) == abi.PIE_EINVAL   # not monotone
     assert ws(1, i32([1, 3]).ctypes.data, 16, C.byref(n)) == abi.PIE_EINVAL      # indptr[0] != 0

@@ -118,6 +118,23 @@ CASES = {
                       none_every=0),
     # guidance-pair prefill shape: 64 lanes x 64 rows, q site
     "prefill_64x64_r16": dict(rows=[64] * 64, d_in=4096, d_out=4096, rank=16, n_adapters=16),
+    # few rows per adapter (the grouped path, a cluster per adapter): eighths
+    # of d_in of 5 vectors, 32-column eighths of d_out, every rank, no IA3,
+    # an adapter with exactly 16 rows; 17 rows on one adapter takes the tiles
+    "grouped_r8": dict(rows=[1, 2, 1, 3, 1, 4, 2], d_in=320, d_out=512, rank=8, n_adapters=3,
+                       none_every=4),
+    "grouped_r32": dict(rows=[1] * 40, d_in=1024, d_out=768, rank=32, n_adapters=8,
+                        none_every=6),
+    "grouped_r64": dict(rows=[2, 1, 3, 2, 1, 1], d_in=256, d_out=256, rank=64, n_adapters=2,
+                        none_every=0),
+    "grouped_no_ia3": dict(rows=[1] * 10, d_in=512, d_out=1024, rank=16, n_adapters=4,
+                           ia3=False, none_every=0),
+    "grouped_16_rows": dict(rows=[15, 1], d_in=512, d_out=512, rank=16, n_adapters=1,
+                            none_every=0),
+    "grouped_4_rows": dict(rows=[1] * 8, d_in=2048, d_out=1536, rank=16, n_adapters=8,
+                           none_every=0),
+    "tiles_17_rows": dict(rows=[16, 1], d_in=512, d_out=512, rank=16, n_adapters=1,
+                          none_every=0),
 }
 
 
