@@ -433,48 +433,34 @@ def run_ours(args, ws, rank, local, pg):
     st = int(status.item())
 
     # ---- end to end: host q/k/v in, readout back to host, every step
-    # each batch's q, k and v packed in one pinned host buffer (one copy in per
-    # step), the readout and its lse in one device buffer (one copy out)
+    # each step's q, k and v packed in one pinned host buffer (one copy in), the
+    # whole pass through one pie_fwd_forward call (plan, append, attend, fold),
+    # its readout and lse from one device buffer (one copy out); all on one
+    # stream, so a step's copy in follows the previous step's kernels and the
+    # host runs ahead of the GPU
+    from programmable_paged_kv_gb300 import forward
     qkv_h = [torch.cat([x.reshape(-1) for x in (q_d[j], k_d[j], v_d[j])]).cpu().pin_memory()
              for j in range(NB)]
     nq, nk = q_d[0].numel(), k_d[0].numel()
     ob, lb = out.numel() * out.element_size(), lse.numel() * lse.element_size()
-    # inputs and results double-buffered: step t+1's q/k/v come in on the copy
-    # stream while step t computes, and step t's readout goes back on a third
-    # stream while step t+1 computes (a serving loop's pipelining; every step
-    # still moves its own inputs in and its result out)
-    d2h_stream = torch.cuda.Stream(dev)
-    qkv_d = [torch.empty_like(qkv_h[0], device=dev) for _ in range(2)]
-    ins = [(x[:nq].view(q_d[0].shape), x[nq:nq + nk].view(k_d[0].shape),
-            x[nq + nk:].view(v_d[0].shape)) for x in qkv_d]
-    res_d = [torch.empty(ob + lb, dtype=torch.uint8, device=dev) for _ in range(2)]
-    outs = [(x[:ob].view(out.dtype).view(out.shape), x[ob:].view(lse.dtype).view(lse.shape))
-            for x in res_d]
+    qkv_d = torch.empty_like(qkv_h[0], device=dev)
+    ins = (qkv_d[:nq].view(q_d[0].shape), qkv_d[nq:nq + nk].view(k_d[0].shape),
+           qkv_d[nq + nk:].view(v_d[0].shape))
+    res_d = torch.empty(ob + lb, dtype=torch.uint8, device=dev)
+    o_e, l_e = res_d[:ob].view(out.dtype).view(out.shape), res_d[ob:].view(lse.dtype).view(lse.shape)
     res_h = [torch.empty(ob + lb, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    step_done = [torch.cuda.Event() for _ in range(2)]  # inputs free, result ready
-    out_free = [torch.cuda.Event() for _ in range(2)]
-
-    def issue_inputs(t):
-        b, j = t % 2, t % NB
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(step_done[b])
-            qkv_d[b].copy_(qkv_h[j], non_blocking=True)
-            in_ready[b].record(copy_stream)
+    ws_e = workspaces[0]
+    for pl in live:
+        pl.close()
+    live.clear()
+    torch.cuda.synchronize()
 
     def e2e_step(t):
-        b = t % 2
-        issue_inputs(t + 1)  # overlaps this step
-        stream.wait_event(in_ready[b])
-        stream.wait_event(out_free[b])
-        step(t, *ins[b], o=outs[b][0], lo=outs[b][1])
-        step_done[b].record(stream)
-        with torch.cuda.stream(d2h_stream):
-            d2h_stream.wait_event(step_done[b])
-            res_h[b].copy_(res_d[b], non_blocking=True)
-            out_free[b].record(d2h_stream)
+        qkv_d.copy_(qkv_h[t % NB], non_blocking=True)
+        forward(cdesc, metas[t], ws_e, *ins, q_rot, k_pool, v_pool, frozen, None, o_e, l_e,
+                None, None, None, status)
+        res_h[t % 2].copy_(res_d, non_blocking=True)
 
-    issue_inputs(t)
     for _ in range(Wm):
         e2e_step(t)
         t += 1
@@ -488,9 +474,7 @@ def run_ours(args, ws, rank, local, pg):
         e_tok += acct[t][0]
         e2e_step(t)
         t += 1
-    for ev_ in out_free:  # the last results are on the host
-        stream.wait_event(ev_)
-    e1.record(stream)
+    e1.record(stream)  # after the last result's copy to the host
     torch.cuda.synchronize()
     barrier(pg)
     e_ms = max_over_ranks(pg, e0.elapsed_time(e1))

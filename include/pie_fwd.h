@@ -217,6 +217,22 @@ int pie_fwd_fold(const pie_fwd_plan_t* plan, int32_t* frozen_len, const int32_t*
  * still in flight; never waits for kernels. */
 void pie_fwd_plan_destroy(pie_fwd_plan_t* plan);
 
+/* One whole ForwardPass (steps 1-4 of "The forward pass") in one call, on
+ * `stream`: pie_fwd_plan into dev_workspace, pie_fwd_append_kv,
+ * pie_fwd_set_mask when the pass has a mask, pie_fwd_attend, pie_fwd_fold,
+ * then pie_fwd_plan_destroy (the plan's pinned staging is reused only after
+ * its upload completed).  Every argument means what it means in those calls;
+ * mask_words and channel are NULL when the pass has neither.  The workspace
+ * is busy until the pass's kernels have finished: a caller that plans the
+ * next pass on another stream first waits for an event recorded after this
+ * call.  Errors: those of the calls, from the first that fails (nothing later
+ * is launched). */
+int pie_fwd_forward(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_workspace,
+                    size_t ws_bytes, const void* q, const void* k, const void* v, void* q_rot,
+                    void* k_pool, void* v_pool, int32_t* frozen_len, const uint32_t* mask_words,
+                    void* out_readout, float* lse_readout, void* out_all, float* lse_all,
+                    const int32_t* channel, uint32_t* status, void* stream);
+
 /* Message for the calling thread's most recent error ("" if none). */
 const char* pie_fwd_last_error(void);
 

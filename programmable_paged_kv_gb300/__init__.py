@@ -94,6 +94,22 @@ def set_timing_events(start=None, stop=None) -> None:
               "pie_fwd_set_timing_events")
 
 
+def forward(desc: abi.pie_fwd_desc, meta: _HostMeta, workspace, q, k, v, q_rot, k_pool, v_pool,
+            frozen_len, mask_words=None, out_readout=None, lse_readout=None, out_all=None,
+            lse_all=None, channel=None, status=None, stream=None) -> None:
+    """pie_fwd_forward: plan, append, (mask), attend and fold of one pass in
+    one native call; workspace: uint8 CUDA tensor of at least
+    workspace_bytes(desc, meta), busy until the pass's kernels finish."""
+    abi.check(abi.load().pie_fwd_forward(
+        C.byref(desc), C.byref(meta.c), _ptr(workspace, "workspace"), workspace.numel(),
+        _ptr(q, "q"), _ptr(k, "k"), _ptr(v, "v"), _ptr(q_rot, "q_rot"), _ptr(k_pool, "k_pool"),
+        _ptr(v_pool, "v_pool"), _ptr(frozen_len, "frozen_len"),
+        _ptr(mask_words, "mask_words", False), _ptr(out_readout, "out_readout", False),
+        _ptr(lse_readout, "lse_readout", False), _ptr(out_all, "out_all", False),
+        _ptr(lse_all, "lse_all", False), _ptr(channel, "channel", False),
+        _ptr(status, "status", False), _stream(stream)), "pie_fwd_forward")
+
+
 def decode_loop_workspace_bytes(desc: abi.pie_fwd_desc, num_lanes: int, max_pages_per_lane: int) -> int:
     n = C.c_size_t(0)
     abi.check(abi.load().pie_fwd_decode_loop_workspace_bytes(C.byref(desc), num_lanes,

@@ -65,6 +65,8 @@ SIGNATURES = {
     "pie_fwd_append_kv": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pie_fwd_attend": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pie_fwd_fold": (C.c_int, [_P, _P, _P, _P, _P]),
+    "pie_fwd_forward": (C.c_int, [_P, _P, _P, C.c_size_t, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  _P, _P, _P, _P, _P]),
     "pie_fwd_plan_destroy": (None, [_P]),
     "pie_fwd_last_error": (C.c_char_p, []),
     "pie_fwd_abi_version": (C.c_int, []),

@@ -483,7 +483,7 @@ extern "C" {
 
 const char* pie_fwd_last_error(void) { return g_last_error.c_str(); }
 
-int pie_fwd_abi_version(void) { return 104; }
+int pie_fwd_abi_version(void) { return 105; }
 
 static thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 
@@ -708,6 +708,24 @@ int pie_fwd_set_mask(pie_fwd_plan_t* plan, const uint32_t* mask_words, void* str
   }
   plan->mask_set = mask_words;
   return PIE_OK;
+}
+
+int pie_fwd_forward(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_workspace,
+                    size_t ws_bytes, const void* q, const void* k, const void* v, void* q_rot,
+                    void* k_pool, void* v_pool, int32_t* frozen_len, const uint32_t* mask_words,
+                    void* out_readout, float* lse_readout, void* out_all, float* lse_all,
+                    const int32_t* channel, uint32_t* status, void* stream) {
+  pie_fwd_plan_t* plan = nullptr;
+  int rc = pie_fwd_plan(desc, meta, dev_workspace, ws_bytes, stream, &plan);
+  if (rc != PIE_OK) return rc;
+  rc = pie_fwd_append_kv(plan, q, k, v, q_rot, k_pool, v_pool, frozen_len, status, stream);
+  if (rc == PIE_OK && plan->has_mask && mask_words) rc = pie_fwd_set_mask(plan, mask_words, stream);
+  if (rc == PIE_OK)
+    rc = pie_fwd_attend(plan, q_rot, k_pool, v_pool, mask_words, out_readout, lse_readout,
+                        out_all, lse_all, status, stream);
+  if (rc == PIE_OK) rc = pie_fwd_fold(plan, frozen_len, channel, status, stream);
+  pie_fwd_plan_destroy(plan);
+  return rc;
 }
 
 int pie_fwd_fold(const pie_fwd_plan_t* plan, int32_t* frozen_len, const int32_t* channel,

@@ -71,11 +71,12 @@ class DevicePools:
         self.used = idx
 
 
-def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True):
+def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True, one_call: bool = False):
     """Run every pass of `sc`; returns (k_used, v_used, frozen, results) where
     k_used/v_used are the pool pages listed in sc.pool_pages (storage arrays)
     and results[i] holds q_rot, out_all, lse_all, out_readout, lse_readout
-    and status of pass i."""
+    and status of pass i.  one_call: each pass through pie_fwd_forward
+    instead of plan / append_kv / attend / fold."""
     import torch
     d = sc.desc
     desc = make_desc(d)
@@ -85,6 +86,9 @@ def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True):
     for p in sc.passes:
         meta = make_meta(p, sc.num_pool_pages)
         plan = ForwardPlan(desc, meta)
+        if one_call:  # only its readout count is used; the pass plans itself
+            R = plan.num_readout
+            plan.close()
         N, Hq, D = p.num_rows, d.num_q_heads, d.head_dim
         tdt = torch.float32 if d.dtype == 0 else torch.bfloat16
         q = to_device(p.q, d.dtype)
@@ -92,8 +96,9 @@ def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True):
         v = to_device(p.v, d.dtype)
         q_rot = torch.empty((N, Hq, D), dtype=tdt, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        plan.append_kv(q, k, v, q_rot, pools.k, pools.v, frozen, status)
-        R = plan.num_readout
+        if not one_call:
+            plan.append_kv(q, k, v, q_rot, pools.k, pools.v, frozen, status)
+            R = plan.num_readout
         out_ro = torch.empty((R, Hq, D), dtype=tdt, device="cuda")
         lse_ro = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
         out_all = torch.empty((N, Hq, D), dtype=tdt, device="cuda") if want_all else None
@@ -101,12 +106,18 @@ def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True):
         mw = None
         if p.mask_words is not None:
             mw = torch.from_numpy(p.mask_words.view(np.int32)).cuda()
-        plan.attend(q_rot, pools.k, pools.v, mw, out_ro, lse_ro, out_all, lse_all, status)
         chan = None
         if p.channel is not None:
             # the epilogue's write of the accepted counts, ordered on the stream
             chan = torch.from_numpy(p.channel.astype(np.int32)).cuda()
-        plan.fold(frozen, chan, status)
+        if one_call:
+            from . import forward, workspace_bytes
+            ws = torch.empty(workspace_bytes(desc, meta) + 256, dtype=torch.uint8, device="cuda")
+            forward(desc, meta, ws, q, k, v, q_rot, pools.k, pools.v, frozen, mw, out_ro, lse_ro,
+                    out_all, lse_all, chan, status)
+        else:
+            plan.attend(q_rot, pools.k, pools.v, mw, out_ro, lse_ro, out_all, lse_all, status)
+            plan.fold(frozen, chan, status)
         torch.cuda.synchronize()
         res = dict(q_rot=to_host(q_rot, d.dtype), out_readout=to_host(out_ro, d.dtype),
                    lse_readout=lse_ro.cpu().numpy(), status=int(status.item()) & 0xFFFFFFFF)
@@ -114,7 +125,8 @@ def run_scenario(sc, want_all: bool = True, status_per_pass: bool = True):
             res["out_all"] = to_host(out_all, d.dtype)
             res["lse_all"] = lse_all.cpu().numpy()
         results.append(res)
-        plan.close()
+        if not one_call:
+            plan.close()
     k_used = to_host(pools.k.index_select(0, pools.used), d.dtype)
     v_used = to_host(pools.v.index_select(0, pools.used), d.dtype)
     untouched_ok = _untouched_is_canary(pools, d.dtype)

@@ -34,7 +34,7 @@ def test_build_can_be_called_again(lib):
 
 
 def test_abi_version(lib):
-    assert lib.pie_fwd_abi_version() == 104
+    assert lib.pie_fwd_abi_version() == 105
 
 
 def test_timing_events_need_both_or_neither(lib):
