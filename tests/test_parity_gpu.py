@@ -6,7 +6,8 @@ same seeded inputs.
   rows, frozen lengths and status words;
 * the full-size configurations, in the launch configuration the benchmark
   times, compared on sampled rows (the oracle computes those rows only) plus
-  every bookkeeping result;
+  every bookkeeping result, and the full guidance-pair configuration on every
+  row (all 4,096 prefill rows of the tensor-core path);
 * edge cases: empty passes, lanes without rows, empty visible sets, frozen
   writes, clamped channel counts, fold gaps, other head sizes, page sizes
   and fp32.
@@ -83,6 +84,16 @@ def test_full_size_configuration_sampled(name):
         # decode passes of the guidance scenario: every row (one per lane)
     gpu, orc = _run_both(sc, rows)
     compare_scenario(sc, gpu, orc, rows)
+
+
+def test_full_size_guidance_prefill_every_row():
+    """The full guidance-pair configuration (64 lanes x 64 prefill rows on a
+    shared 1,024-slot prefix, then 16 decode passes) with every row of every
+    pass recomputed by the oracle: all 4,096 prefill rows of the tensor-core
+    path, not a sample."""
+    sc = W.FULL["guidance_pairs"](0)
+    gpu, orc = _run_both(sc)
+    compare_scenario(sc, gpu, orc)
 
 
 VARIANTS = {
