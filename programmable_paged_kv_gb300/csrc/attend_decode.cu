@@ -410,6 +410,8 @@ static cudaError_t launch_dec_nq(const pie_fwd_plan_t& p, const void* q_rot, con
 cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
                                  const void* v_pool, const uint32_t* mask_words,
                                  uint32_t* status, cudaStream_t s) {
+  if (decode_mma_supported(p))
+    return launch_attend_decode_mma(p, q_rot, k_pool, v_pool, mask_words, status, s);
   const bool bf = p.desc.dtype == PIE_BF16;
   if (p.desc.head_dim == 128)
     return bf ? launch_dec_nq<__nv_bfloat16, 128>(p, q_rot, k_pool, v_pool, mask_words, status, s)

@@ -180,6 +180,13 @@ cudaError_t launch_fold(const pie_fwd_plan_t& p, int32_t* frozen_len, const int3
 cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
                                  const void* v_pool, const uint32_t* mask_words,
                                  uint32_t* status, cudaStream_t s);
+// the tensor-core (warp-level MMA) variant of the split-KV kernel, for bf16
+// pools with head_dim 128; launch_attend_decode takes it when supported
+bool decode_mma_supported(const pie_fwd_plan_t& p);
+cudaError_t launch_attend_decode_mma(const pie_fwd_plan_t& p, const void* q_rot,
+                                     const void* k_pool, const void* v_pool,
+                                     const uint32_t* mask_words, uint32_t* status,
+                                     cudaStream_t s);
 cudaError_t launch_attend_tc(const pie_fwd_plan_t& p, const void* q_rot, const void* k_pool,
                              const void* v_pool, const uint32_t* mask_words, void* out_readout,
                              float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
