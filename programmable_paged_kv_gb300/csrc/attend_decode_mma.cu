@@ -8,17 +8,19 @@
 // once for the NQ (2, 4 or 8) query vectors of a GQA group.  Computing those
 // few dot products with scalar FMAs costs about 57 warp instructions per
 // (slot, kv head), enough to keep the kernel short of the copy bandwidth, so
-// here each compute warp takes its 16 slots of a 64-slot stage with
-//   * S = Q K^T as 16 x 8 x 16 bf16 MMAs (the query vectors are the rows of
-//     A, padded to 16 with zeros; two 8-slot column tiles, eight 16-wide
-//     steps over d), K fragments read with ldmatrix;
-//   * the online softmax on the accumulator fragments: each row's 16 scores
-//     sit in the four lanes of its quad (two shuffles for the maximum), and
-//     the running maximum used for the exponent only moves when a tile's
-//     maximum exceeds it by more than 2^8, so the output is rarely rescaled;
-//   * O += P V as 16 MMAs, P (bf16) taken straight from the score fragments
-//     as the A operand, V fragments read with ldmatrix.trans.
-// That is about 100 warp instructions per warp and stage where the scalar
+// here each compute warp takes its 16 slots of a 64-slot stage with 16 x 8
+// x 16 bf16 MMAs, both products transposed so that the (up to 8) query
+// vectors are the MMA's 8 columns and no row is padding:
+//   * S^T = K Q^T: eight MMAs over d, K fragments read with ldmatrix;
+//   * the online softmax on the accumulator fragments: each query's 16
+//     scores sit in the 8 lanes of its column (three shuffles for the
+//     maximum), and the running maximum used for the exponent only moves
+//     when a unit's maximum exceeds it by more than 2^8, so the output is
+//     rarely rescaled;
+//   * O^T += V^T P^T: eight MMAs, one per 16-wide tile of d, V fragments read
+//     with ldmatrix.trans; the probabilities (bf16) become the B operand by
+//     an in-register 8 x 8 transpose (movmatrix) of the score fragments.
+// That is about 60 warp instructions per warp and stage where the scalar
 // kernel needs about 900.  The fragments need K and V rows in shared memory
 // without bank conflicts between slots, so the producer warp copies each
 // (page, kv head) block as two 2-D tensor boxes of P rows x 128 bytes (one
@@ -57,19 +59,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// D[g][2t..2t+1] += A[g][.] B[.][2t..2t+1] for a 16 x 8 x 16 bf16 MMA whose
-// A rows 8..15 are zero (a1 = a3 = 0): only the accumulators of rows 0..7
-// are kept; those of rows 8..15 stay zero and are discarded.
-__device__ __forceinline__ void mma_top(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0,
-                                        uint32_t b1) {
-  float z0, z1;
+// D (16 x 8, fp32) += A (16 x 16, bf16) B (16 x 8, bf16), fragments in the
+// warp-level MMA layout
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %10, %10};"
-      : "+f"(d0), "+f"(d1), "=f"(z0), "=f"(z1)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-  (void)z0;
-  (void)z1;
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// the transpose of an 8 x 8 matrix of 16-bit elements held one pair per lane
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -162,28 +167,46 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
   }
 
   // ---------------- compute warps ---------------------------------------------
-  const int g = lane >> 2, t = lane & 3;  // fragment row (query vector) and column pair
-  const bool valid_q = g < nqv;
-  const int qv = valid_q ? g : 0;
-  const int row = it.row0 + qv / G, head = it.kv_head * G + qv % G;
-  const int slot_lim = valid_q ? m.slots[row] : -1;
-  const uint32_t* mrow = (mask_words && valid_q) ? mask_words + m.mask_word_indptr[row] : nullptr;
-  // A fragments of Q (rows 0..7; rows 8..15 are zero): a0 = Q[g][16k + 2t, +1],
-  // a2 = Q[g][16k + 2t + 8, +9]
-  uint32_t qa[8][2];
+  // Fragments (g = lane / 4, t = lane % 4).  Both products are taken
+  // transposed, so that the query vectors are the 8 columns of the MMA and no
+  // row is padding:
+  //   S^T (16 slots x 8 queries) = K (16 slots x 128 d) Q^T: lane holds
+  //     S^T[slot g][q 2t, 2t+1] and S^T[slot g + 8][q 2t, 2t+1];
+  //   O^T (16 d x 8 queries) += V^T (16 d x 16 slots) P^T, for each of the
+  //     eight 16-wide tiles of d: lane holds O^T[d g][q 2t, 2t+1] and
+  //     O^T[d g + 8][q 2t, 2t+1] of its tile.
+  // So each lane keeps the online softmax of queries 2t and 2t + 1; a
+  // query's 16 scores of a unit sit in the 8 lanes of its column pair.
+  const int g = lane >> 2, t = lane & 3;
+  // B fragments of Q^T: b0 = Q[g][16k + 2t, +1], b1 = Q[g][16k + 2t + 8, +9]
+  uint32_t qb[8][2];
   {
+    const bool vq = g < nqv;
+    const int row = it.row0 + (vq ? g : 0) / G, head = it.kv_head * G + (vq ? g : 0) % G;
     const uint32_t* qp =
         reinterpret_cast<const uint32_t*>(q_rot + (int64_t(row) * Hq + head) * D) + t;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      qa[k][0] = valid_q ? qp[8 * k] : 0u;
-      qa[k][1] = valid_q ? qp[8 * k + 4] : 0u;
+      qb[k][0] = vq ? qp[8 * k] : 0u;
+      qb[k][1] = vq ? qp[8 * k + 4] : 0u;
     }
   }
-  float o[16][2];  // O[g][8 n + 2t, +1]
+  // this lane's two query vectors 2t + i: validity, causal limit, mask row
+  bool valid_q[2];
+  int slot_lim[2];
+  const uint32_t* mrow[2];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = 0.f;
-  float m_used = -INFINITY, l_part = 0.f;  // l_part: this lane's share of the row sum
+  for (int i = 0; i < 2; ++i) {
+    const int qv = 2 * t + i;
+    valid_q[i] = qv < nqv;
+    const int row = it.row0 + (valid_q[i] ? qv : 0) / G;
+    slot_lim[i] = valid_q[i] ? m.slots[row] : -1;
+    mrow[i] = (mask_words && valid_q[i]) ? mask_words + m.mask_word_indptr[row] : nullptr;
+  }
+  float o[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_used[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
   const uint32_t ring_s = smem_u32(ring);
   // ldmatrix row addresses: lane i serves row i & 7 of matrix i >> 3
   const int mi = lane >> 3, mr = lane & 7;
@@ -213,57 +236,75 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
         fence_proxy_async_smem();  // the stage is later rewritten by the copy engine
         __syncwarp();
       }
-      // ---- S = Q K^T: column tiles of 8 slots (n = 0, 1); scores of row g at
-      // unit slots 2t, 2t + 1 (x[0], x[1]) and 8 + 2t, 9 + 2t (x[2], x[3])
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K Q^T; A matrices: (slots 0-7, d chunk 2k), (8-15, 2k),
+      // (0-7, 2k+1), (8-15, 2k+1)
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        // matrices: (slots 0-7, d chunk 2k), (0-7, 2k+1), (8-15, 2k), (8-15, 2k+1)
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(dm::chunk_addr(kbase, unit + (mi >> 1) * 8 + mr, 2 * k + (mi & 1)), b0, b1, b2, b3);
-        mma_top(x[0], x[1], qa[k][0], qa[k][1], b0, b1);
-        mma_top(x[2], x[3], qa[k][0], qa[k][1], b2, b3);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(dm::chunk_addr(kbase, unit + (mi & 1) * 8 + mr, 2 * k + (mi >> 1)), a0, a1, a2, a3);
+        dm::mma16816(c, a0, a1, a2, a3, qb[k][0], qb[k][1]);
       }
-      const uint32_t word = mrow ? (mrow[unit_base >> 5] >> (unit_base & 31)) : ~0u;
+      // c[e]: slot g + 8 (e >> 1) of the unit, query 2t + (e & 1)
+      uint32_t word[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) word[i] = mrow[i] ? (mrow[i][unit_base >> 5] >> (unit_base & 31)) : ~0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int cs = (e >> 1) * 8 + 2 * t + (e & 1);  // slot within the unit
-        const bool vis = valid_q && cs < nvalid &&
-                         (mrow ? ((word >> cs) & 1u) != 0 : unit_base + cs <= slot_lim);
-        x[e] = vis ? x[e] : -INFINITY;
+        const int cs = g + 8 * (e >> 1), i = e & 1;
+        const bool vis = valid_q[i] && cs < nvalid &&
+                         (mrow[i] ? ((word[i] >> cs) & 1u) != 0 : unit_base + cs <= slot_lim[i]);
+        c[e] = vis ? c[e] : -INFINITY;
       }
-      float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      mt *= scale_log2;  // scale > 0: the maximum commutes with it
-      float m_new = m_used;
-      if (m_used == -INFINITY || mt > m_used + 8.f) m_new = fmaxf(m_used, mt);
-      if (__any_sync(0xffffffffu, m_new != m_used)) {
-        const float alpha = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
+      float mt[2] = {fmaxf(c[0], c[2]), fmaxf(c[1], c[3])};
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          o[n][0] *= alpha;
-          o[n][1] *= alpha;
-        }
-        l_part *= alpha;
-        m_used = m_new;
+      for (int off = 4; off < 32; off <<= 1) {
+        mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], off));
+        mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xffffffffu, mt[1], off));
       }
-      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+      float m_new[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float mti = mt[i] * scale_log2;  // scale > 0: the maximum commutes with it
+        m_new[i] = m_used[i];
+        if (m_used[i] == -INFINITY || mti > m_used[i] + 8.f) m_new[i] = fmaxf(m_used[i], mti);
+      }
+      if (__any_sync(0xffffffffu, m_new[0] != m_used[0] || m_new[1] != m_used[1])) {
+        float alpha[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          alpha[i] = (m_new[i] == m_used[i]) ? 1.f : ex2(m_used[i] - m_new[i]);
+          l_part[i] *= alpha[i];
+          m_used[i] = m_new[i];
+        }
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          o[n][0] *= alpha[0];
+          o[n][1] *= alpha[1];
+          o[n][2] *= alpha[0];
+          o[n][3] *= alpha[1];
+        }
+      }
+      const float neg_m[2] = {m_used[0] == -INFINITY ? 0.f : -m_used[0],
+                              m_used[1] == -INFINITY ? 0.f : -m_used[1]};
       float p[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = ex2(fmaf(x[e], scale_log2, neg_m));
-      l_part += (p[0] + p[1]) + (p[2] + p[3]);
-      // P as the A operand of P V: a0 = P[g][2t, +1], a2 = P[g][8 + 2t, +1]
-      const uint32_t pa0 = dm::pack_bf16(p[0], p[1]), pa2 = dm::pack_bf16(p[2], p[3]);
-      // ---- O += P V: output column tiles n = 2j, 2j + 1 (8 d each)
+      for (int e = 0; e < 4; ++e) p[e] = ex2(fmaf(c[e], scale_log2, neg_m[e & 1]));
+      l_part[0] += p[0] + p[2];
+      l_part[1] += p[1] + p[3];
+      // P^T rows (slots) g and g + 8 as two 8 x 8 bf16 matrices, transposed
+      // in registers into the B fragments of P^T: b0 = P[g][2t, 2t+1],
+      // b1 = P[g][8 + 2t, 9 + 2t]
+      const uint32_t pb0 = dm::movmatrix_t(dm::pack_bf16(p[0], p[1]));
+      const uint32_t pb1 = dm::movmatrix_t(dm::pack_bf16(p[2], p[3]));
+      // ---- O^T += V^T P^T; A matrices (ldmatrix.trans of V rows): (slots 0-7,
+      // d chunk 2n), (0-7, 2n+1), (8-15, 2n), (8-15, 2n+1)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        // matrices: (slots 0-7, d chunk 2j), (8-15, 2j), (0-7, 2j+1), (8-15, 2j+1)
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(dm::chunk_addr(vbase, unit + (mi & 1) * 8 + mr, 2 * jj + (mi >> 1)), b0, b1, b2,
-                  b3);
-        mma_top(o[2 * jj][0], o[2 * jj][1], pa0, pa2, b0, b1);
-        mma_top(o[2 * jj + 1][0], o[2 * jj + 1][1], pa0, pa2, b2, b3);
+      for (int n = 0; n < 8; ++n) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(dm::chunk_addr(vbase, unit + (mi >> 1) * 8 + mr, 2 * n + (mi & 1)), a0, a1, a2,
+                  a3);
+        dm::mma16816(o[n], a0, a1, a2, a3, pb0, pb1);
       }
     }
     __syncwarp();
@@ -273,22 +314,31 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
 
   // ---- merge the 4 warps' states (the ring is free: every stage issued was
   // consumed, so no copy is in flight) and write the item's partials
-  float l_row = l_part;
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+  float l_q[2] = {l_part[0], l_part[1]};
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l_q[0] += __shfl_xor_sync(0xffffffffu, l_q[0], off);
+    l_q[1] += __shfl_xor_sync(0xffffffffu, l_q[1], off);
+  }
   asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
   float* mw = reinterpret_cast<float*>(ring);  // [WARPS][NQ]
   float* lw = mw + WARPS * NQ;                 // [WARPS][NQ]
   float* ow = lw + WARPS * NQ;                 // [WARPS][NQ][D]
-  if (g < NQ) {
-    if (t == 0) {
-      mw[warp * NQ + g] = m_used;
-      lw[warp * NQ + g] = l_row;
-    }
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<float2*>(ow + (warp * NQ + g) * D + 8 * n + 2 * t) =
-          make_float2(o[n][0], o[n][1]);
+  for (int i = 0; i < 2; ++i) {
+    const int q = 2 * t + i;
+    if (q < NQ) {
+      if (g == 0) {
+        mw[warp * NQ + q] = m_used[i];
+        lw[warp * NQ + q] = l_q[i];
+      }
+      float* orow = ow + (warp * NQ + q) * D;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        orow[16 * n + g] = o[n][i];
+        orow[16 * n + g + 8] = o[n][2 + i];
+      }
+    }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
   for (int idx = threadIdx.x; idx < NQ * D; idx += WARPS * 32) {
@@ -310,7 +360,6 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
     if (cc == 0) m.part_ml[it.part_base + qq] = make_float2(M, Ls);
   }
 }
-
 template <int NQ>
 static cudaError_t launch_nq(const pie_fwd_plan_t& p, const void* q_rot,
                              const uint32_t* mask_words, uint32_t* status, const CUtensorMap& km,
