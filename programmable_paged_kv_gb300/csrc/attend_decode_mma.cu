@@ -24,8 +24,8 @@
 // kernel needs about 900.  The fragments need K and V rows in shared memory
 // without bank conflicts between slots, so the producer warp copies each
 // (page, kv head) block as two 2-D tensor boxes of P rows x 128 bytes (one
-// per half of d) with the 128-byte swizzle; with two CTAs per SM, each with
-// a three-stage ring, those copies stream at the copy bandwidth.
+// per half of d) with the 128-byte swizzle; with three CTAs per SM, each with
+// a two-stage ring, those copies stream at the copy bandwidth.
 // Each work item writes one partial (max, sum, unnormalised output) per query
 // vector; the combine kernel (combine.cu) merges an item's chunks.  Every wait
 // is bounded in time.
@@ -42,8 +42,9 @@ constexpr int WARPS = 4;                           // compute warps (+1 producer
 constexpr int THREADS = (WARPS + 1) * 32;
 constexpr int HALF_BYTES = kStageSlots * 128;      // one half of d of a stage's K (or V): 8 KB
 constexpr int STAGE_BYTES = 4 * HALF_BYTES;        // K halves, then V halves: 32 KB
-constexpr int STAGES = 3;                          // a 96 KB ring: two CTAs per SM
-constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 2 * STAGES * 8;  // + alignment + barriers
+constexpr int STAGES = 2;                          // a 64 KB ring: three CTAs per SM
+constexpr int Q_BYTES = 8 * D * 2;                 // the item's query vectors (8 rows), swizzled
+constexpr int SMEM = STAGES * STAGE_BYTES + Q_BYTES + 1024 + 2 * STAGES * 8;  // + align + barriers
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -91,7 +92,7 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int r, int c) {
 }  // namespace dm
 
 template <int NQ>
-__global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
+__global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
     DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const __nv_bfloat16* q_rot,
     const uint32_t* mask_words, uint32_t* status, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap) {
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * STAGE_BYTES);
+  uint8_t* qs = ring + STAGES * STAGE_BYTES;  // query vector q, 16-byte chunk c at q * 256 + (c ^ q) * 16
+  uint64_t* full = reinterpret_cast<uint64_t*>(qs + Q_BYTES);
   uint64_t* empty = full + STAGES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -178,19 +180,21 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
   // So each lane keeps the online softmax of queries 2t and 2t + 1; a
   // query's 16 scores of a unit sit in the 8 lanes of its column pair.
   const int g = lane >> 2, t = lane & 3;
-  // B fragments of Q^T: b0 = Q[g][16k + 2t, +1], b1 = Q[g][16k + 2t + 8, +9]
-  uint32_t qb[8][2];
+  // the query vectors into shared memory (zeros past the item's), 16 bytes
+  // per thread, chunks XOR-swizzled by the row so that ldmatrix reads of the
+  // eight rows hit distinct banks; the B fragments of Q^T are read from there
+  // at every stage (b0 = Q[g][16k + 2t, +1], b1 = Q[g][16k + 2t + 8, +9])
   {
-    const bool vq = g < nqv;
-    const int row = it.row0 + (vq ? g : 0) / G, head = it.kv_head * G + (vq ? g : 0) % G;
-    const uint32_t* qp =
-        reinterpret_cast<const uint32_t*>(q_rot + (int64_t(row) * Hq + head) * D) + t;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      qb[k][0] = vq ? qp[8 * k] : 0u;
-      qb[k][1] = vq ? qp[8 * k + 4] : 0u;
+    const int qv = threadIdx.x >> 4, ch = threadIdx.x & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (qv < nqv) {
+      const int row = it.row0 + qv / G, head = it.kv_head * G + qv % G;
+      v = *reinterpret_cast<const uint4*>(q_rot + (int64_t(row) * Hq + head) * D + ch * 8);
     }
+    *reinterpret_cast<uint4*>(qs + qv * 256 + ((ch ^ qv) << 4)) = v;
   }
+  asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
+  const uint32_t qs_s = smem_u32(qs);
   // this lane's two query vectors 2t + i: validity, causal limit, mask row
   bool valid_q[2];
   int slot_lim[2];
@@ -240,10 +244,19 @@ __global__ void __launch_bounds__(dm::THREADS, 2) attend_decode_mma_kernel(
       // (0-7, 2k+1), (8-15, 2k+1)
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(dm::chunk_addr(kbase, unit + (mi & 1) * 8 + mr, 2 * k + (mi >> 1)), a0, a1, a2, a3);
-        dm::mma16816(c, a0, a1, a2, a3, qb[k][0], qb[k][1]);
+      for (int kk = 0; kk < 4; ++kk) {
+        // Q^T fragments of steps 2kk and 2kk + 1: matrices (queries 0-7, chunk 4kk + mi)
+        uint32_t b[4];
+        const int qc = 4 * kk + mi;
+        ldsm_x4(qs_s + mr * 256 + ((qc ^ mr) << 4), b[0], b[1], b[2], b[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * kk + h;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(dm::chunk_addr(kbase, unit + (mi & 1) * 8 + mr, 2 * k + (mi >> 1)), a0, a1, a2,
+                  a3);
+          dm::mma16816(c, a0, a1, a2, a3, b[2 * h], b[2 * h + 1]);
+        }
       }
       // c[e]: slot g + 8 (e >> 1) of the unit, query 2t + (e & 1)
       uint32_t word[2];
