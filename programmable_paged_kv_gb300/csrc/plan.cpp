@@ -391,17 +391,25 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
         H.comb.push_back(CombEntry{static_cast<int32_t>(part), direct ? -1 : nchunks,
                                    use_tc ? stride * H.tc_nt : stride, b0, mblk, 0, 0, 0});
         if (!direct) ++H.num_comb_merge;
-        for (int c = 0; c < nchunks; ++c) {
-          const int kb = c * chunk, ke = std::min(ext, kb + chunk);
-          if (use_tc) {
-            const int32_t blk = block_of_row.empty() ? -1 : block_of_row[b0];
+        if (use_tc) {
+          const int32_t blk = block_of_row.empty() ? -1 : block_of_row[b0];
+          for (int c = 0; c < nchunks; ++c) {
+            const int kb = c * chunk, ke = std::min(ext, kb + chunk);
             H.tc.push_back(TcItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part),
                                   direct ? 1 : 0, blk, c, nchunks, 0});
             part += direct ? 0 : stride * H.tc_nt;
-          } else {
-            H.dec.push_back(DecItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part), 0});
-            part += stride;
           }
+        } else {
+          // the unit's chunks written in place (a decode batch has thousands)
+          const size_t base = H.dec.size();
+          H.dec.resize(base + nchunks);
+          DecItem* di = H.dec.data() + base;
+          for (int c = 0; c < nchunks; ++c) {
+            const int kb = c * chunk;
+            di[c] = DecItem{l, g, b0, b1 - b0, kb, std::min(ext, kb + chunk),
+                            static_cast<int32_t>(part + int64_t(c) * stride), 0};
+          }
+          part += int64_t(nchunks) * stride;
         }
       }
     }
