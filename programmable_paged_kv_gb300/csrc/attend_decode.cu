@@ -412,6 +412,9 @@ cudaError_t launch_attend_decode(const pie_fwd_plan_t& p, const void* q_rot, con
                                  uint32_t* status, cudaStream_t s) {
   if (decode_mma_supported(p))
     return launch_attend_decode_mma(p, q_rot, k_pool, v_pool, mask_words, status, s);
+  // items that walk compacted lists are only planned for passes the kernel
+  // above takes
+  if (p.dec_lists) return cudaErrorNotSupported;
   const bool bf = p.desc.dtype == PIE_BF16;
   if (p.desc.head_dim == 128)
     return bf ? launch_dec_nq<__nv_bfloat16, 128>(p, q_rot, k_pool, v_pool, mask_words, status, s)

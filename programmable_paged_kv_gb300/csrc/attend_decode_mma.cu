@@ -26,6 +26,12 @@
 // (page, kv head) block as two 2-D tensor boxes of P rows x 128 bytes (one
 // per half of d) with the 128-byte swizzle; with three CTAs per SM, each with
 // a two-stage ring, those copies stream at the copy bandwidth.
+// In a masked pass an item walks its chunk of the compacted list of the slots
+// its rows see (Attention masks; built by the mask pre-pass): the producer
+// copies the listed whole pages of a window-like list the same way, or the
+// listed rows of a scattered list four at a time (tile::gather4 over one-row
+// boxes), and the rows' visibility comes from their mask words re-expressed
+// over the list.
 // Each work item writes one partial (max, sum, unnormalised output) per query
 // vector; the combine kernel (combine.cu) merges an item's chunks.  Every wait
 // is bounded in time.
@@ -94,8 +100,9 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int r, int c) {
 template <int NQ>
 __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
     DevMeta m, int Hq, int Hkv, int G, int P, float scale_log2, const __nv_bfloat16* q_rot,
-    const uint32_t* mask_words, uint32_t* status, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap) {
+    const uint32_t* mask_words, int list_tile, uint32_t* status,
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __grid_constant__ CUtensorMap kgmap, const __grid_constant__ CUtensorMap vgmap) {
   using namespace dm;
   static_assert(NQ <= 8, "query vectors of an item fill at most the top 8 MMA rows");
   extern __shared__ uint8_t smem_raw[];
@@ -118,7 +125,23 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
   grid_dep_wait();
   grid_dep_launch();
   const DecItem it = m.dec_items[blockIdx.x];
-  const int kb = it.kv_begin, ke = it.kv_end;
+  int kb = it.kv_begin, ke = it.kv_end;
+  // a listed item: chunk kv_begin of the kv_end provisioned ones of its
+  // block's list, in whole list tiles (the split the combine step computes the
+  // same way); chunks past the list's share write nothing
+  const bool listed = it.block >= 0;
+  MaskBlock mb{0, 0, 0, 0, 0, 0, 0, 0};
+  bool page_list = false;
+  if (listed) {
+    mb = m.mblocks[it.block];
+    const int U = m.list_len[it.block];
+    const int tiles = (U + list_tile - 1) / list_tile;
+    const int nch = masked_chunks(tiles, it.kv_end, *m.mask_tiles, Hkv, m.num_sms * kDecListWaves);
+    if (it.kv_begin >= nch) return;
+    kb = (it.kv_begin * tiles / nch) * list_tile;
+    ke = min(U, ((it.kv_begin + 1) * tiles / nch) * list_tile);
+    page_list = m.list_mode[it.block] != 0;
+  }
   const int nstages = ke > kb ? (ke - kb + kStageSlots - 1) / kStageSlots : 0;
   const int nqv = it.nrows * G;
   const uint64_t wait_ns = m.test_wait_us ? uint64_t(m.test_wait_us) * 1000ull : kWaitLimitNs;
@@ -131,11 +154,46 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
     // A page id outside the pool is not copied and sets PIE_STATUS_BOUNDS.
     const uint64_t pol = policy_evict_first();
     const int32_t* pages = m.page_ids + m.page_indptr[it.lane];
+    // a listed slot's row in the pools viewed as [rows][d], less kv_head * P
+    const int32_t* lrow = listed ? m.lrow + mb.list_off : nullptr;
+    if (listed && !page_list) {
+      // ---- a scattered list: lane i gathers rows 4(i % 16) .. 4(i % 16) + 3
+      // of every stage from K (i < 16) or V, both halves of d; rows past the
+      // last listed one repeat it (finite data, never visible)
+      const int gi = lane & 15, tv = lane >> 4, hrow = it.kv_head * P;
+      for (int s = 0; s < nstages; ++s) {
+        if (s == m.test_stall - 1) break;
+        const int st = s % STAGES, use = s / STAGES;
+        if (use > 0 && !mbar_wait_ns(&empty[st], (use - 1) & 1, wait_ns)) {
+          if (lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
+          break;
+        }
+        const int sb = kb + s * kStageSlots;
+        const int n = min(kStageSlots, ke - sb);
+        const int ng = (n + 3) >> 2;
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(ng) * 4u * 128u * 2u * 2u);
+        __syncwarp();
+        if (gi < ng) {
+          int y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = lrow[sb + min(4 * gi + e, n - 1)] + hrow;
+          uint8_t* dst = ring + st * STAGE_BYTES + tv * 2 * HALF_BYTES + 4 * gi * 128;
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+            tc::tma_gather4(dst + a * HALF_BYTES, tv ? &vgmap : &kgmap, 64 * a, y[0], y[1], y[2],
+                            y[3], &full[st], pol);
+        }
+      }
+      return;
+    }
+    // whole pages: the lane's own, or the listed pages of a window-like list
+    // (page i of the list at positions i * P ..)
     const int c = lane & 3, pi = lane >> 2;
     auto page_of = [&](int s) -> int64_t {
       const int sb = kb + s * kStageSlots;
       const int p0 = sb / P, p1 = (min(sb + kStageSlots, ke) - 1) / P;
-      return pi <= p1 - p0 ? int64_t(pages[p0 + pi]) : 0;
+      if (pi > p1 - p0) return 0;
+      return listed ? int64_t(lrow[(p0 + pi) * P]) / (int64_t(Hkv) * P) : int64_t(pages[p0 + pi]);
     };
     int64_t pid = nstages > 0 ? page_of(0) : 0;
     for (int s = 0; s < nstages; ++s) {
@@ -205,7 +263,12 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
     valid_q[i] = qv < nqv;
     const int row = it.row0 + (valid_q[i] ? qv : 0) / G;
     slot_lim[i] = valid_q[i] ? m.slots[row] : -1;
-    mrow[i] = (mask_words && valid_q[i]) ? mask_words + m.mask_word_indptr[row] : nullptr;
+    // mask words: the row's own over the lane's slots, or, for a listed item,
+    // re-expressed over its block's list
+    mrow[i] = !valid_q[i] ? nullptr
+              : listed    ? m.cmask + mb.cmask_off + int64_t(row - mb.r0) * mb.nw
+              : mask_words ? mask_words + m.mask_word_indptr[row]
+                           : nullptr;
   }
   float o[8][4];
 #pragma unroll
@@ -215,9 +278,19 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
   // ldmatrix row addresses: lane i serves row i & 7 of matrix i >> 3
   const int mi = lane >> 3, mr = lane & 7;
   bool timed_out = false;
+  // the rows' mask words of this warp's unit, fetched one stage ahead
+  uint32_t wnext[2] = {~0u, ~0u};
+  auto load_words = [&](int ss) {
+    const int ub = kb + ss * kStageSlots + warp * kWarpSlots;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) wnext[i] = (mrow[i] && ub < ke) ? (mrow[i][ub >> 5] >> (ub & 31)) : ~0u;
+  };
+  if (nstages > 0) load_words(0);
 
   for (int s = 0; s < nstages; ++s) {
     const int st = s % STAGES;
+    const uint32_t word[2] = {wnext[0], wnext[1]};
+    if (s + 1 < nstages) load_words(s + 1);
     if (!mbar_wait_ns(&full[st], (s / STAGES) & 1, wait_ns)) {
       timed_out = true;
       break;
@@ -259,9 +332,6 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
         }
       }
       // c[e]: slot g + 8 (e >> 1) of the unit, query 2t + (e & 1)
-      uint32_t word[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) word[i] = mrow[i] ? (mrow[i][unit_base >> 5] >> (unit_base & 31)) : ~0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int cs = g + 8 * (e >> 1), i = e & 1;
@@ -376,7 +446,8 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
 template <int NQ>
 static cudaError_t launch_nq(const pie_fwd_plan_t& p, const void* q_rot,
                              const uint32_t* mask_words, uint32_t* status, const CUtensorMap& km,
-                             const CUtensorMap& vm, cudaStream_t s) {
+                             const CUtensorMap& vm, const CUtensorMap& kgm, const CUtensorMap& vgm,
+                             cudaStream_t s) {
   static std::atomic<uint64_t> configured{0};  // per instantiation and device
   cudaError_t e = set_smem_limit(attend_decode_mma_kernel<NQ>, dm::SMEM, configured);
   if (e != cudaSuccess) return e;
@@ -385,7 +456,8 @@ static cudaError_t launch_nq(const pie_fwd_plan_t& p, const void* q_rot,
   return launch_dependent(attend_decode_mma_kernel<NQ>, dim3(p.num_dec_items), dim3(dm::THREADS),
                           dm::SMEM, s, true, m, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
                           p.desc.page_size, p.desc.sm_scale * dm::kLog2e,
-                          static_cast<const __nv_bfloat16*>(q_rot), mask_words, status, km, vm);
+                          static_cast<const __nv_bfloat16*>(q_rot), mask_words,
+                          tc_kv_tile(p.tc_nt), status, km, vm, kgm, vgm);
 }
 
 // bf16 pools with head_dim 128 whose rows (pool pages x kv heads x page
@@ -408,10 +480,17 @@ cudaError_t launch_attend_decode_mma(const pie_fwd_plan_t& p, const void* q_rot,
   const cuuint32_t box[2] = {64, cuuint32_t(P)};
   if (!tc::make_map(&km, k_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
   if (!tc::make_map(&vm, v_pool, 2, dims, str, box)) return cudaErrorInvalidValue;
+  // one-row boxes for the gathers of scattered lists
+  CUtensorMap kgm = km, vgm = vm;
+  if (p.dec_lists) {
+    const cuuint32_t box1[2] = {64, 1};
+    if (!tc::make_map(&kgm, k_pool, 2, dims, str, box1)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&vgm, v_pool, 2, dims, str, box1)) return cudaErrorInvalidValue;
+  }
   switch (p.nq) {
-    case 2: return launch_nq<2>(p, q_rot, mask_words, status, km, vm, s);
-    case 4: return launch_nq<4>(p, q_rot, mask_words, status, km, vm, s);
-    default: return launch_nq<8>(p, q_rot, mask_words, status, km, vm, s);
+    case 2: return launch_nq<2>(p, q_rot, mask_words, status, km, vm, kgm, vgm, s);
+    case 4: return launch_nq<4>(p, q_rot, mask_words, status, km, vm, kgm, vgm, s);
+    default: return launch_nq<8>(p, q_rot, mask_words, status, km, vm, kgm, vgm, s);
   }
 }
 

@@ -83,7 +83,7 @@ __global__ void noalloc_items_kernel(int L, int Hkv, int MC, int nq, int max_kv_
     ext = max(ext, 0);
     const int kb = c * kNoAllocChunk;
     const int ke = max(kb, min(ext, kb + kNoAllocChunk));
-    items[i] = DecItem{l, g, l, 1, kb, ke, i * nq, 0};
+    items[i] = DecItem{l, g, l, 1, kb, ke, i * nq, -1};  // -1: no compacted list
   }
   if (i < L * Hkv) comb[i] = CombEntry{i * MC * nq, MC, nq, i / Hkv, -1, 0, 0, 0};  // block l = row l
   if (i < L) readout[i] = i;

@@ -45,10 +45,13 @@ __global__ void __launch_bounds__(128) combine_kernel(DevMeta m, int Hq, int Hkv
   if (!tables_early) read_tables();
   if (!active || ce.nchunks < 0) return;  // < 0: written directly by the tensor-core kernel
   const int qi = (row - ce.row0) * G + h % G;
-  // a masked tensor-core block uses as many chunks as its list length gives
+  // a masked block uses as many chunks as its list length gives, for as many
+  // waves of items as its kernel's (one on the tensor-core path, three on the
+  // split-KV path)
   const int nch = ce.mblock < 0 ? ce.nchunks
                                 : masked_chunks((m.list_len[ce.mblock] + tc_bn - 1) / tc_bn,
-                                                ce.nchunks, *m.mask_tiles, Hkv, m.num_sms);
+                                                ce.nchunks, *m.mask_tiles, Hkv,
+                                                m.num_sms * ce.waves);
   float o[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) o[e] = 0.f;

@@ -109,7 +109,7 @@ __global__ void loop_step_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int 
     const int ext = ok ? f + 1 : 0;
     const int kb = c * kLoopChunk;
     const int ke = max(kb, min(ext, kb + kLoopChunk));
-    const_cast<DecItem*>(m.dec_items)[i] = DecItem{l, g, l, 1, kb, ke, i * nq, lg};
+    const_cast<DecItem*>(m.dec_items)[i] = DecItem{l, g, l, 1, kb, ke, i * nq, -1};  // no list
     if (g == 0 && c == 0) {
       const_cast<int32_t*>(m.positions)[l] = f;
       const_cast<int32_t*>(m.slots)[l] = ok ? f : -1;  // -1: no slot, nothing is written

@@ -15,22 +15,33 @@ namespace pie {
 // [row0, row0 + nrows) of `lane` that read kv head `kv_head` (nrows * G query
 // vectors, padded to the kernel's NQ), over the slot chunk [kv_begin, kv_end).
 // kv_begin is a multiple of kStageSlots.  Partial softmax state goes to
-// partial slots part_base .. part_base + NQ - 1.
+// partial slots part_base .. part_base + NQ - 1.  In masked passes `block` is
+// the row block whose compacted visible-slot list the item walks (else -1);
+// then kv_begin is the item's chunk and kv_end the chunks provisioned, and the
+// chunks used come from the list's length (masked_chunks).
 struct alignas(16) DecItem {
   int32_t lane, kv_head, row0, nrows;
-  int32_t kv_begin, kv_end, part_base, pad;
+  int32_t kv_begin, kv_end, part_base, block;
 };
+
+// The split-KV kernel keeps three CTAs per SM: a masked unit on it splits its
+// list for two waves of three CTAs per SM (so that each CTA's start-up -- its
+// item, the list length, the first copies -- partly runs under other CTAs'
+// streaming; one wave, three or five measured slower), where a tensor-core
+// unit splits for one wave of one.
+constexpr int kDecListWaves = 6;
 
 // How the combine step finds the partials of a row block (the rows one work
 // item serves) and kv head: row r of the block, q head h, chunk c lives at
 // part_base + c * stride + (r - row0) * G + (h % G).  nchunks < 0 marks blocks
 // whose outputs the tensor-core kernel wrote directly (nothing to combine).
-// mblock >= 0 marks a masked row block on the tensor-core path: nchunks is
-// then only the chunks provisioned, and the chunks used come from its list
-// length (masked_chunks).
+// mblock >= 0 marks a masked row block: nchunks is then only the chunks
+// provisioned, and the chunks used come from its list length (masked_chunks
+// for `waves` waves of items: 1 on the tensor-core path, kDecListWaves on the
+// split-KV path).
 struct alignas(16) CombEntry {
   int32_t part_base, nchunks, stride, row0;
-  int32_t mblock, pad0, pad1, pad2;
+  int32_t mblock, waves, pad1, pad2;
 };
 
 // Work item of the tensor-core attention kernel: up to NT tiles of 128 query
@@ -49,7 +60,7 @@ struct alignas(16) TcItem {
   int32_t block, chunk, nchunks, pad;
 };
 
-// A row block of a masked pass on the tensor-core path: rows [r0, r1) of
+// A row block of a masked pass: rows [r0, r1) of
 // `lane`, whose masks cover nw = ceil(kv_len / 32) words each.  The mask
 // pre-pass writes, at these offsets of the scratch arrays, the block's
 // compacted list of slots visible to at least one of its rows (list_off, up to
@@ -112,7 +123,7 @@ struct DevMeta {
   const int32_t* row_block;         // [N] row block of each row
   float* part_o;                    // [num_part_slots][d] unnormalised
   float2* part_ml;                  // [num_part_slots] (max, sum), log2 domain
-  const MaskBlock* mblocks;         // [num_mblocks] (masked passes with tensor-core lanes)
+  const MaskBlock* mblocks;         // [num_mblocks] (masked passes whose lanes walk lists)
   int32_t* list;                    // compacted visible-slot lists (scratch)
   int32_t* lrow;                    // page * Hkv * P + slot % P of each listed slot: its
                                     //   row in the pools viewed as [rows][d] is this
@@ -157,7 +168,9 @@ struct pie_fwd_plan {
   int32_t num_dec_items;
   int32_t num_tc_items;
   int32_t tc_nt;             // query tiles per tensor-core item (1 or 2)
-  int32_t num_mblocks;       // masked row blocks (0 unless masked tensor-core lanes)
+  int32_t num_mblocks;       // masked row blocks (0 unless some lane walks a list)
+  bool dec_lists;            // some split-KV item walks its block's list (the
+                             // tensor-core split-KV kernel must take the pass)
   int32_t mblock_max_nw;     // largest nw over the masked row blocks
   int32_t mblock_max_rows;   // most rows in a masked row block
   int64_t num_part_slots;

@@ -94,6 +94,7 @@ struct HostPlan {
   int64_t list_total = 0, cmask_total = 0;
   int mblock_max_nw = 0, mblock_max_rows = 0;
   bool has_mask = false, any_channel = false;
+  bool dec_lists = false;  // some split-KV item walks a compacted list
   std::vector<int32_t> row_lane, readout;
   std::vector<float> rope_freq;
   std::vector<DecItem> dec;
@@ -296,15 +297,22 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   const bool tc_ok = D.dtype == PIE_BF16 && D.head_dim == 128 &&
                      kTcTileQueries % G == 0 &&
                      static_cast<int64_t>(M.num_pool_pages) * Hkv * D.page_size <= INT32_MAX;
-  // A masked lane goes to the tensor-core kernel whatever its row count: that
-  // kernel walks the compacted list of the slots its rows see (whole pages of
-  // a window, single rows of a scattered mask), so a masked decode row reads
-  // only what it attends; its padding query rows cost MMA time, which a
-  // decode row's memory-bound work hides.
+  // the tensor-core split-KV kernel (bf16, d 128, 32-bit tensor-copy rows);
+  // the launch takes it under the same condition (decode_mma_supported)
+  const int64_t pool_rows = static_cast<int64_t>(M.num_pool_pages) * Hkv * D.page_size;
+  const bool mma_ok = D.dtype == PIE_BF16 && D.head_dim == 128 && pool_rows > 0 &&
+                      pool_rows <= INT32_MAX;
+  // Lanes with many query vectors per kv head go to the tensor-core kernel.  In
+  // a masked pass both kernels walk the compacted list of the slots a row
+  // block sees (whole pages of a window, single rows of a scattered mask), so a
+  // masked row reads only what it attends; a masked lane the list-walking
+  // kernels cannot take (fp32, d 64) reads its whole range on the scalar
+  // split-KV kernel.
   auto lane_tc = [&](int l) {
     const int n = M.row_indptr[l + 1] - M.row_indptr[l];
-    return tc_ok && n > 0 && (n * G >= kTcMinQueries || H.has_mask);
+    return tc_ok && n > 0 && (n * G >= kTcMinQueries || (H.has_mask && !mma_ok));
   };
+  auto lane_list = [&](int l) { return H.has_mask && (lane_tc(l) || mma_ok); };
   // split-KV items: chunk length from the total work
   int64_t work = 0;
   for (int l = 0; l < L; ++l)
@@ -337,21 +345,25 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
   H.row_block.assign(N, 0);
   H.dec.clear();
   H.tc.clear();
-  // masked passes: tensor-core lanes walk the compacted list of the slots
-  // their row block can see (one list per row block, shared by all kv heads)
+  // masked passes: the list-walking lanes' items walk the compacted list of
+  // the slots their row block can see (one list per row block, shared by all
+  // kv heads)
   H.mblocks.clear();
-  bool any_tc = false;
-  for (int l = 0; l < L; ++l) any_tc = any_tc || lane_tc(l);
-  std::vector<int32_t> block_of_row(H.has_mask && any_tc ? N : 0, -1);
+  bool any_list = false;
+  for (int l = 0; l < L; ++l) any_list = any_list || lane_list(l);
+  std::vector<int32_t> block_of_row(any_list ? N : 0, -1);
   H.list_total = H.cmask_total = 0;
   H.mblock_max_nw = H.mblock_max_rows = 0;
+  H.dec_lists = false;
   if (!block_of_row.empty()) {
     for (int l = 0; l < L; ++l) {
-      if (!lane_tc(l)) continue;
+      if (!lane_list(l)) continue;
       const int r0 = M.row_indptr[l], r1 = M.row_indptr[l + 1];
       const int nw = (M.kv_len[l] + 31) / 32;
-      for (int b0 = r0; b0 < r1; b0 += tc_rows) {
-        const int b1 = std::min(r1, b0 + tc_rows);
+      const int blk_rows = lane_tc(l) ? tc_rows : rows_per_item;
+      H.dec_lists = H.dec_lists || (!lane_tc(l) && r1 > r0);
+      for (int b0 = r0; b0 < r1; b0 += blk_rows) {
+        const int b1 = std::min(r1, b0 + blk_rows);
         block_of_row[b0] = static_cast<int32_t>(H.mblocks.size());
         H.mblocks.push_back(MaskBlock{l, b0, b1, nw, static_cast<int32_t>(H.list_total),
                                       static_cast<int32_t>(H.cmask_total), 0, 0});
@@ -382,38 +394,51 @@ static int build_host_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, H
         chunk = ((ext + nchunks - 1) / nchunks + kTcTileSlots - 1) / kTcTileSlots * kTcTileSlots;
         nchunks = std::max(1, (ext + chunk - 1) / std::max(1, chunk));
       } else {
+        // a listed unit has at least one item: the combine step reads at
+        // least one chunk of every list (an empty list's item writes the
+        // empty state)
         nchunks = (ext + CH - 1) / CH;
+        if (!block_of_row.empty() && block_of_row[b0] >= 0) nchunks = std::max(1, nchunks);
         chunk = CH;
       }
       const bool direct = use_tc && nchunks == 1;
+      const int32_t mblk = block_of_row.empty() ? -1 : block_of_row[b0];
       for (int g = 0; g < Hkv; ++g) {
-        const int32_t mblk = (use_tc && !block_of_row.empty()) ? block_of_row[b0] : -1;
         H.comb.push_back(CombEntry{static_cast<int32_t>(part), direct ? -1 : nchunks,
-                                   use_tc ? stride * H.tc_nt : stride, b0, mblk, 0, 0, 0});
+                                   use_tc ? stride * H.tc_nt : stride, b0, mblk,
+                                   use_tc ? 1 : kDecListWaves, 0, 0});
         if (!direct) ++H.num_comb_merge;
         if (use_tc) {
-          const int32_t blk = block_of_row.empty() ? -1 : block_of_row[b0];
           for (int c = 0; c < nchunks; ++c) {
             const int kb = c * chunk, ke = std::min(ext, kb + chunk);
             H.tc.push_back(TcItem{l, g, b0, b1 - b0, kb, ke, static_cast<int32_t>(part),
-                                  direct ? 1 : 0, blk, c, nchunks, 0});
+                                  direct ? 1 : 0, mblk, c, nchunks, 0});
             part += direct ? 0 : stride * H.tc_nt;
           }
         } else {
-          // the unit's chunks written in place (a decode batch has thousands)
+          // the unit's chunks written in place (a decode batch has thousands);
+          // a listed item names its list block and its chunk of the list
           const size_t base = H.dec.size();
           H.dec.resize(base + nchunks);
           DecItem* di = H.dec.data() + base;
           for (int c = 0; c < nchunks; ++c) {
             const int kb = c * chunk;
-            di[c] = DecItem{l, g, b0, b1 - b0, kb, std::min(ext, kb + chunk),
-                            static_cast<int32_t>(part + int64_t(c) * stride), 0};
+            const int32_t pb = static_cast<int32_t>(part + int64_t(c) * stride);
+            di[c] = mblk >= 0 ? DecItem{l, g, b0, b1 - b0, c, nchunks, pb, mblk}
+                              : DecItem{l, g, b0, b1 - b0, kb, std::min(ext, kb + chunk), pb, -1};
           }
           part += int64_t(nchunks) * stride;
         }
       }
     }
   }
+  // listed split-KV items chunk-major (every unit's first chunk, then every
+  // unit's second, ...): the CTAs in flight spread over all lanes and kv
+  // heads, and the chunks a short list leaves unused come last
+  if (H.dec_lists)
+    std::stable_sort(H.dec.begin(), H.dec.end(), [](const DecItem& a, const DecItem& b) {
+      return (a.block >= 0 ? a.kv_begin : 0) < (b.block >= 0 ? b.kv_begin : 0);
+    });
   // readout positions per row (a row may be read out several times)
   H.ro_indptr.assign(N + 1, 0);
   for (int j = 0; j < H.R; ++j) H.ro_indptr[H.readout[j] + 1]++;
@@ -613,6 +638,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->num_tc_items = static_cast<int32_t>(H.tc.size());
   p->tc_nt = H.tc_nt;
   p->num_mblocks = static_cast<int32_t>(H.mblocks.size());
+  p->dec_lists = H.dec_lists;
   p->mblock_max_nw = H.mblock_max_nw;
   p->mblock_max_rows = H.mblock_max_rows;
   p->num_part_slots = H.num_part_slots;
