@@ -191,9 +191,10 @@ int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_
 
 /* The pass's attention mask, once for every layer ("The forward pass",
  * Attention masks: the mask belongs to the ForwardPass, and every attention
- * layer of the pass applies it).  For the row blocks served by the
- * tensor-core kernel, attention walks a compacted list of the slots some row
- * of the block sees (and each row's mask re-expressed over that list), built
+ * layer of the pass applies it).  For bf16 lanes with head_dim 128 (decode
+ * rows and prefill alike), attention walks, per row block, a compacted list of
+ * the slots some row of the block sees (and each row's mask re-expressed over
+ * that list), built
  * from the mask words and the page table -- data of the pass, not of the
  * layer.  pie_fwd_set_mask builds those lists on `stream` into the plan's
  * workspace and records `mask_words`; every later pie_fwd_attend call on this

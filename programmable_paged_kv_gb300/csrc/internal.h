@@ -85,8 +85,8 @@ int device_sm_count();
 // (two score buffers per query tile and every tile's O share 512 TMEM columns)
 constexpr int tc_kv_tile(int nt) { return nt == 1 ? 128 : 64; }
 
-// Chunks a masked tensor-core unit (row block x kv head) splits its list
-// into: its share of one wave of `sms` items (one per SM), in proportion to its
+// Chunks a masked unit (row block x kv head) splits its list into: its share
+// of one wave of `sms` items (the SMs times the unit's waves), in proportion to its
 // KV tiles among all masked units' (total_tiles counts each row block's tiles
 // once; every block has Hkv units), at least 1 and at most the provisioned
 // items and its tiles.  The kernel and the combine step both use it.
@@ -132,7 +132,7 @@ struct DevMeta {
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
   int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
   int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
-  int32_t num_sms;                  // SMs the masked tensor-core chunks are sized for
+  int32_t num_sms;                  // SMs the masked units' chunks are sized for
   int32_t num_pool_pages;           // page ids at or past it are skipped (PIE_STATUS_BOUNDS)
   int32_t test_stall;               // test hook: 0 none; s + 1: the split-KV producer stops
                                     //   before stage s of every item

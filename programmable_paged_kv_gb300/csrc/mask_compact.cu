@@ -1,4 +1,4 @@
-// Mask pre-pass for masked passes on the tensor-core path (Pie "The forward
+// Mask pre-pass for masked passes on the list-walking kernels (Pie "The forward
 // pass", Attention masks: a row may skip slots it would read under a causal
 // mask -- sliding windows, attention sinks, TOVA-style eviction).
 //
@@ -6,7 +6,8 @@
 // its algorithmic bytes: a window of 4,096 slots in a 32,768-slot working set
 // touches an eighth of the pages, and a TOVA mask that keeps a quarter of the
 // slots touches nearly every page but only a quarter of the slots.  For every
-// row block (the rows one tensor-core item serves) three small kernels build
+// row block (the rows one tensor-core or split-KV item serves) three small
+// kernels build
 //   1. the union of the rows' mask words (bits at or past kv_len cleared);
 //   2. the compacted list of the slots set in the union, ascending, and its
 //      length (and the KV tiles of all blocks' lists, which set how many
@@ -14,9 +15,10 @@
 //   3. each row's mask re-expressed over that list (bit i of a row's word
 //      i/32 = the row sees list[i]), and the pool row of every listed slot
 //      (its page looked up once here, not by every kv head's item).
-// The tensor-core kernel then walks tiles of the list, gathering the K/V
-// rows of those slots, and tests visibility with the re-expressed words
-// exactly as it tests plain mask words.  The union words are kept in
+// The attention kernels then walk tiles of the list, copying the K/V rows of
+// those slots (whole pages when the list is page-granular), and test
+// visibility with the re-expressed words exactly as they test plain mask
+// words.  The union words are kept in
 // the first row of the block's re-expressed mask area until step 3
 // overwrites it.
 
