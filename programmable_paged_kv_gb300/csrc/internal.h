@@ -30,6 +30,12 @@ struct alignas(16) DecItem {
 // streaming; one wave, three or five measured slower), where a tensor-core
 // unit splits for one wave of one.
 constexpr int kDecListWaves = 6;
+// Consecutive items one CTA of the tensor-core split-KV kernel walks, so that
+// an item's start-up runs under the one before: two for the short items of list
+// passes (masked decode 3-5 % faster); one for plain passes, whose longer items
+// gain less than a longer last wave costs (two: the decode batch 3.5 % slower).
+constexpr int kDecItemsPerCta = 1;
+constexpr int kDecListItemsPerCta = 2;
 
 // How the combine step finds the partials of a row block (the rows one work
 // item serves) and kv head: row r of the block, q head h, chunk c lives at
@@ -171,6 +177,8 @@ struct pie_fwd_plan {
   int32_t num_mblocks;       // masked row blocks (0 unless some lane walks a list)
   bool dec_lists;            // some split-KV item walks its block's list (the
                              // tensor-core split-KV kernel must take the pass)
+  int32_t dec_items_per_cta; // consecutive split-KV items one CTA of the
+                             // tensor-core split-KV kernel walks (0 or 1: one)
   int32_t mblock_max_nw;     // largest nw over the masked row blocks
   int32_t mblock_max_rows;   // most rows in a masked row block
   int64_t num_part_slots;

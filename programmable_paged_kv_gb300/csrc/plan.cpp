@@ -639,6 +639,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->tc_nt = H.tc_nt;
   p->num_mblocks = static_cast<int32_t>(H.mblocks.size());
   p->dec_lists = H.dec_lists;
+  p->dec_items_per_cta = H.dec_lists ? kDecListItemsPerCta : kDecItemsPerCta;
   p->mblock_max_nw = H.mblock_max_nw;
   p->mblock_max_rows = H.mblock_max_rows;
   p->num_part_slots = H.num_part_slots;
