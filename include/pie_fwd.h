@@ -387,11 +387,13 @@ int pie_fwd_set_timing_events(void* start_event, void* stop_event);
  * pie_fwd_test_wait_expiry(stage, wait_us) with stage >= 0, every split-KV
  * attention kernel that the calling thread launches (pie_fwd_attend, the
  * decode loop, the no-allocation decode) has its producer warp stop before
- * stage `stage` of every work item -- so no copy of that stage, or of any
- * later one, is ever in flight -- and gives each of its waits `wait_us`
- * microseconds: the compute warps' wait for that stage expires, the kernel
- * sets PIE_STATUS_TIMEOUT, writes whatever partial state it has and returns.
- * Items with fewer stages are not affected.  (-1, 0) turns the hook off.
+ * stage `stage` of a work item -- so no copy of that stage, or of any later
+ * one, is ever in flight (a CTA that walks several items issues nothing for
+ * its later items) -- and gives each of its waits `wait_us` microseconds: the
+ * compute warps' wait for that stage expires, the kernel sets
+ * PIE_STATUS_TIMEOUT, writes whatever partial state it has and returns.
+ * Items with fewer stages that a CTA walks first are not affected.  (-1, 0)
+ * turns the hook off.
  * Errors: PIE_EINVAL for stage < -1, or stage >= 0 with wait_us == 0. */
 int pie_fwd_test_wait_expiry(int32_t stage, uint32_t wait_us);
 
