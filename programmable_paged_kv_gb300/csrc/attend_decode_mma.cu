@@ -50,7 +50,8 @@ constexpr int HALF_BYTES = kStageSlots * 128;      // one half of d of a stage's
 constexpr int STAGE_BYTES = 4 * HALF_BYTES;        // K halves, then V halves: 32 KB
 constexpr int STAGES = 2;                          // a 64 KB ring: three CTAs per SM
 constexpr int Q_BYTES = 8 * D * 2;                 // the item's query vectors (8 rows), swizzled
-constexpr int SMEM = STAGES * STAGE_BYTES + Q_BYTES + 1024 + 2 * STAGES * 8;  // + align + barriers
+constexpr int SMEM = STAGES * STAGE_BYTES + Q_BYTES + 1024 + 2 * STAGES * 8 + 64;  // + align,
+                                                                           // barriers, item queue
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -120,11 +121,22 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
   uint8_t* qs = ring + STAGES * STAGE_BYTES;  // query vector q, 16-byte chunk c at q * 256 + (c ^ q) * 16
   uint64_t* full = reinterpret_cast<uint64_t*>(qs + Q_BYTES);
   uint64_t* empty = full + STAGES;
+  // item queue: the producer hands each item index (or -1: no more) to the
+  // compute warps through two slots; compute warp 0 reads a slot and writes
+  // the decision every compute warp then takes (-2: the wait ran out)
+  uint64_t* item_full = empty + STAGES;
+  uint64_t* item_empty = item_full + 2;
+  int* qidx = reinterpret_cast<int*>(item_empty + 2);
+  int* decision = qidx + 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], WARPS);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&item_full[q], 1);
+      mbar_init(&item_empty[q], 1);
     }
     fence_barrier_init();
   }
@@ -133,10 +145,12 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
   // items may come from a kernel queued just before this one)
   grid_dep_wait();
   grid_dep_launch();
-  // This CTA's items: items_per_cta consecutive ones.  The producer runs its
-  // stages straight through from one item into the next (the ring's stages and
-  // phases continue), so the next item's first copies are in flight while the
-  // compute warps merge the last one.
+  // This CTA's items: taken one by one from the plan's work counter (a
+  // persistent grid), or, without a counter, items_per_cta consecutive ones.
+  // The producer runs its stages straight through from one item into the
+  // next (the ring's stages and phases continue), so the next item's first
+  // copies are in flight while the compute warps merge the last one.
+  int* const work = m.dec_work;
   const int first = blockIdx.x * items_per_cta;
   const int last = min(num_items, first + items_per_cta);
   auto resolve = [&](int idx) {
@@ -182,7 +196,39 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
     const int c = lane & 3, pi = lane >> 2;
     const int gi = lane & 15, tv = lane >> 4;
     int gs = 0;  // stages issued by this CTA so far (ring slot gs % STAGES)
-    for (int idx = first; idx < last; ++idx) {
+    // every way out of the producer counts the CTA done; the last CTA done
+    // sets the counter back to zero for the next launch
+    auto finish = [&]() {
+      if (work && lane == 0) {
+        __threadfence();
+        if (atomicAdd(work + 1, 1) == int(gridDim.x) - 1) {
+          atomicExch(work, 0);
+          atomicExch(work + 1, 0);
+        }
+      }
+    };
+    for (int k = 0;; ++k) {
+      // the next item: from the counter, or the CTA's next fixed one
+      int idx;
+      if (work) {
+        idx = 0;
+        if (lane == 0) idx = atomicAdd(work, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx >= num_items) idx = -1;
+      } else {
+        idx = first + k < last ? first + k : -1;
+      }
+      const int q = k & 1;
+      if (k >= 2 && !mbar_wait_ns(&item_empty[q], ((k >> 1) - 1) & 1, wait_ns)) {
+        if (lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
+        finish();
+        return;
+      }
+      if (lane == 0) {
+        qidx[q] = idx;
+        mbar_arrive(&item_full[q]);  // release: the index is visible to the waiters
+      }
+      if (idx < 0) break;
       const DecRange r = resolve(idx);
       const int32_t* pages = m.page_ids + m.page_indptr[r.it.lane];
       // a listed slot's row in the pools viewed as [rows][d], less kv_head * P
@@ -200,10 +246,14 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
       for (int s = 0; s < r.nstages; ++s, ++gs) {
         // test hook: stop before this stage of the first item (no copy of it,
         // or of anything later, is ever issued)
-        if (s == m.test_stall - 1) return;
+        if (s == m.test_stall - 1) {
+          finish();
+          return;
+        }
         const int st = gs % STAGES, use = gs / STAGES;
         if (use > 0 && !mbar_wait_ns(&empty[st], (use - 1) & 1, wait_ns)) {
           if (lane == 0) set_status(status, PIE_STATUS_TIMEOUT);
+          finish();
           return;
         }
         const int sb = r.kb + s * kStageSlots;
@@ -244,6 +294,7 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
         if (s + 1 < r.nstages) pid = page_of(s + 1);
       }
     }
+    finish();
     return;
   }
 
@@ -269,7 +320,22 @@ __global__ void __launch_bounds__(dm::THREADS, 3) attend_decode_mma_kernel(
   // (the other warps' waits end too, bounded), so the CTA ends; the status
   // word says the outputs are not valid.
   bool dead = false;
-  for (int idx = first; idx < last; ++idx) {
+  for (int k = 0;; ++k) {
+    // the item the producer handed over, decided once for all compute warps
+    if (warp == 0) {
+      const int q = k & 1;
+      const bool ok = mbar_wait_ns(&item_full[q], (k >> 1) & 1, wait_ns);
+      int v = ok ? qidx[q] : -2;
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (lane == 0) {
+        decision[k & 1] = v;
+        if (v != -2) mbar_arrive(&item_empty[q]);
+        if (v == -2) set_status(status, PIE_STATUS_TIMEOUT);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
+    const int idx = decision[k & 1];
+    if (idx < 0) break;
     const DecRange r = resolve(idx);
     if (r.skip) continue;
     const DecItem& it = r.it;
@@ -506,8 +572,11 @@ static cudaError_t launch_nq(const pie_fwd_plan_t& p, const void* q_rot,
   if (e != cudaSuccess) return e;
   DevMeta m = p.dev;
   test_wait_hook(&m.test_stall, &m.test_wait_us);
+  // a plan's work counter: a persistent grid of three CTAs per SM; without
+  // one (the no-allocation decode, the decode loop), fixed runs of items
   const int per = p.dec_items_per_cta > 0 ? p.dec_items_per_cta : 1;
-  const int grid = (p.num_dec_items + per - 1) / per;
+  const int grid = p.dev.dec_work ? std::min(p.num_dec_items, 3 * std::max(1, p.dev.num_sms))
+                                  : (p.num_dec_items + per - 1) / per;
   return launch_dependent(attend_decode_mma_kernel<NQ>, dim3(grid), dim3(dm::THREADS),
                           dm::SMEM, s, true, m, p.desc.num_q_heads, p.desc.num_kv_heads, p.G,
                           p.desc.page_size, p.desc.sm_scale * dm::kLog2e,

@@ -30,11 +30,12 @@ struct alignas(16) DecItem {
 // streaming; one wave, three or five measured slower), where a tensor-core
 // unit splits for one wave of one.
 constexpr int kDecListWaves = 6;
-// Consecutive items one CTA of the tensor-core split-KV kernel walks, so that
-// an item's start-up runs under the one before: two for the short items of list
-// passes (masked decode 3-5 % faster); one for plain passes, whose longer items
-// gain less than a longer last wave costs (two: the decode batch 3.5 % slower).
-constexpr int kDecItemsPerCta = 1;
+// The tensor-core split-KV kernel runs an item's start-up under the item
+// before.  Plain passes: a persistent grid takes items from a counter (the
+// decode batch 3.5 % faster than one item per CTA; fixed runs of two items
+// lengthen its last wave and were 3.5 % slower).  List passes: fixed runs of
+// two consecutive items per CTA (masked decode 3-5 % faster than one; the
+// counter gave the same kernel times and slower calls).
 constexpr int kDecListItemsPerCta = 2;
 
 // How the combine step finds the partials of a row block (the rows one work
@@ -138,6 +139,9 @@ struct DevMeta {
   int32_t* list_len;                // [num_mblocks] entries of each list (scratch)
   int32_t* list_mode;               // [num_mblocks] 1: the list is page-granular (scratch)
   int32_t* mask_tiles;              // [1] KV tiles of all masked row blocks' lists (scratch)
+  int32_t* dec_work;                // [2] the split-KV items handed out and the CTAs done
+                                    //   (zero between launches), or NULL: each CTA walks
+                                    //   its fixed run of items
   int32_t num_sms;                  // SMs the masked units' chunks are sized for
   int32_t num_pool_pages;           // page ids at or past it are skipped (PIE_STATUS_BOUNDS)
   int32_t test_stall;               // test hook: 0 none; s + 1: the split-KV producer stops

@@ -462,7 +462,7 @@ struct Layout {
       row_lane, mask_word_indptr, readout, ro_indptr, ro_idx, rope_freq, dec, tc, comb, mblocks,
       row_block;
   size_t copy_bytes;  // everything above
-  size_t part_o, part_ml, list, lrow, cmask, list_len, list_mode, mask_tiles;
+  size_t part_o, part_ml, list, lrow, cmask, list_len, list_mode, mask_tiles, dec_work;
   size_t total;
 };
 
@@ -495,6 +495,9 @@ static Layout make_layout(const pie_fwd_desc& D, const HostPlan& H) {
   Y.comb = take(sizeof(CombEntry) * H.comb.size());
   Y.row_block = take(sizeof(int32_t) * H.row_block.size());
   Y.mblocks = take(sizeof(MaskBlock) * H.mblocks.size());
+  // the split-KV kernel's work counter and finished-CTA count (zero from the
+  // upload; the kernel sets them back to zero when it ends)
+  Y.dec_work = take(H.dec.empty() ? 0 : 2 * sizeof(int32_t));
   Y.copy_bytes = o;
   Y.part_o = take(sizeof(float) * static_cast<size_t>(H.num_part_slots) * D.head_dim);
   Y.part_ml = take(sizeof(float2) * static_cast<size_t>(H.num_part_slots));
@@ -639,7 +642,7 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   p->tc_nt = H.tc_nt;
   p->num_mblocks = static_cast<int32_t>(H.mblocks.size());
   p->dec_lists = H.dec_lists;
-  p->dec_items_per_cta = H.dec_lists ? kDecListItemsPerCta : kDecItemsPerCta;
+  p->dec_items_per_cta = H.dec_lists ? kDecListItemsPerCta : 1;
   p->mblock_max_nw = H.mblock_max_nw;
   p->mblock_max_rows = H.mblock_max_rows;
   p->num_part_slots = H.num_part_slots;
@@ -673,6 +676,10 @@ int pie_fwd_plan(const pie_fwd_desc* desc, const pie_fwd_meta* meta, void* dev_w
   dm.list_len = reinterpret_cast<int32_t*>(w + Y.list_len);
   dm.list_mode = reinterpret_cast<int32_t*>(w + Y.list_mode);
   dm.mask_tiles = reinterpret_cast<int32_t*>(w + Y.mask_tiles);
+  // plain passes: a persistent grid takes the split-KV items from the counter;
+  // list passes: fixed runs of kDecListItemsPerCta items per CTA
+  dm.dec_work = (H.dec.empty() || H.dec_lists) ? nullptr
+                                                : reinterpret_cast<int32_t*>(w + Y.dec_work);
   dm.num_sms = H.sms;
   dm.num_pool_pages = M.num_pool_pages;
   p->staging = blk;
