@@ -183,7 +183,11 @@ int pie_fwd_append_kv(const pie_fwd_plan_t* plan, const void* q, const void* k, 
  * NULL (every row's output); lse_all: device float [N,Hq] or NULL.
  * The pools are only read.  Precondition: every slot below kv_len holds
  * finite K and V (masked-out slots included); slots at or past kv_len may
- * hold anything.  status: device uint32 or NULL (PIE_STATUS_TIMEOUT). */
+ * hold anything.  status: device uint32 or NULL (PIE_STATUS_TIMEOUT).
+ * Calls on one plan share its workspace (the split partials, and the work
+ * counter from which the split-KV kernel's persistent grid takes its items):
+ * queue them one after another (one per layer, on one stream or ordered by
+ * events), never concurrently. */
 int pie_fwd_attend(const pie_fwd_plan_t* plan, const void* q_rot, const void* k_pool,
                    const void* v_pool, const uint32_t* mask_words, void* out_readout,
                    float* lse_readout, void* out_all, float* lse_all, uint32_t* status,
