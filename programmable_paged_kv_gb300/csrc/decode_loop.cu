@@ -37,7 +37,7 @@ constexpr int kLoopChunk = 512;  // slots per split-KV item (a multiple of kStag
 
 struct LoopLayout {
   size_t row_indptr, row_lane, positions, slots, kv_len, fold_mode, fold_count, readout,
-      ro_indptr, ro_idx, rope_freq, dec, comb, row_block, part_ml, part_o, total;
+      ro_indptr, ro_idx, rope_freq, dec, comb, row_block, work, part_ml, part_o, total;
 };
 
 static LoopLayout loop_layout(int L, int Hkv, int MC, int nq, int d) {
@@ -64,6 +64,7 @@ static LoopLayout loop_layout(int L, int Hkv, int MC, int nq, int d) {
   Y.dec = take(sizeof(DecItem) * items);
   Y.comb = take(sizeof(CombEntry) * Ls * Hkv);
   Y.row_block = take(4 * Ls);
+  Y.work = take(2 * sizeof(int32_t));  // the split-KV kernel's work counter and CTAs done
   Y.part_ml = take(sizeof(float2) * items * nq);
   Y.part_o = take(sizeof(float) * items * nq * d);
   Y.total = o;
@@ -75,6 +76,10 @@ static LoopLayout loop_layout(int L, int Hkv, int MC, int nq, int d) {
 // (double, rounded once to float).
 __global__ void loop_init_kernel(DevMeta m, int L, int Hkv, int MC, int nq, int d, float base) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i == 0) {  // the persistent split-KV grid's counter starts from zero
+    m.dec_work[0] = 0;
+    m.dec_work[1] = 0;
+  }
   if (i <= L) {
     const_cast<int32_t*>(m.row_indptr)[i] = i;
     const_cast<int32_t*>(m.ro_indptr)[i] = i;
@@ -214,6 +219,9 @@ extern "C" int pie_fwd_decode_loop(const pie_fwd_desc* desc, int32_t num_lanes, 
   m.page_indptr = page_indptr;
   m.page_ids = page_ids;
   m.num_pool_pages = num_pool_pages;
+  // each step's split-KV items go to a persistent grid sized for this device
+  m.dec_work = reinterpret_cast<int32_t*>(w + Y.work);
+  m.num_sms = device_sm_count();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int init_n = std::max(L * Hkv, std::max(L + 1, d / 2));
